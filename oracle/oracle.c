@@ -1,0 +1,238 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for exact scaled-dot-product attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or load this
+ * file; only the tests, the smoke check and the benchmark's CPU-baseline leg use it.
+ * It shares no code, header or constant with the CUDA library.
+ *
+ * What it computes (the plain definition that the tiled GPU method reaches exactly,
+ * up to rounding order):
+ *
+ *   "FlashAttention principles and engineering practice", section 2.1 (memory access):
+ *   the standard implementation forms attn = (q k^T) * scale, applies softmax over the
+ *   last dimension and multiplies by v.  Per (b,h) head, with Q,K,V of shape [L,D]:
+ *
+ *     S   = scale * Q K^T                      (S_ij = -inf for j > i when causal)
+ *     m_i = max_j S_ij
+ *     P   = exp(S - m) / rowsum(exp(S - m))    (materialised, fp64)
+ *     O   = P V
+ *     LSE_i = m_i + ln sum_j exp(S_ij - m_i)
+ *
+ *   "FlashAttention data-flow optimisation: MI50 memory and bandwidth bottlenecks",
+ *   section 2.2, third layer (gradient re-computation): only the per-row softmax
+ *   statistics are kept for the backward pass.  The backward formulas are not printed on
+ *   the pages; they are the textbook softmax-Jacobian derivation:
+ *
+ *     dV = P^T dO
+ *     dP = dO V^T
+ *     Delta_i = sum_j P_ij dP_ij                (equals sum_d dO_id O_id)
+ *     dS = P o (dP - Delta 1^T)
+ *     dQ = scale * dS K
+ *     dK = scale * dS^T Q
+ *
+ * Masked entries (causal, j > i) have P_ij = exp(-inf) = 0 exactly, so they are simply
+ * not visited: every sum below runs over the visible keys j < n_i, n_i = i+1 (causal)
+ * or L.  Rows of S and P are materialised one row block at a time; a block holds every
+ * row of the head whenever R*L doubles fit the block budget, so for test sizes the whole
+ * L x L matrix is materialised at once.
+ *
+ * Layout: every tensor is contiguous [B,H,L,D] (LSE, Delta: [B,H,L]) in fp64.
+ * Parallelism: OpenMP over rows (and over key columns for dK/dV) inside one head.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARG 1
+#define ORACLE_NO_MEMORY 2
+
+/* Default cap on doubles held by one materialised block of S/P (2^25 = 256 MiB). */
+#define ORACLE_DEFAULT_BLOCK_DOUBLES (1L << 25)
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+static long visible_keys(long i, long L, int causal) { return causal ? i + 1 : L; }
+
+/* Row i of S (scaled logits), written into s[0..n), and returns n. */
+static long logits_row(const double* Q, const double* K, long i, long L, long D, double scale,
+                       int causal, double* s) {
+    long n = visible_keys(i, L, causal);
+    const double* q = Q + i * D;
+    for (long j = 0; j < n; ++j) {
+        const double* k = K + j * D;
+        double dot = 0.0;
+        for (long d = 0; d < D; ++d) dot += q[d] * k[d];
+        s[j] = scale * dot;
+    }
+    return n;
+}
+
+/* Turns s[0..n) into the softmax row P in place; returns LSE = m + ln(sum exp(s - m)). */
+static double softmax_row(double* s, long n) {
+    double m = -INFINITY;
+    for (long j = 0; j < n; ++j)
+        if (s[j] > m) m = s[j];
+    double sum = 0.0;
+    for (long j = 0; j < n; ++j) {
+        s[j] = exp(s[j] - m);
+        sum += s[j];
+    }
+    for (long j = 0; j < n; ++j) s[j] /= sum;
+    return m + log(sum);
+}
+
+static long block_rows(long L, long block_doubles) {
+    if (block_doubles <= 0) block_doubles = ORACLE_DEFAULT_BLOCK_DOUBLES;
+    long r = block_doubles / (L > 0 ? L : 1);
+    if (r < 1) r = 1;
+    if (r > L) r = L;
+    return r;
+}
+
+/* Forward pass for one head. */
+static int fwd_head(const double* Q, const double* K, const double* V, double* O, double* lse,
+                    long L, long D, double scale, int causal, long block_doubles) {
+    long R = block_rows(L, block_doubles);
+    double* P = (double*)malloc(sizeof(double) * (size_t)R * (size_t)L);
+    if (!P) return ORACLE_NO_MEMORY;
+    for (long i0 = 0; i0 < L; i0 += R) {
+        long i1 = i0 + R < L ? i0 + R : L;
+#pragma omp parallel for schedule(dynamic, 4)
+        for (long i = i0; i < i1; ++i) {
+            double* p = P + (i - i0) * L;
+            long n = logits_row(Q, K, i, L, D, scale, causal, p);
+            lse[i] = softmax_row(p, n);
+            double* o = O + i * D;
+            for (long d = 0; d < D; ++d) o[d] = 0.0;
+            for (long j = 0; j < n; ++j) {
+                const double* v = V + j * D;
+                for (long d = 0; d < D; ++d) o[d] += p[j] * v[d];
+            }
+        }
+    }
+    free(P);
+    return ORACLE_OK;
+}
+
+/* Backward pass for one head (P recomputed from the definition, nothing cached). */
+static int bwd_head(const double* Q, const double* K, const double* V, const double* dO,
+                    double* dQ, double* dK, double* dV, double* delta, long L, long D,
+                    double scale, int causal, long block_doubles) {
+    long R = block_rows(L, block_doubles / 2);
+    double* P = (double*)malloc(sizeof(double) * (size_t)R * (size_t)L);
+    double* dS = (double*)malloc(sizeof(double) * (size_t)R * (size_t)L);
+    if (!P || !dS) {
+        free(P);
+        free(dS);
+        return ORACLE_NO_MEMORY;
+    }
+    memset(dK, 0, sizeof(double) * (size_t)L * (size_t)D);
+    memset(dV, 0, sizeof(double) * (size_t)L * (size_t)D);
+    for (long i0 = 0; i0 < L; i0 += R) {
+        long i1 = i0 + R < L ? i0 + R : L;
+        /* Rows: P, dP, Delta, dS and dQ. */
+#pragma omp parallel for schedule(dynamic, 4)
+        for (long i = i0; i < i1; ++i) {
+            double* p = P + (i - i0) * L;
+            double* ds = dS + (i - i0) * L;
+            long n = logits_row(Q, K, i, L, D, scale, causal, p);
+            (void)softmax_row(p, n);
+            const double* g = dO + i * D;
+            double dlt = 0.0;
+            for (long j = 0; j < n; ++j) {
+                const double* v = V + j * D;
+                double dp = 0.0;
+                for (long d = 0; d < D; ++d) dp += g[d] * v[d];
+                ds[j] = dp; /* dP_ij for now */
+                dlt += p[j] * dp;
+            }
+            delta[i] = dlt;
+            for (long j = 0; j < n; ++j) ds[j] = p[j] * (ds[j] - dlt);
+            double* dq = dQ + i * D;
+            for (long d = 0; d < D; ++d) dq[d] = 0.0;
+            for (long j = 0; j < n; ++j) {
+                const double* k = K + j * D;
+                for (long d = 0; d < D; ++d) dq[d] += ds[j] * k[d];
+            }
+            for (long d = 0; d < D; ++d) dq[d] *= scale;
+        }
+        /* Columns: dV_j += sum_i P_ij dO_i and dK_j += scale * sum_i dS_ij Q_i over this block. */
+#pragma omp parallel for schedule(dynamic, 4)
+        for (long j = 0; j < L; ++j) {
+            double* dv = dV + j * D;
+            double* dk = dK + j * D;
+            for (long i = i0; i < i1; ++i) {
+                if (causal && j > i) continue; /* P_ij = 0 and dS_ij = 0 */
+                double pij = P[(i - i0) * L + j];
+                double dsij = dS[(i - i0) * L + j];
+                const double* g = dO + i * D;
+                const double* q = Q + i * D;
+                for (long d = 0; d < D; ++d) {
+                    dv[d] += pij * g[d];
+                    dk[d] += scale * dsij * q[d];
+                }
+            }
+        }
+    }
+    free(P);
+    free(dS);
+    return ORACLE_OK;
+}
+
+static int bad_shape(long B, long H, long L, long D) { return B < 0 || H < 0 || L < 0 || D < 1; }
+
+/*
+ * Forward over all heads.  q,k,v: [B,H,L,D]; o: [B,H,L,D]; lse: [B,H,L].
+ * block_doubles caps the doubles of one materialised S/P block (<= 0: default).
+ */
+int oracle_fwd_f64(const double* q, const double* k, const double* v, double* o, double* lse,
+                   long B, long H, long L, long D, double scale, int causal, long block_doubles) {
+    if (bad_shape(B, H, L, D)) return ORACLE_BAD_ARG;
+    for (long bh = 0; bh < B * H; ++bh) {
+        size_t off = (size_t)bh * (size_t)L * (size_t)D;
+        int rc = fwd_head(q + off, k + off, v + off, o + off, lse + (size_t)bh * (size_t)L, L, D,
+                          scale, causal, block_doubles);
+        if (rc) return rc;
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Backward over all heads.  Inputs q,k,v,dO: [B,H,L,D]; outputs dq,dk,dv: [B,H,L,D] and
+ * delta: [B,H,L] (Delta_i = sum_j P_ij dP_ij).
+ */
+int oracle_bwd_f64(const double* q, const double* k, const double* v, const double* dO,
+                   double* dq, double* dk, double* dv, double* delta, long B, long H, long L,
+                   long D, double scale, int causal, long block_doubles) {
+    if (bad_shape(B, H, L, D)) return ORACLE_BAD_ARG;
+    for (long bh = 0; bh < B * H; ++bh) {
+        size_t off = (size_t)bh * (size_t)L * (size_t)D;
+        int rc = bwd_head(q + off, k + off, v + off, dO + off, dq + off, dk + off, dv + off,
+                          delta + (size_t)bh * (size_t)L, L, D, scale, causal, block_doubles);
+        if (rc) return rc;
+    }
+    return ORACLE_OK;
+}
+
+/* The full probability matrix P [L,L] of one head (masked entries are 0). */
+int oracle_probs_f64(const double* q, const double* k, double* p, long L, long D, double scale,
+                     int causal) {
+    if (bad_shape(1, 1, L, D)) return ORACLE_BAD_ARG;
+    for (long i = 0; i < L; ++i) {
+        double* row = p + i * L;
+        long n = logits_row(q, k, i, L, D, scale, causal, row);
+        (void)softmax_row(row, n);
+        for (long j = n; j < L; ++j) row[j] = 0.0;
+    }
+    return ORACLE_OK;
+}
