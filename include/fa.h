@@ -1,0 +1,118 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library (libfa.so).
+ *
+ * Operation.  Per (b,h) head, with Q, K, V, O of shape [L, D]:
+ *     S = scale * Q K^T   (S_ij = -inf for j > i when causal)
+ *     P = softmax(S) row by row,  O = P V,  LSE_i = log(sum_j exp(S_ij))
+ * computed the tiled, streaming way: Q in 128-row tiles kept on chip, K/V streamed in 128-key
+ * tiles, a running row max and row sum with the partial output rescaled as tiles arrive, and
+ * only O and the per-row log-sum-exp written ("FlashAttention data-flow optimisation: MI50
+ * memory and bandwidth bottlenecks", section 2.2, first and second layers;
+ * "FlashAttention principles and engineering practice", section 2.1 for the plain
+ * definition attn = softmax(q k^T * scale) v).  The backward pass recomputes P from the saved
+ * LSE instead of storing the L x L matrix (data-flow page, section 2.2, third layer).
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are DEVICE pointers to contiguous row-major [B, H, L, D] arrays (LSE: [B, H, L]
+ *    fp32), each 16-byte aligned.  q, k, v, o, dO, dq, dk, dv all have the dtype `dtype`.
+ *  - Supported: D in {64, 128}; B, H, L >= 0 (an empty problem returns FA_OK and launches
+ *    nothing); causal in {0, 1} (query i sees key j iff j <= i); scale finite.
+ *  - The caller allocates and owns every buffer, including the backward workspace; the
+ *    library never allocates or frees device memory in these calls.
+ *  - Calls are asynchronous: they validate, enqueue on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) and return without synchronising.  Argument errors are reported
+ *    before anything is enqueued and leave every output untouched.  A non-OK status from a
+ *    launch leaves outputs undefined.  Kernels never spin without bound: a wait that exceeds
+ *    its time limit records FA_ERR_TIMEOUT in a device status word, read by
+ *    fa_get_device_status().
+ *  - Outputs must not overlap inputs.  fa_bwd overwrites dq, dk, dv (it does not accumulate).
+ *  - The library keeps no per-call state; it caches only the driver entry point used to
+ *    build TMA descriptors and, per device, the address of its status word.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* null/misaligned/overlapping pointer, bad size, bad flag */
+    FA_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels implement (e.g. D) */
+    FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a launch failed */
+    FA_ERR_TIMEOUT = 4      /* a device-side bounded wait ran out (see fa_get_device_status) */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_FP16 = 1 } fa_dtype;
+
+/*
+ * Forward.  Writes o [B,H,L,D] (dtype) and lse [B,H,L] (fp32, natural log).
+ * Data-flow page, section 2.2 (tiling, streaming softmax, statistics kept for backward).
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int L, int D, float scale, int causal, int dtype, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for this shape: two fp32 vectors per head padded to
+ * a whole number of 128-row tiles (LSE * log2(e) and Delta = rowsum(dO * O)).
+ * Returns 0 for an empty problem or invalid sizes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int L, int D);
+
+/*
+ * Backward.  Given q, k, v, the forward's o and lse, and the output gradient dout, writes
+ * dq, dk, dv [B,H,L,D] (dtype).  `workspace` is a device buffer of at least
+ * fa_bwd_workspace_bytes(B,H,L,D) bytes, 16-byte aligned, owned by the caller; its contents
+ * on entry do not matter.  Three kernels are enqueued on `stream`: the Delta/LSE preprocess,
+ * the dK/dV pass (one CTA per key tile) and the dQ pass (one CTA per query tile).
+ * Data-flow page, section 2.2, third layer (recompute P from the saved statistics).
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                 size_t workspace_bytes, int B, int H, int L, int D, float scale, int causal,
+                 int dtype, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status word.  Returns
+ * FA_OK, FA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last call, or
+ * FA_ERR_CUDA if synchronisation itself failed.
+ */
+fa_status fa_get_device_status(void* stream);
+
+/* Time limit of every device-side wait, in nanoseconds (default 4e9).  0 restores the
+ * default.  Applies to launches made after the call; returns FA_OK. */
+fa_status fa_set_wait_timeout_ns(uint64_t timeout_ns);
+
+/*
+ * Self-test of the bounded-wait machinery: enqueues one tiny kernel that waits on a barrier
+ * nothing will ever complete, with the given limit.  The kernel gives up, records
+ * FA_ERR_TIMEOUT in the status word and returns, so the following fa_get_device_status()
+ * reports FA_ERR_TIMEOUT and the context stays usable.
+ */
+fa_status fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
+
+/*
+ * Kernel timing trace (the CUDA-event measurement the TFLOP/s figures rest on, per kernel).
+ * Arms the next fa_fwd / fa_bwd call made by this host thread: the i-th kernel that call
+ * enqueues is bracketed by cudaEventRecord(events[2*i], stream) and
+ * cudaEventRecord(events[2*i+1], stream).  `events` holds n_pairs pairs of cudaEvent_t created
+ * by the caller (with timing enabled); kernels beyond n_pairs are not traced.  The next call
+ * consumes the arming.  fa_fwd enqueues 1 kernel, fa_bwd 3 (preprocess, dK/dV, dQ).
+ */
+fa_status fa_trace_next_call(void* const* events, int n_pairs);
+
+/* Number of kernels this library has enqueued in this process so far. */
+uint64_t fa_launch_count(void);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */

@@ -1,0 +1,107 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path, run the oracle, compare.
+
+Tolerances are the ones the method's target states for 16-bit inputs with fp32 accumulation:
+O max-abs <= 1e-2 and mean-abs <= 1e-3 (N(0,1) inputs), LSE max-abs <= 1e-3, and dQ/dK/dV
+relative Frobenius error <= 2e-2.
+
+O is returned in the 16-bit input dtype, so even the exact result stored in that dtype is off
+by up to half an ulp of the format (0.0078 for |O| in [2,4) in bf16).  The O bounds therefore
+apply to the error beyond that unavoidable rounding: per element,
+    excess = max(0, |O_gpu - O_ref| - ulp16(O_ref) / 2),
+and max(excess) <= 1e-2, mean(excess) <= 1e-3.  The raw errors are reported alongside.
+"""
+import numpy as np
+import pytest
+import torch
+
+import tiled_attention_08_gb300 as fa
+import workloads
+
+O_MAX_ABS = 1e-2
+O_MEAN_ABS = 1e-3
+LSE_MAX_ABS = 1e-3
+GRAD_REL_FRO = 2e-2
+
+
+def require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tiled_attention_08_gb300 import build
+    build.build()
+    fa.load_library()
+
+
+def sample_heads(B, H, n_random=2, seed=1234):
+    """All heads when there are few, else first, last and n_random seeded ones."""
+    if B * H <= 4:
+        return [(b, h) for b in range(B) for h in range(H)]
+    rng = np.random.default_rng(seed)
+    picks = {(0, 0), (B - 1, H - 1)}
+    while len(picks) < 2 + n_random:
+        picks.add((int(rng.integers(B)), int(rng.integers(H))))
+    return sorted(picks)
+
+
+def run_gpu(w, inp, backward=True):
+    dev = torch.device("cuda:0")
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    o, lse = fa.forward(q, k, v, w.causal, w.scale)
+    out = {"o": o, "lse": lse}
+    if backward:
+        do = inp["do"].to(dev)
+        dq, dk, dv = fa.backward(q, k, v, o, lse, do, w.causal, w.scale)
+        out.update(dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    st = fa.fa_get_device_status(torch.cuda.current_stream().cuda_stream)
+    assert st == fa.FA_OK, f"device status {fa.fa_status_string(st)}"
+    return out
+
+
+def half_ulp16(ref, dtype):
+    """Half the spacing of the 16-bit format at |ref| (normal range; subnormals floored)."""
+    mant, emin = (7, -126) if dtype == torch.bfloat16 else (10, -14)
+    a = np.maximum(np.abs(ref), 2.0 ** emin)
+    e = np.maximum(np.floor(np.log2(a)), emin)
+    return 0.5 * 2.0 ** (e - mant)
+
+
+def o_errors(o, o_ref, dtype):
+    if not o.size:
+        return {"o_max": 0.0, "o_mean": 0.0, "o_raw_max": 0.0, "o_raw_mean": 0.0}
+    raw = np.abs(o - o_ref)
+    excess = np.maximum(0.0, raw - half_ulp16(o_ref, dtype))
+    return {"o_max": float(excess.max()), "o_mean": float(excess.mean()),
+            "o_raw_max": float(raw.max()), "o_raw_mean": float(raw.mean())}
+
+
+def f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def check_head(oracle, w, inp, out, b, h, backward=True):
+    """Compares one (b,h) head of the GPU result with the oracle; returns the error summary."""
+    q, k, v = (f64(inp[n][b, h]) for n in ("q", "k", "v"))
+    o_ref, lse_ref = oracle.forward(q, k, v, w.scale, w.causal)
+    o = f64(out["o"][b, h])
+    lse = f64(out["lse"][b, h])
+    err = o_errors(o, o_ref, w.dtype)
+    err["lse_max"] = float(np.max(np.abs(lse - lse_ref))) if lse.size else 0.0
+    assert err["o_max"] <= O_MAX_ABS, (b, h, err)
+    assert err["o_mean"] <= O_MEAN_ABS, (b, h, err)
+    assert err["lse_max"] <= LSE_MAX_ABS, (b, h, err)
+    if backward:
+        do = f64(inp["do"][b, h])
+        dq_ref, dk_ref, dv_ref, _ = oracle.backward(q, k, v, do, w.scale, w.causal)
+        for name, ref in (("dq", dq_ref), ("dk", dk_ref), ("dv", dv_ref)):
+            got = f64(out[name][b, h])
+            ref_norm = float(np.linalg.norm(ref))
+            if ref_norm < 1e-9:
+                # The exact gradient vanishes (e.g. dQ and dK with a single visible key): a
+                # relative error is undefined there, so bound the absolute error instead.
+                err[name + "_abs"] = float(np.max(np.abs(got))) if got.size else 0.0
+                assert err[name + "_abs"] <= O_MAX_ABS, (b, h, name, err)
+                continue
+            rel = float(np.linalg.norm(got - ref) / ref_norm)
+            err[name + "_rel"] = rel
+            assert rel <= GRAD_REL_FRO, (b, h, name, err)
+    return err

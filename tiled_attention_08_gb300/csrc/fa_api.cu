@@ -1,0 +1,328 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument checks, TMA descriptors, launches,
+// and the per-device status word that bounded device waits report into.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+__device__ int g_status_word;  // first device-side error since the last fa_get_device_status
+
+std::atomic<uint64_t> g_timeout_ns{4000000000ull};
+constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;
+
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    return g_encode;
+}
+
+// Device address of the status word of the current device (looked up once per device).
+int* status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int*>(ptr);
+    }
+    return g_status_ptr[dev];
+}
+
+// [BH, L, D] 16-bit tensor viewed as 3-D {D, L, BH}; box = 64 elements x 128 rows x 1, with
+// the 128-byte swizzle the tcgen05 descriptors expect.  Rows past L read as zeros.
+bool make_map(CUtensorMap* m, const void* ptr, int BH, int L, int D, bool bf16) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)L * D * 2};
+    cuuint32_t box[3] = {(cuuint32_t)kChunkElems, (cuuint32_t)kTileRows, 1};
+    cuuint32_t elem[3] = {1, 1, 1};
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     3, const_cast<void*>(ptr), dims, strides, box, elem,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Per-thread trace arming (fa_trace_next_call) and the process-wide launch counter.
+constexpr int kMaxTracePairs = 8;
+thread_local int t_trace_pairs = 0;
+thread_local cudaEvent_t t_trace_events[2 * kMaxTracePairs];
+std::atomic<uint64_t> g_launches{0};
+
+// Enqueues one kernel through `launch`, bracketed by the armed trace events (if any).
+template <typename F>
+cudaError_t traced_launch(int index, cudaStream_t s, F&& launch) {
+    const bool traced = index < t_trace_pairs;
+    if (traced && cudaEventRecord(t_trace_events[2 * index], s) != cudaSuccess)
+        return cudaErrorInvalidValue;
+    cudaError_t e = launch();
+    if (e != cudaSuccess) return e;
+    g_launches.fetch_add(1);
+    if (traced && cudaEventRecord(t_trace_events[2 * index + 1], s) != cudaSuccess)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+// Consumes the trace arming at the end of a public call, whatever its outcome.
+struct TraceDisarm {
+    ~TraceDisarm() { t_trace_pairs = 0; }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+Range range(const void* p, size_t bytes) {
+    uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return {a, a + bytes};
+}
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+struct Shape {
+    int BH = 0, L = 0, D = 0, n_tiles = 0, Lpad = 0;
+    size_t tensor_bytes = 0, row_bytes = 0;
+    bool empty = true;
+};
+
+// Checks sizes and flags shared by both passes.  Does not touch the GPU.
+fa_status check_shape(int B, int H, int L, int D, float scale, int causal, int dtype, Shape* sh) {
+    if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || L < 0 || D <= 0) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    const long long bh = (long long)B * (long long)H;
+    const long long tiles = ((long long)L + kTileRows - 1) / kTileRows;
+    if (bh > 0x7fffffffLL || tiles * bh > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    sh->BH = (int)bh;
+    sh->L = L;
+    sh->D = D;
+    sh->n_tiles = (int)tiles;
+    sh->Lpad = (int)(tiles * kTileRows);
+    sh->tensor_bytes = (size_t)bh * (size_t)L * (size_t)D * 2u;
+    sh->row_bytes = (size_t)bh * (size_t)L * 4u;
+    sh->empty = (bh == 0 || L == 0);
+    return FA_OK;
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s);
+
+namespace {
+__global__ void fa_wait_selftest_kernel(int* status, uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bar, 1);  // nothing ever arrives on it
+        mbar_fence_init();
+    }
+    __syncthreads();
+    const bool ok = wait_bounded(&bar, 0, &abort_flag, timeout_ns);
+    if (!ok && threadIdx.x == 0) record_timeout(status, &abort_flag);
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s) {
+    fa_wait_selftest_kernel<<<1, 32, 0, s>>>(status, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char* fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+        default: return "FA_ERR_UNKNOWN";
+    }
+}
+
+fa_status fa_set_wait_timeout_ns(uint64_t timeout_ns) {
+    g_timeout_ns.store(timeout_ns ? timeout_ns : kDefaultTimeoutNs);
+    return FA_OK;
+}
+
+fa_status fa_trace_next_call(void* const* events, int n_pairs) {
+    if (n_pairs < 0 || n_pairs > kMaxTracePairs || (n_pairs > 0 && !events))
+        return FA_ERR_INVALID_ARG;
+    for (int i = 0; i < 2 * n_pairs; ++i) {
+        if (!events[i]) return FA_ERR_INVALID_ARG;
+        t_trace_events[i] = static_cast<cudaEvent_t>(events[i]);
+    }
+    t_trace_pairs = n_pairs;
+    return FA_OK;
+}
+
+uint64_t fa_launch_count(void) { return g_launches.load(); }
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int L, int D, float scale, int causal, int dtype, void* stream) {
+    TraceDisarm disarm;
+    Shape sh;
+    fa_status st = check_shape(B, H, L, D, scale, causal, dtype, &sh);
+    if (st != FA_OK) return st;
+    if (sh.empty) return FA_OK;
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_INVALID_ARG;
+    const Range rq = range(q, sh.tensor_bytes), rk = range(k, sh.tensor_bytes),
+                rv = range(v, sh.tensor_bytes), ro = range(o, sh.tensor_bytes),
+                rl = range(lse, sh.row_bytes);
+    for (Range out : {ro, rl})
+        for (Range in : {rq, rk, rv})
+            if (overlap(out, in)) return FA_ERR_INVALID_ARG;
+    if (overlap(ro, rl)) return FA_ERR_INVALID_ARG;
+
+    FwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    const bool bf16 = dtype == FA_BF16;
+    if (!make_map(&p.tm_q, q, sh.BH, L, D, bf16) || !make_map(&p.tm_k, k, sh.BH, L, D, bf16) ||
+        !make_map(&p.tm_v, v, sh.BH, L, D, bf16))
+        return FA_ERR_CUDA;
+    p.o = o;
+    p.lse = lse;
+    p.L = L;
+    p.BH = sh.BH;
+    p.n_tiles = sh.n_tiles;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.status = status_ptr();
+    p.timeout_ns = g_timeout_ns.load();
+    if (!p.status) return FA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = traced_launch(0, s, [&] { return launch_fwd(p, D, bf16, causal != 0, s); });
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int L, int D) {
+    Shape sh;
+    if (check_shape(B, H, L, D, 1.0f, 0, FA_BF16, &sh) != FA_OK || sh.empty) return 0;
+    return 2u * (size_t)sh.BH * (size_t)sh.Lpad * 4u;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                 size_t workspace_bytes, int B, int H, int L, int D, float scale, int causal,
+                 int dtype, void* stream) {
+    TraceDisarm disarm;
+    Shape sh;
+    fa_status st = check_shape(B, H, L, D, scale, causal, dtype, &sh);
+    if (st != FA_OK) return st;
+    if (sh.empty) return FA_OK;
+    const size_t ws_need = 2u * (size_t)sh.BH * (size_t)sh.Lpad * 4u;
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
+        return FA_ERR_INVALID_ARG;
+    if (workspace_bytes < ws_need) return FA_ERR_INVALID_ARG;
+    const void* all[] = {q, k, v, o, dout, lse, dq, dk, dv, workspace};
+    for (const void* ptr : all)
+        if (!aligned16(ptr)) return FA_ERR_INVALID_ARG;
+    const size_t tb = sh.tensor_bytes;
+    const Range ins[] = {range(q, tb), range(k, tb), range(v, tb), range(o, tb), range(dout, tb),
+                         range(lse, sh.row_bytes)};
+    const Range outs[] = {range(dq, tb), range(dk, tb), range(dv, tb), range(workspace, ws_need)};
+    for (const Range& a : outs) {
+        for (const Range& b : ins)
+            if (overlap(a, b)) return FA_ERR_INVALID_ARG;
+        for (const Range& b : outs)
+            if (&a != &b && overlap(a, b)) return FA_ERR_INVALID_ARG;
+    }
+
+    const bool bf16 = dtype == FA_BF16;
+    BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!make_map(&p.tm_q, q, sh.BH, L, D, bf16) || !make_map(&p.tm_k, k, sh.BH, L, D, bf16) ||
+        !make_map(&p.tm_v, v, sh.BH, L, D, bf16) || !make_map(&p.tm_do, dout, sh.BH, L, D, bf16))
+        return FA_ERR_CUDA;
+    float* lse2_pad = static_cast<float*>(workspace);
+    float* delta_pad = lse2_pad + (size_t)sh.BH * sh.Lpad;
+    p.lse2_pad = lse2_pad;
+    p.delta_pad = delta_pad;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.L = L;
+    p.Lpad = sh.Lpad;
+    p.BH = sh.BH;
+    p.n_tiles = sh.n_tiles;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.status = status_ptr();
+    p.timeout_ns = g_timeout_ns.load();
+    if (!p.status) return FA_ERR_CUDA;
+
+    BwdPreParams pp;
+    pp.o = o;
+    pp.dout = dout;
+    pp.lse = lse;
+    pp.lse2_pad = lse2_pad;
+    pp.delta_pad = delta_pad;
+    pp.L = L;
+    pp.Lpad = sh.Lpad;
+    pp.BH = sh.BH;
+    pp.D = D;
+    pp.bf16 = bf16 ? 1 : 0;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (traced_launch(0, s, [&] { return launch_bwd_pre(pp, s); }) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (traced_launch(1, s, [&] { return launch_bwd_dkdv(p, D, bf16, causal != 0, s); }) !=
+        cudaSuccess)
+        return FA_ERR_CUDA;
+    if (traced_launch(2, s, [&] { return launch_bwd_dq(p, D, bf16, causal != 0, s); }) !=
+        cudaSuccess)
+        return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+fa_status fa_get_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    if (!status_ptr()) return FA_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+    if (word == 0) return FA_OK;
+    return word == (int)kDevTimeout ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
+}
+
+fa_status fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
+    int* sp = status_ptr();
+    if (!sp) return FA_ERR_CUDA;
+    if (launch_wait_selftest(sp, timeout_ns, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+}  // extern "C"

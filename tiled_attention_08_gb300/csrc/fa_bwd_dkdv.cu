@@ -1,0 +1,294 @@
+// fa_bwd_dkdv.cu -- attention backward, dK and dV: one CTA per (b*h, 128-key tile).
+//
+// Recompute-based backward ("FlashAttention data-flow optimisation: MI50 memory and bandwidth
+// bottlenecks", section 2.2, third layer): P is rebuilt tile by tile from Q, K and the saved
+// log-sum-exp instead of being stored.  For the CTA's key tile j and every query tile i that
+// can see it (i >= j under the causal mask):
+//   S^T  = K_j Q_i^T                      (tcgen05, both operands K-major in shared memory)
+//   dP^T = V_j dO_i^T
+//   P^T  = exp2(S^T * scale*log2e - LSE_i*log2e)        (per column: query)
+//   dS^T = P^T o (dP^T - Delta_i)
+//   dV_j += P^T dO_i,  dK_j += dS^T Q_i   (A operand = 16-bit P^T / dS^T written back to TMEM)
+// and at the end dK_j is multiplied by the softmax scale.
+//
+// CTA roles (192 threads): warps 0-3 elementwise (thread = key row = TMEM lane), warp 4 TMA
+// producer (K_j, V_j once; Q_i, dO_i, LSE_i, Delta_i per stage), warp 5 MMA issuer + TMEM owner.
+// TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D).
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+template <int D, bool BF16, bool CAUSAL>
+struct DkdvCfg {
+    static constexpr int kChunks = D / kChunkElems;
+    static constexpr int kTileBytes = kTileRows * D * 2;
+    static constexpr int kStages = (D == 128) ? 2 : 3;
+    static constexpr int kVecBytes = 2 * kTileRows * 4;  // LSE*log2e then Delta, fp32
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kTileBytes;
+    static constexpr int kOffQ = 2 * kTileBytes;
+    static constexpr int kOffDO = kOffQ + kStages * kTileBytes;
+    static constexpr int kOffVec = kOffDO + kStages * kTileBytes;
+    static constexpr int kSmemBytes = kOffVec + kStages * kVecBytes + 1024;
+    static constexpr int kThreads = 192;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kTmST = 0, kTmDPT = 128, kTmDV = 256, kTmDK = 256 + D;
+    static constexpr uint32_t kIdescS = idesc_f16(BF16, 128, 128, false, false);
+    static constexpr uint32_t kIdescG = idesc_f16(BF16, 128, D, false, true);
+};
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(192, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+    using C = DkdvCfg<D, BF16, CAUSAL>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    __shared__ uint64_t bar_kv, bar_qf[C::kStages], bar_qe[C::kStages], bar_sf, bar_pf, bar_done,
+        bar_fin;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int tile_id = blockIdx.x;
+    const int bh = tile_id % p.BH;
+    const int kt = tile_id / p.BH;  // key tile; low kt has the most query tiles under the mask
+    const int it0 = CAUSAL ? kt : 0;
+    const int n_it = p.n_tiles - it0;
+    volatile int* abort_v = &abort_flag;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bar_kv, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&bar_qf[s], 1);
+            mbar_init(&bar_qe[s], 1);
+        }
+        mbar_init(&bar_sf, 1);
+        mbar_init(&bar_pf, 128);
+        mbar_init(&bar_done, 1);
+        mbar_init(&bar_fin, 1);
+        mbar_fence_init();
+    }
+    if (warp == 5) tmem_alloc(&tmem_base_sh, C::kTmemCols);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = tmem_base_sh;
+
+    if (warp == 4) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tm_q);
+            tma_prefetch_desc(&p.tm_k);
+            tma_prefetch_desc(&p.tm_v);
+            tma_prefetch_desc(&p.tm_do);
+            mbar_arrive_expect_tx(&bar_kv, 2 * C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c) {
+                tma_load_3d(smem + C::kOffK + c * kChunkBytes, &p.tm_k, &bar_kv, c * kChunkElems,
+                            kt * kTileRows, bh);
+                tma_load_3d(smem + C::kOffV + c * kChunkBytes, &p.tm_v, &bar_kv, c * kChunkElems,
+                            kt * kTileRows, bh);
+            }
+            bool ok = true;
+            int issued = 0;
+            for (int t = 0; t < n_it; ++t) {
+                const int it = it0 + t;
+                const int st = t % C::kStages;
+                const uint32_t ph = (uint32_t)(t / C::kStages) & 1u;
+                if (t >= C::kStages && !wait_bounded(&bar_qe[st], ph ^ 1u, abort_v, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bar_qf[st], 2 * C::kTileBytes + C::kVecBytes);
+                for (int c = 0; c < C::kChunks; ++c) {
+                    tma_load_3d(smem + C::kOffQ + st * C::kTileBytes + c * kChunkBytes, &p.tm_q,
+                                &bar_qf[st], c * kChunkElems, it * kTileRows, bh);
+                    tma_load_3d(smem + C::kOffDO + st * C::kTileBytes + c * kChunkBytes, &p.tm_do,
+                                &bar_qf[st], c * kChunkElems, it * kTileRows, bh);
+                }
+                const size_t voff = (size_t)bh * p.Lpad + (size_t)it * kTileRows;
+                uint8_t* vec = smem + C::kOffVec + st * C::kVecBytes;
+                bulk_load(vec, p.lse2_pad + voff, kTileRows * 4, &bar_qf[st]);
+                bulk_load(vec + kTileRows * 4, p.delta_pad + voff, kTileRows * 4, &bar_qf[st]);
+                issued = t + 1;
+            }
+            if (!ok) record_timeout(p.status, abort_v);
+            wait_bounded(&bar_kv, 0, nullptr, p.timeout_ns);
+            for (int t = issued - 1; t >= 0 && t >= issued - C::kStages; --t)
+                wait_bounded(&bar_qf[t % C::kStages], (uint32_t)(t / C::kStages) & 1u, nullptr,
+                             p.timeout_ns);
+        }
+    } else if (warp == 5) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            const uint32_t k_base = smem_u32(smem + C::kOffK);
+            const uint32_t v_base = smem_u32(smem + C::kOffV);
+            bool ok = wait_bounded(&bar_kv, 0, abort_v, p.timeout_ns);
+            for (int t = 0; t < n_it && ok; ++t) {
+                const int st = t % C::kStages;
+                const uint32_t ph = (uint32_t)(t / C::kStages) & 1u;
+                if (!wait_bounded(&bar_qf[st], ph, abort_v, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t q_base = smem_u32(smem + C::kOffQ + st * C::kTileBytes);
+                const uint32_t do_base = smem_u32(smem + C::kOffDO + st * C::kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::kTmST, sdesc_kmajor_sw128(k_base + off),
+                           sdesc_kmajor_sw128(q_base + off), C::kIdescS, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::kTmDPT, sdesc_kmajor_sw128(v_base + off),
+                           sdesc_kmajor_sw128(do_base + off), C::kIdescS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar_sf);
+                if (!wait_bounded(&bar_pf, (uint32_t)t & 1u, abort_v, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < kTileRows / 16; ++kk) {
+                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+                    mma_ts(tmem + C::kTmDV, tmem + C::kTmST + kk * 8,
+                           sdesc_mnmajor_sw128(do_base + kk * 2048, kChunkBytes), C::kIdescG, acc);
+                    mma_ts(tmem + C::kTmDK, tmem + C::kTmDPT + kk * 8,
+                           sdesc_mnmajor_sw128(q_base + kk * 2048, kChunkBytes), C::kIdescG, acc);
+                }
+                mma_commit(&bar_qe[st]);
+            }
+            if (ok) mma_commit(&bar_done);
+            if (!ok) record_timeout(p.status, abort_v);
+            mma_commit(&bar_fin);
+            wait_bounded(&bar_fin, 0, nullptr, p.timeout_ns);
+        }
+    } else {
+        // ------------------------------ elementwise warps ------------------------------
+        const int row = warp * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const int key = kt * kTileRows + row;
+        bool ok = true;
+        for (int t = 0; t < n_it; ++t) {
+            const int it = it0 + t;
+            const int st = t % C::kStages;
+            const uint32_t ph = (uint32_t)(t / C::kStages) & 1u;
+            ok = wait_bounded(&bar_qf[st], ph, abort_v, p.timeout_ns) &&
+                 wait_bounded(&bar_sf, (uint32_t)t & 1u, abort_v, p.timeout_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const float* lse2v = reinterpret_cast<const float*>(smem + C::kOffVec + st * C::kVecBytes);
+            const float* dltv = lse2v + kTileRows;
+            const int q0 = it * kTileRows;
+            const bool masked = (CAUSAL && it == kt) || (q0 + kTileRows > p.L);
+            const int qlim = p.L - 1;  // last valid query
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tmem + lane_off + C::kTmST + c * 32, sr);
+                tmem_ld32(tmem + lane_off + C::kTmDPT + c * 32, dr);
+                uint32_t pp[16], pd[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float pv[2], dsv[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int col = c * 32 + 2 * i + e;
+                        float pr = ex2_approx(
+                            fmaf(__uint_as_float(sr[2 * i + e]), p.scale_log2, -lse2v[col]));
+                        if (masked) {
+                            const int qg = q0 + col;
+                            if (qg > qlim || (CAUSAL && key > qg)) pr = 0.0f;
+                        }
+                        pv[e] = pr;
+                        dsv[e] = pr * (__uint_as_float(dr[2 * i + e]) - dltv[col]);
+                    }
+                    pp[i] = pack2<BF16>(pv[0], pv[1]);
+                    pd[i] = pack2<BF16>(dsv[0], dsv[1]);
+                }
+                tmem_st16(tmem + lane_off + C::kTmST + c * 16, pp);
+                tmem_st16(tmem + lane_off + C::kTmDPT + c * 16, pd);
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(&bar_pf);
+        }
+        if (ok) {
+            ok = wait_bounded(&bar_done, 0, abort_v, p.timeout_ns);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (!ok) {
+            if (lane == 0) record_timeout(p.status, abort_v);
+        } else {
+            tc_fence_after_sync();
+            const bool valid = key < p.L;
+            const size_t roff = ((size_t)bh * p.L + key) * D * 2;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col0 = which ? C::kTmDK : C::kTmDV;
+                const float mul = which ? p.scale : 1.0f;
+                uint8_t* dst_row = reinterpret_cast<uint8_t*>(which ? p.dk : p.dv) + roff;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_off + col0 + c * 32, r);
+                    if (valid) {
+                        uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 64);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            uint4 w;
+                            w.x = pack2<BF16>(__uint_as_float(r[v4 * 8 + 0]) * mul,
+                                              __uint_as_float(r[v4 * 8 + 1]) * mul);
+                            w.y = pack2<BF16>(__uint_as_float(r[v4 * 8 + 2]) * mul,
+                                              __uint_as_float(r[v4 * 8 + 3]) * mul);
+                            w.z = pack2<BF16>(__uint_as_float(r[v4 * 8 + 4]) * mul,
+                                              __uint_as_float(r[v4 * 8 + 5]) * mul);
+                            w.w = pack2<BF16>(__uint_as_float(r[v4 * 8 + 6]) * mul,
+                                              __uint_as_float(r[v4 * 8 + 7]) * mul);
+                            dst[v4] = w;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_t(const BwdParams& p, cudaStream_t s) {
+    using C = DkdvCfg<D, BF16, CAUSAL>;
+    auto kern = fa_bwd_dkdv_kernel<D, BF16, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)p.n_tiles * (unsigned)p.BH, C::kThreads, C::kSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dkdv(const BwdParams& p, int D, bool bf16, bool causal, cudaStream_t s) {
+    if (D == 64) {
+        if (bf16) return causal ? launch_t<64, true, true>(p, s) : launch_t<64, true, false>(p, s);
+        return causal ? launch_t<64, false, true>(p, s) : launch_t<64, false, false>(p, s);
+    }
+    if (bf16) return causal ? launch_t<128, true, true>(p, s) : launch_t<128, true, false>(p, s);
+    return causal ? launch_t<128, false, true>(p, s) : launch_t<128, false, false>(p, s);
+}
+
+}  // namespace fa

@@ -1,0 +1,264 @@
+// fa_bwd_dq.cu -- attention backward, dQ: one CTA per (b*h, 128-query tile).
+//
+// The separate-pass form of the dQ accumulation: for the CTA's query tile i and every key
+// tile j it can see (j <= i under the causal mask), P and dS are recomputed from the saved
+// log-sum-exp ("FlashAttention data-flow optimisation: MI50 memory and bandwidth
+// bottlenecks", section 2.2, third layer) and
+//   S  = Q_i K_j^T,  dP = dO_i V_j^T                 (tcgen05, K-major operands)
+//   P  = exp2(S * scale*log2e - LSE_i*log2e),  dS = P o (dP - Delta_i)   (per row: scalars)
+//   dQ_i += dS K_j                                   (A operand = 16-bit dS written to TMEM)
+// dQ_i is scaled by the softmax scale and written once: no atomics, deterministic.
+//
+// CTA roles (192 threads): warps 0-3 elementwise (thread = query row = TMEM lane), warp 4 TMA
+// producer (Q_i, dO_i once; K_j, V_j per stage), warp 5 MMA issuer + TMEM owner.
+// TMEM: S [0,128), dP [128,256), dQ [256,256+D).
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+template <int D, bool BF16, bool CAUSAL>
+struct DqCfg {
+    static constexpr int kChunks = D / kChunkElems;
+    static constexpr int kTileBytes = kTileRows * D * 2;
+    static constexpr int kStages = (D == 128) ? 2 : 4;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffDO = kTileBytes;
+    static constexpr int kOffK = 2 * kTileBytes;
+    static constexpr int kOffV = kOffK + kStages * kTileBytes;
+    static constexpr int kSmemBytes = kOffV + kStages * kTileBytes + 1024;
+    static constexpr int kThreads = 192;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmDQ = 256;
+    static constexpr uint32_t kIdescS = idesc_f16(BF16, 128, 128, false, false);
+    static constexpr uint32_t kIdescG = idesc_f16(BF16, 128, D, false, true);
+};
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(192, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+    using C = DqCfg<D, BF16, CAUSAL>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    __shared__ uint64_t bar_qd, bar_kvf[C::kStages], bar_kve[C::kStages], bar_sf, bar_pf, bar_done,
+        bar_fin;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int tile_id = blockIdx.x;
+    const int bh = tile_id % p.BH;
+    const int qt = p.n_tiles - 1 - tile_id / p.BH;  // heaviest query tiles first
+    const int n_kv = CAUSAL ? (qt + 1) : p.n_tiles;
+    volatile int* abort_v = &abort_flag;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bar_qd, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&bar_kvf[s], 1);
+            mbar_init(&bar_kve[s], 1);
+        }
+        mbar_init(&bar_sf, 1);
+        mbar_init(&bar_pf, 128);
+        mbar_init(&bar_done, 1);
+        mbar_init(&bar_fin, 1);
+        mbar_fence_init();
+    }
+    if (warp == 5) tmem_alloc(&tmem_base_sh, C::kTmemCols);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = tmem_base_sh;
+
+    if (warp == 4) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tm_q);
+            tma_prefetch_desc(&p.tm_k);
+            tma_prefetch_desc(&p.tm_v);
+            tma_prefetch_desc(&p.tm_do);
+            mbar_arrive_expect_tx(&bar_qd, 2 * C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c) {
+                tma_load_3d(smem + C::kOffQ + c * kChunkBytes, &p.tm_q, &bar_qd, c * kChunkElems,
+                            qt * kTileRows, bh);
+                tma_load_3d(smem + C::kOffDO + c * kChunkBytes, &p.tm_do, &bar_qd, c * kChunkElems,
+                            qt * kTileRows, bh);
+            }
+            bool ok = true;
+            int issued = 0;
+            for (int j = 0; j < n_kv; ++j) {
+                const int st = j % C::kStages;
+                const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
+                if (j >= C::kStages && !wait_bounded(&bar_kve[st], ph ^ 1u, abort_v, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bar_kvf[st], 2 * C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c) {
+                    tma_load_3d(smem + C::kOffK + st * C::kTileBytes + c * kChunkBytes, &p.tm_k,
+                                &bar_kvf[st], c * kChunkElems, j * kTileRows, bh);
+                    tma_load_3d(smem + C::kOffV + st * C::kTileBytes + c * kChunkBytes, &p.tm_v,
+                                &bar_kvf[st], c * kChunkElems, j * kTileRows, bh);
+                }
+                issued = j + 1;
+            }
+            if (!ok) record_timeout(p.status, abort_v);
+            wait_bounded(&bar_qd, 0, nullptr, p.timeout_ns);
+            for (int j = issued - 1; j >= 0 && j >= issued - C::kStages; --j)
+                wait_bounded(&bar_kvf[j % C::kStages], (uint32_t)(j / C::kStages) & 1u, nullptr,
+                             p.timeout_ns);
+        }
+    } else if (warp == 5) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            const uint32_t q_base = smem_u32(smem + C::kOffQ);
+            const uint32_t do_base = smem_u32(smem + C::kOffDO);
+            bool ok = wait_bounded(&bar_qd, 0, abort_v, p.timeout_ns);
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int st = j % C::kStages;
+                const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
+                if (!wait_bounded(&bar_kvf[st], ph, abort_v, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t k_base = smem_u32(smem + C::kOffK + st * C::kTileBytes);
+                const uint32_t v_base = smem_u32(smem + C::kOffV + st * C::kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::kTmS, sdesc_kmajor_sw128(q_base + off),
+                           sdesc_kmajor_sw128(k_base + off), C::kIdescS, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::kTmDP, sdesc_kmajor_sw128(do_base + off),
+                           sdesc_kmajor_sw128(v_base + off), C::kIdescS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar_sf);
+                if (!wait_bounded(&bar_pf, (uint32_t)j & 1u, abort_v, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < kTileRows / 16; ++kk)
+                    mma_ts(tmem + C::kTmDQ, tmem + C::kTmS + kk * 8,
+                           sdesc_mnmajor_sw128(k_base + kk * 2048, kChunkBytes), C::kIdescG,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&bar_kve[st]);
+            }
+            if (ok) mma_commit(&bar_done);
+            if (!ok) record_timeout(p.status, abort_v);
+            mma_commit(&bar_fin);
+            wait_bounded(&bar_fin, 0, nullptr, p.timeout_ns);
+        }
+    } else {
+        // ------------------------------ elementwise warps ------------------------------
+        const int row = warp * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const int q_row = qt * kTileRows + row;  // < Lpad always
+        const float lse2 = p.lse2_pad[(size_t)bh * p.Lpad + q_row];
+        const float dlt = p.delta_pad[(size_t)bh * p.Lpad + q_row];
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            ok = wait_bounded(&bar_sf, (uint32_t)j & 1u, abort_v, p.timeout_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const int key0 = j * kTileRows;
+            const bool masked = (CAUSAL && j == n_kv - 1) || (key0 + kTileRows > p.L);
+            const int klim = CAUSAL ? min(p.L - 1, q_row) : (p.L - 1);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tmem + lane_off + C::kTmS + c * 32, sr);
+                tmem_ld32(tmem + lane_off + C::kTmDP + c * 32, dr);
+                uint32_t pd[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float dsv[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int col = c * 32 + 2 * i + e;
+                        float pr = ex2_approx(fmaf(__uint_as_float(sr[2 * i + e]), p.scale_log2, -lse2));
+                        if (masked && key0 + col > klim) pr = 0.0f;
+                        dsv[e] = pr * (__uint_as_float(dr[2 * i + e]) - dlt);
+                    }
+                    pd[i] = pack2<BF16>(dsv[0], dsv[1]);
+                }
+                tmem_st16(tmem + lane_off + C::kTmS + c * 16, pd);
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(&bar_pf);
+        }
+        if (ok) {
+            ok = wait_bounded(&bar_done, 0, abort_v, p.timeout_ns);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (!ok) {
+            if (lane == 0) record_timeout(p.status, abort_v);
+        } else {
+            tc_fence_after_sync();
+            const bool valid = q_row < p.L;
+            uint8_t* dst_row = reinterpret_cast<uint8_t*>(p.dq) + ((size_t)bh * p.L + q_row) * D * 2;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + C::kTmDQ + c * 32, r);
+                if (valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 64);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        uint4 w;
+                        w.x = pack2<BF16>(__uint_as_float(r[v4 * 8 + 0]) * p.scale,
+                                          __uint_as_float(r[v4 * 8 + 1]) * p.scale);
+                        w.y = pack2<BF16>(__uint_as_float(r[v4 * 8 + 2]) * p.scale,
+                                          __uint_as_float(r[v4 * 8 + 3]) * p.scale);
+                        w.z = pack2<BF16>(__uint_as_float(r[v4 * 8 + 4]) * p.scale,
+                                          __uint_as_float(r[v4 * 8 + 5]) * p.scale);
+                        w.w = pack2<BF16>(__uint_as_float(r[v4 * 8 + 6]) * p.scale,
+                                          __uint_as_float(r[v4 * 8 + 7]) * p.scale);
+                        dst[v4] = w;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_t(const BwdParams& p, cudaStream_t s) {
+    using C = DqCfg<D, BF16, CAUSAL>;
+    auto kern = fa_bwd_dq_kernel<D, BF16, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)p.n_tiles * (unsigned)p.BH, C::kThreads, C::kSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dq(const BwdParams& p, int D, bool bf16, bool causal, cudaStream_t s) {
+    if (D == 64) {
+        if (bf16) return causal ? launch_t<64, true, true>(p, s) : launch_t<64, true, false>(p, s);
+        return causal ? launch_t<64, false, true>(p, s) : launch_t<64, false, false>(p, s);
+    }
+    if (bf16) return causal ? launch_t<128, true, true>(p, s) : launch_t<128, true, false>(p, s);
+    return causal ? launch_t<128, false, true>(p, s) : launch_t<128, false, false>(p, s);
+}
+
+}  // namespace fa

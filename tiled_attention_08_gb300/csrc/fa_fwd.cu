@@ -1,0 +1,333 @@
+// fa_fwd.cu -- fused attention forward for sm_103a (TMA + tcgen05/TMEM, online softmax).
+//
+// Method ("FlashAttention data-flow optimisation: MI50 memory and bandwidth bottlenecks",
+// section 2.2): Q is split into 128-row tiles that stay on chip; K/V stream through shared
+// memory in 128-key tiles; each row keeps a running max and a running sum of exponentials
+// while the tiles arrive, the partial output is rescaled when the max grows, and only O and
+// the per-row statistics (folded into one log-sum-exp) are written.  QK^T, the softmax and
+// PV run in this one kernel ("FlashAttention principles and engineering practice",
+// section 1, kernel fusion), so S and P never reach global memory.
+//
+// CTA roles (192 threads, one CTA per (b*h, query tile)):
+//   warps 0-3  softmax: thread t of warp w owns query row 32*w + t == TMEM lane;
+//   warp 4     TMA producer: Q once, then K_j / V_j into a ring of shared-memory stages;
+//   warp 5     MMA issuer (one thread) and TMEM owner.
+// TMEM columns: S double buffer at [0,128) and [128,256) (fp32); the 16-bit P of a tile
+// overwrites the first 64 columns of its S buffer and feeds the PV MMA straight from TMEM;
+// O (fp32, D columns) at [256, 256+D).
+//
+// Online softmax in the log2 domain: y = s * scale * log2(e).  The running reference max m
+// is only raised when a tile's max exceeds it by more than kRescaleThreshold (2^8 headroom
+// for P), so O is rescaled rarely; the result is unchanged because O and the running sum
+// always share the same reference.  LSE = (m + log2(l)) * ln(2).
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D, bool BF16, bool CAUSAL>
+struct FwdCfg {
+    static constexpr int kChunks = D / kChunkElems;            // swizzle boxes per tile row
+    static constexpr int kTileBytes = kTileRows * D * 2;       // one 128 x D tile
+    static constexpr int kStages = (D == 128) ? 2 : 4;         // K and V ring depth
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + kTileBytes;
+    static constexpr int kOffV = kOffK + kStages * kTileBytes;
+    static constexpr int kSmemBytes = kOffV + kStages * kTileBytes + 1024;  // + alignment slack
+    static constexpr int kThreads = 192;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kTmS = 0;    // S buffer b at kTmS + 128*b
+    static constexpr uint32_t kTmO = 256;  // O accumulator
+    static constexpr uint32_t kIdescS = idesc_f16(BF16, 128, 128, false, false);
+    static constexpr uint32_t kIdescO = idesc_f16(BF16, 128, D, false, true);
+};
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(192, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+    using C = FwdCfg<D, BF16, CAUSAL>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    __shared__ uint64_t bar_q, bar_kf[C::kStages], bar_ke[C::kStages], bar_vf[C::kStages],
+        bar_ve[C::kStages], bar_sf[2], bar_pf[2], bar_od, bar_fin;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // Heaviest query tiles (most key tiles under the causal mask) are scheduled first.
+    const int tile_id = blockIdx.x;
+    const int bh = tile_id % p.BH;
+    const int qt = p.n_tiles - 1 - tile_id / p.BH;
+    const int n_kv = CAUSAL ? (qt + 1) : p.n_tiles;
+    volatile int* abort_v = &abort_flag;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bar_q, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&bar_kf[s], 1);
+            mbar_init(&bar_ke[s], 1);
+            mbar_init(&bar_vf[s], 1);
+            mbar_init(&bar_ve[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bar_sf[b], 1);
+            mbar_init(&bar_pf[b], 128);
+        }
+        mbar_init(&bar_od, 1);
+        mbar_init(&bar_fin, 1);
+        mbar_fence_init();
+    }
+    if (warp == 5) tmem_alloc(&tmem_base_sh, C::kTmemCols);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = tmem_base_sh;
+
+    if (warp == 4) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tm_q);
+            tma_prefetch_desc(&p.tm_k);
+            tma_prefetch_desc(&p.tm_v);
+            mbar_arrive_expect_tx(&bar_q, C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(smem + C::kOffQ + c * kChunkBytes, &p.tm_q, &bar_q, c * kChunkElems,
+                            qt * kTileRows, bh);
+            bool ok = true;
+            int issued_k = 0, issued_v = 0;  // fills handed to the TMA unit
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int st = j % C::kStages;
+                const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
+                if (j >= C::kStages && !wait_bounded(&bar_ke[st], ph ^ 1u, abort_v, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bar_kf[st], C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(smem + C::kOffK + st * C::kTileBytes + c * kChunkBytes, &p.tm_k,
+                                &bar_kf[st], c * kChunkElems, j * kTileRows, bh);
+                issued_k = j + 1;
+                if (j >= C::kStages && !wait_bounded(&bar_ve[st], ph ^ 1u, abort_v, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bar_vf[st], C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(smem + C::kOffV + st * C::kTileBytes + c * kChunkBytes, &p.tm_v,
+                                &bar_vf[st], c * kChunkElems, j * kTileRows, bh);
+                issued_v = j + 1;
+            }
+            if (!ok) record_timeout(p.status, abort_v);
+            // Drain: the newest fill of every stage must have landed before the CTA exits.
+            // (These waits return at once on the normal path.)
+            wait_bounded(&bar_q, 0, nullptr, p.timeout_ns);
+            for (int j = issued_k - 1; j >= 0 && j >= issued_k - C::kStages; --j)
+                wait_bounded(&bar_kf[j % C::kStages], (uint32_t)(j / C::kStages) & 1u, nullptr,
+                             p.timeout_ns);
+            for (int j = issued_v - 1; j >= 0 && j >= issued_v - C::kStages; --j)
+                wait_bounded(&bar_vf[j % C::kStages], (uint32_t)(j / C::kStages) & 1u, nullptr,
+                             p.timeout_ns);
+        }
+    } else if (warp == 5) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            const uint32_t q_base = smem_u32(smem + C::kOffQ);
+            bool ok = wait_bounded(&bar_q, 0, abort_v, p.timeout_ns);
+            auto issue_pv = [&](int jj) -> bool {
+                const int b = jj & 1;
+                const int st = jj % C::kStages;
+                const uint32_t ph = (uint32_t)(jj / C::kStages) & 1u;
+                if (!wait_bounded(&bar_pf[b], (uint32_t)(jj >> 1) & 1u, abort_v, p.timeout_ns))
+                    return false;
+                if (!wait_bounded(&bar_vf[st], ph, abort_v, p.timeout_ns)) return false;
+                tc_fence_after_sync();
+                const uint32_t v_base = smem_u32(smem + C::kOffV + st * C::kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < kTileRows / 16; ++kk) {
+                    const uint64_t bd = sdesc_mnmajor_sw128(v_base + kk * 2048, kChunkBytes);
+                    mma_ts(tmem + C::kTmO, tmem + C::kTmS + 128 * b + kk * 8, bd, C::kIdescO,
+                           (jj > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&bar_ve[st]);
+                mma_commit(&bar_od);
+                return true;
+            };
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int st = j % C::kStages;
+                const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
+                const int b = j & 1;
+                if (!wait_bounded(&bar_kf[st], ph, abort_v, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t k_base = smem_u32(smem + C::kOffK + st * C::kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::kTmS + 128 * b, sdesc_kmajor_sw128(q_base + off),
+                           sdesc_kmajor_sw128(k_base + off), C::kIdescS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar_ke[st]);
+                mma_commit(&bar_sf[b]);
+                if (j > 0 && !issue_pv(j - 1)) ok = false;
+            }
+            if (ok && n_kv > 0 && !issue_pv(n_kv - 1)) ok = false;
+            if (!ok) record_timeout(p.status, abort_v);
+            // Every issued MMA must finish before TMEM is released.
+            mma_commit(&bar_fin);
+            wait_bounded(&bar_fin, 0, nullptr, p.timeout_ns);
+        }
+    } else {
+        // ------------------------------ softmax warps ------------------------------
+        const int row = warp * 32 + lane;  // row inside the tile == TMEM lane
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const int q_row = qt * kTileRows + row;
+        float m_ref = -INFINITY;
+        float l_sum = 0.0f;
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            const int b = j & 1;
+            ok = wait_bounded(&bar_sf[b], (uint32_t)(j >> 1) & 1u, abort_v, p.timeout_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint32_t s_addr = tmem + lane_off + C::kTmS + 128 * b;
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld32(s_addr + c * 32, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+            }
+            const int key0 = j * kTileRows;
+            if ((CAUSAL && j == n_kv - 1) || key0 + kTileRows > p.L) {
+                const int lim = CAUSAL ? min(p.L - 1, q_row) : (p.L - 1);
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (key0 + c > lim) s[c] = -INFINITY;
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+            const float m_cand = mx * p.scale_log2;
+            float m_new = m_ref;
+            if (m_cand > m_ref + kRescaleThreshold) m_new = m_cand;
+            const bool rescale = (j > 0) && (m_new != m_ref);
+            const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+            const float alpha = rescale ? ex2_approx(m_ref - m_new) : 1.0f;
+            float sum = 0.0f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float p0 = ex2_approx(fmaf(s[h * 64 + 2 * i], p.scale_log2, -m_use));
+                    const float p1 = ex2_approx(fmaf(s[h * 64 + 2 * i + 1], p.scale_log2, -m_use));
+                    sum += p0 + p1;
+                    pk[i] = pack2<BF16>(p0, p1);
+                }
+                tmem_st32(s_addr + h * 32, pk);
+            }
+            l_sum = l_sum * alpha + sum;
+            if (__any_sync(0xffffffffu, rescale)) {
+                // O holds the sum up to tile j-1: wait for that PV, then rescale in place.
+                bool okw = wait_bounded(&bar_od, (uint32_t)(j - 1) & 1u, abort_v, p.timeout_ns);
+                okw = __all_sync(0xffffffffu, okw);
+                if (!okw) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t o_addr = tmem + lane_off + C::kTmO;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(o_addr + c * 32, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                    tmem_st32(o_addr + c * 32, r);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(&bar_pf[b]);
+            m_ref = m_new;
+        }
+        if (ok && n_kv > 0) {
+            ok = wait_bounded(&bar_od, (uint32_t)(n_kv - 1) & 1u, abort_v, p.timeout_ns);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (!ok) {
+            if (lane == 0) record_timeout(p.status, abort_v);
+        } else {
+            tc_fence_after_sync();
+            const bool valid = q_row < p.L;
+            const float inv_l = 1.0f / l_sum;
+            if (valid) p.lse[(size_t)bh * p.L + q_row] = (m_ref + log2f(l_sum)) * kLn2;
+            uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) + ((size_t)bh * p.L + q_row) * D * 2;
+            const uint32_t o_addr = tmem + lane_off + C::kTmO;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(o_addr + c * 32, r);
+                if (valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        uint4 w;
+                        w.x = pack2<BF16>(__uint_as_float(r[v4 * 8 + 0]) * inv_l,
+                                          __uint_as_float(r[v4 * 8 + 1]) * inv_l);
+                        w.y = pack2<BF16>(__uint_as_float(r[v4 * 8 + 2]) * inv_l,
+                                          __uint_as_float(r[v4 * 8 + 3]) * inv_l);
+                        w.z = pack2<BF16>(__uint_as_float(r[v4 * 8 + 4]) * inv_l,
+                                          __uint_as_float(r[v4 * 8 + 5]) * inv_l);
+                        w.w = pack2<BF16>(__uint_as_float(r[v4 * 8 + 6]) * inv_l,
+                                          __uint_as_float(r[v4 * 8 + 7]) * inv_l);
+                        dst[v4] = w;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_t(const FwdParams& p, cudaStream_t s) {
+    using C = FwdCfg<D, BF16, CAUSAL>;
+    auto kern = fa_fwd_kernel<D, BF16, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)p.n_tiles * (unsigned)p.BH;
+    kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdParams& p, int D, bool bf16, bool causal, cudaStream_t s) {
+    if (D == 64) {
+        if (bf16) return causal ? launch_t<64, true, true>(p, s) : launch_t<64, true, false>(p, s);
+        return causal ? launch_t<64, false, true>(p, s) : launch_t<64, false, false>(p, s);
+    }
+    if (bf16) return causal ? launch_t<128, true, true>(p, s) : launch_t<128, true, false>(p, s);
+    return causal ? launch_t<128, false, true>(p, s) : launch_t<128, false, false>(p, s);
+}
+
+}  // namespace fa

@@ -1,0 +1,65 @@
+// fa_internal.h -- launch parameters shared between the C-ABI layer and the kernel units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+// Status codes a kernel records in the device status word (first error wins).
+enum DeviceError : int {
+    kDevOk = 0,
+    kDevTimeout = 4,  // a bounded wait ran out
+};
+
+// Tile geometry shared by every kernel: 128 query rows x 128 keys per tile; operands are
+// staged in shared memory as 128-row x 64-element boxes with the 128-byte swizzle.
+constexpr int kTileRows = 128;
+constexpr int kChunkElems = 64;
+constexpr int kChunkBytes = kTileRows * kChunkElems * 2;  // 16 KiB per box
+
+struct FwdParams {
+    CUtensorMap tm_q, tm_k, tm_v;  // [BH, L, D] 16-bit, box {64, 128, 1}
+    void* o;                       // [BH, L, D] 16-bit
+    float* lse;                    // [BH, L] natural-log LSE
+    int L;
+    int BH;
+    int n_tiles;        // ceil(L / 128)
+    float scale_log2;   // scale * log2(e)
+    int* status;        // device status word
+    uint64_t timeout_ns;
+};
+
+struct BwdPreParams {
+    const void* o;       // [BH, L, D]
+    const void* dout;    // [BH, L, D]
+    const float* lse;    // [BH, L]
+    float* lse2_pad;     // [BH, Lpad]: LSE * log2(e), zero past L
+    float* delta_pad;    // [BH, Lpad]: rowsum(dO * O), zero past L
+    int L, Lpad, BH, D;
+    int bf16;
+};
+
+struct BwdParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;  // [BH, L, D] 16-bit, box {64, 128, 1}
+    const float* lse2_pad;                // [BH, Lpad]
+    const float* delta_pad;               // [BH, Lpad]
+    void* dq;                             // [BH, L, D]
+    void* dk;
+    void* dv;
+    int L, Lpad, BH, n_tiles;
+    float scale;        // softmax scale (applied to dQ and dK)
+    float scale_log2;   // scale * log2(e)
+    int* status;
+    uint64_t timeout_ns;
+};
+
+// Launchers (one per kernel unit).  Return the launch error, if any.
+cudaError_t launch_fwd(const FwdParams& p, int D, bool bf16, bool causal, cudaStream_t s);
+cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t s);
+cudaError_t launch_bwd_dkdv(const BwdParams& p, int D, bool bf16, bool causal, cudaStream_t s);
+cudaError_t launch_bwd_dq(const BwdParams& p, int D, bool bf16, bool causal, cudaStream_t s);
+cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s);
+
+}  // namespace fa
