@@ -76,6 +76,35 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  size_t workspace_bytes, int B, int H, int L, int D, float scale, int causal,
                  int dtype, void* stream);
 
+/* Size of the fixed device scratch array behind fa_bwd_noalloc: 16 MiB. */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * Backward for callers that cannot allocate device memory.  The pages describe no such entry
+ * point; it has no counterpart in the method and exists only for callers that must not call
+ * cudaMalloc themselves (for example a plugin whose host framework owns all device memory and
+ * passes it only inputs and outputs, or a running latency-critical loop where an allocation
+ * could synchronise the device at an unbounded cost).
+ *
+ * Same arguments, results and checks as fa_bwd, minus the workspace: the scratch fa_bwd would
+ * take from `workspace` comes from a file-scope device array of FA_BWD_NOALLOC_SCRATCH_BYTES
+ * compiled into the library, which every GPU that loads the library's code holds until the
+ * process exits.  The limit: fa_bwd_workspace_bytes(B,H,L,D) = 8*B*H*ceil(L/128)*128 bytes
+ * must not exceed FA_BWD_NOALLOC_SCRATCH_BYTES (B*H*ceil(L/128)*128 <= 2^21 rows, e.g.
+ * B*H = 256 heads at L = 8192); larger problems return FA_ERR_UNSUPPORTED before anything is
+ * enqueued.  The call allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ *
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current); make that first call before any stream capture.  Every call on
+ * a device shares the one array, so calls whose kernels overlap on the GPU (on different
+ * streams, or from different threads) race on it and give undefined results: serialise them.
+ * Nothing in the array needs clearing between calls; each call's first kernel overwrites
+ * everything its later kernels read.
+ */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                         int H, int L, int D, float scale, int causal, int dtype, void* stream);
+
 /*
  * Synchronises `stream`, then reads and clears the current device's status word.  Returns
  * FA_OK, FA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last call, or

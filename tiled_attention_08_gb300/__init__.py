@@ -19,7 +19,7 @@ import threading
 __all__ = ["FaError", "load_library", "library_path", "fa_fwd", "fa_bwd",
            "fa_bwd_workspace_bytes", "fa_get_device_status", "fa_set_wait_timeout_ns",
            "fa_selftest_wait_timeout", "fa_trace_next_call", "fa_launch_count", "fa_status_string",
-           "forward", "backward", "attention",
+           "fa_bwd_noalloc", "forward", "backward", "attention",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
            "FA_BF16", "FA_FP16"]
 
@@ -33,7 +33,7 @@ _lock = threading.Lock()
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_device_status",
             "fa_set_wait_timeout_ns", "fa_selftest_wait_timeout", "fa_trace_next_call",
-            "fa_launch_count", "fa_status_string")
+            "fa_launch_count", "fa_status_string", "fa_bwd_noalloc")
 
 
 class FaError(RuntimeError):
@@ -63,6 +63,9 @@ def load_library():
         lib.fa_bwd_workspace_bytes.restype = sz
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, i, vp]
         lib.fa_bwd.restype = i
+        lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i,
+                                       vp]
+        lib.fa_bwd_noalloc.restype = i
         lib.fa_get_device_status.argtypes = [vp]
         lib.fa_get_device_status.restype = i
         lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
@@ -94,6 +97,14 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, 
            causal, dtype, stream) -> int:
     return load_library().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
                                  B, H, L, D, scale, int(causal), dtype, stream)
+
+
+def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, L, D, scale, causal, dtype,
+                   stream) -> int:
+    """fa_bwd without a caller workspace, for callers that cannot allocate device memory: the
+    scratch comes from a fixed 16 MiB array compiled into the library (see include/fa.h)."""
+    return load_library().fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, L, D, scale,
+                                         int(causal), dtype, stream)
 
 
 def fa_get_device_status(stream) -> int:
