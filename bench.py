@@ -406,9 +406,39 @@ def run_ours(args, w):
                 "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS bf16 GEMM)"
                                + (" of measured" if peak_src == "measured" else " of fallback")}
 
-    # End to end through the same API, pinned host buffers, copies inside the timed region.
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype_name,
+        "data": "synthetic (seeded N(0,1) tensors; no dataset or weights)",
+        "config": dict(w.describe(),
+                       parallelism=("replicas: one independent copy per GPU"
+                                    if world > 1 else "single GPU"),
+                       step="fa_fwd + fa_bwd (4 kernels)",
+                       l2=f"inputs larger than L2 ({q.numel() * 2 / 2**20:.0f} MiB per tensor); "
+                          "no flush"),
+        "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2),
+        "fwd_frac_of_peak": round(fwd_tf / peak_tf, 4),
+        "bwd_frac_of_peak": round(bwd_tf / peak_tf, 4),
+        "peak_tflops": peak_tf, "peak_hbm_gbs": peak_bw,
+        "kernels": kernels,
+        "roofline": roofline,
+        "gpu_launches": int(reduce_sum(launches, dev)),
+        "clocks": clocks,
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(w, inp, q, o, lse, dq, dk, dv, call_fwd, call_bwd, stream, dev, K)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, inp)
+    return result if rank == 0 else None
+
+
+def run_e2e(w, inp, q, o, lse, dq, dk, dv, call_fwd, call_bwd, stream, dev, K):
+    """End to end through the same API, pinned host buffers, copies inside the timed region."""
+    import torch
+    import tiled_attention_08_gb300 as fa
     pin = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
-    dq_d, dk_d, dv_d = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
                 for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
     qd, kd, vd, dod = (torch.empty_like(q) for _ in range(4))
@@ -438,36 +468,11 @@ def run_ours(args, w):
     e2e_ms = max(e0.elapsed_time(e1), wall * 1e3)
     e2e_ms = reduce_max(e2e_ms, dev)
     e2e_value = reduce_sum(step_flops(w) * K_e2e, dev) / (e2e_ms * 1e-3) / 1e12
-    st = fa.fa_get_device_status(sh)
+    st = fa.fa_get_device_status(stream.cuda_stream)
     if st != fa.FA_OK:
         raise fa.FaError("e2e region", st)
-
-    result = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
-        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms / K, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.dtype_name,
-        "data": "synthetic (seeded N(0,1) tensors; no dataset or weights)",
-        "config": dict(w.describe(),
-                       parallelism=("replicas: one independent copy per GPU"
-                                    if world > 1 else "single GPU"),
-                       step="fa_fwd + fa_bwd (4 kernels)",
-                       l2=f"inputs larger than L2 ({q.numel() * 2 / 2**20:.0f} MiB per tensor); "
-                          "no flush"),
-        "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2),
-        "fwd_frac_of_peak": round(fwd_tf / peak_tf, 4),
-        "bwd_frac_of_peak": round(bwd_tf / peak_tf, 4),
-        "peak_tflops": peak_tf, "peak_hbm_gbs": peak_bw,
-        "kernels": kernels,
-        "roofline": roofline,
-        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / K_e2e, 4)},
-        "gpu_launches": int(reduce_sum(launches, dev)),
-        "clocks": clocks,
-    }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, inp)
-    return result if rank == 0 else None
+    return {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / K_e2e, 4)}
 
 
 def main(argv=None):
@@ -477,7 +482,11 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size B (smaller profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the host-buffer end-to-end pass (profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -485,6 +494,11 @@ def main(argv=None):
     if args.workload not in workloads.WORKLOADS:
         ap.error(f"unknown workload; choose from {sorted(workloads.WORKLOADS)}")
     w = workloads.WORKLOADS[args.workload]
+    if args.batch is not None:
+        if args.batch < 1:
+            ap.error("--batch must be positive")
+        from dataclasses import replace
+        w = replace(w, name=f"{w.name}_B{args.batch}", B=args.batch)
     if not w.backward:
         ap.error("the benchmark step is forward + backward; pick a workload with a backward")
     if args.impl == "reference":
