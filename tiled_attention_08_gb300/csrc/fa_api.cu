@@ -91,6 +91,18 @@ struct TraceDisarm {
     ~TraceDisarm() { t_trace_pairs = 0; }
 };
 
+// Heads per schedule group: the streamed per-head operands (two [L, D] 16-bit tensors) of a
+// group should take at most kGroupBytes of L2, so that tiles of the same head that run at the
+// same time reuse them from L2 instead of HBM.
+constexpr size_t kGroupBytes = size_t(48) << 20;
+int schedule_group(int BH, int L, int D) {
+    const size_t per_head = (size_t)2 * (size_t)L * (size_t)D * 2u;
+    size_t g = per_head ? kGroupBytes / per_head : (size_t)BH;
+    if (g < 1) g = 1;
+    if (g > (size_t)BH) g = (size_t)BH;
+    return (int)g;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Range {
@@ -217,6 +229,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     p.L = L;
     p.BH = sh.BH;
     p.n_tiles = sh.n_tiles;
+    p.group = schedule_group(sh.BH, L, D);
     p.scale_log2 = scale * 1.4426950408889634f;
     p.status = status_ptr();
     p.timeout_ns = g_timeout_ns.load();
@@ -276,6 +289,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     p.Lpad = sh.Lpad;
     p.BH = sh.BH;
     p.n_tiles = sh.n_tiles;
+    p.group = schedule_group(sh.BH, L, D);
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.status = status_ptr();

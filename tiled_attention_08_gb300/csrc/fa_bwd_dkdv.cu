@@ -11,9 +11,13 @@
 //   dV_j += P^T dO_i,  dK_j += dS^T Q_i   (A operand = 16-bit P^T / dS^T written back to TMEM)
 // and at the end dK_j is multiplied by the softmax scale.
 //
-// CTA roles (192 threads): warps 0-3 elementwise (thread = key row = TMEM lane), warp 4 TMA
-// producer (K_j, V_j once; Q_i, dO_i, LSE_i, Delta_i per stage), warp 5 MMA issuer + TMEM owner.
-// TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D).
+// CTA roles (320 threads): warps 0-7 elementwise (warp w: key rows 32*(w%4).. == TMEM lanes,
+// query columns [64*(w/4), +64)), warp 8 TMA producer (K_j, V_j once; Q_i, dO_i, LSE_i,
+// Delta_i per stage), warp 9 MMA issuer + TMEM owner.  Per query tile the MMA warp issues
+// S^T, then dP^T; the elementwise warps turn S^T into P^T (which releases the dV MMA) and
+// then dP^T into dS^T (which releases the dK MMA), so dP^T and dV run under the elementwise
+// work.  TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D); the 16-bit
+// P^T and dS^T overwrite the first 64 columns of S^T and dP^T.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -32,7 +36,13 @@ struct DkdvCfg {
     static constexpr int kOffDO = kOffQ + kStages * kTileBytes;
     static constexpr int kOffVec = kOffDO + kStages * kTileBytes;
     static constexpr int kSmemBytes = kOffVec + kStages * kVecBytes + 1024;
-    static constexpr int kThreads = 192;
+    static constexpr int kEwWarps = 8;
+    static constexpr int kEwThreads = kEwWarps * 32;
+    static constexpr int kProducerWarp = kEwWarps;
+    static constexpr int kMmaWarp = kEwWarps + 1;
+    static constexpr int kThreads = (kEwWarps + 2) * 32;
+    static constexpr int kCols = 64;      // query columns per elementwise warp
+    static constexpr int kOutCols = D / 2;  // dK/dV columns per elementwise warp
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kTmST = 0, kTmDPT = 128, kTmDV = 256, kTmDK = 256 + D;
     static constexpr uint32_t kIdescS = idesc_f16(BF16, 128, 128, false, false);
@@ -40,21 +50,22 @@ struct DkdvCfg {
 };
 
 template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(192, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = DkdvCfg<D, BF16, CAUSAL>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    __shared__ uint64_t bar_kv, bar_qf[C::kStages], bar_qe[C::kStages], bar_sf, bar_pf, bar_done,
-        bar_fin;
+    __shared__ uint64_t bar_kv, bar_qf[C::kStages], bar_qe[C::kStages], bar_sf, bar_df, bar_pp,
+        bar_pd, bar_done, bar_fin;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int tile_id = blockIdx.x;
-    const int bh = tile_id % p.BH;
-    const int kt = tile_id / p.BH;  // key tile; low kt has the most query tiles under the mask
+    // Heads in L2-sized groups (their Q/dO/LSE/Delta are streamed by every key tile); inside
+    // a group key tile 0 first: it has the most query tiles under the causal mask.
+    int bh, kt;
+    tile_coords(blockIdx.x, p.BH, p.n_tiles, p.group, bh, kt);
     const int it0 = CAUSAL ? kt : 0;
     const int n_it = p.n_tiles - it0;
     volatile int* abort_v = &abort_flag;
@@ -67,18 +78,20 @@ __global__ void __launch_bounds__(192, 1) fa_bwd_dkdv_kernel(const __grid_consta
             mbar_init(&bar_qe[s], 1);
         }
         mbar_init(&bar_sf, 1);
-        mbar_init(&bar_pf, 128);
+        mbar_init(&bar_df, 1);
+        mbar_init(&bar_pp, C::kEwThreads);
+        mbar_init(&bar_pd, C::kEwThreads);
         mbar_init(&bar_done, 1);
         mbar_init(&bar_fin, 1);
         mbar_fence_init();
     }
-    if (warp == 5) tmem_alloc(&tmem_base_sh, C::kTmemCols);
+    if (warp == C::kMmaWarp) tmem_alloc(&tmem_base_sh, C::kTmemCols);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_base_sh;
 
-    if (warp == 4) {
+    if (warp == C::kProducerWarp) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
             tma_prefetch_desc(&p.tm_q);
@@ -121,7 +134,7 @@ __global__ void __launch_bounds__(192, 1) fa_bwd_dkdv_kernel(const __grid_consta
                 wait_bounded(&bar_qf[t % C::kStages], (uint32_t)(t / C::kStages) & 1u, nullptr,
                              p.timeout_ns);
         }
-    } else if (warp == 5) {
+    } else if (warp == C::kMmaWarp) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
             const uint32_t k_base = smem_u32(smem + C::kOffK);
@@ -143,26 +156,35 @@ __global__ void __launch_bounds__(192, 1) fa_bwd_dkdv_kernel(const __grid_consta
                     mma_ss(tmem + C::kTmST, sdesc_kmajor_sw128(k_base + off),
                            sdesc_kmajor_sw128(q_base + off), C::kIdescS, kk > 0 ? 1u : 0u);
                 }
+                mma_commit(&bar_sf);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
                     mma_ss(tmem + C::kTmDPT, sdesc_kmajor_sw128(v_base + off),
                            sdesc_kmajor_sw128(do_base + off), C::kIdescS, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(&bar_sf);
-                if (!wait_bounded(&bar_pf, (uint32_t)t & 1u, abort_v, p.timeout_ns)) {
+                mma_commit(&bar_df);
+                const uint32_t acc0 = t > 0 ? 1u : 0u;
+                if (!wait_bounded(&bar_pp, (uint32_t)t & 1u, abort_v, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
 #pragma unroll
-                for (int kk = 0; kk < kTileRows / 16; ++kk) {
-                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+                for (int kk = 0; kk < kTileRows / 16; ++kk)
                     mma_ts(tmem + C::kTmDV, tmem + C::kTmST + kk * 8,
-                           sdesc_mnmajor_sw128(do_base + kk * 2048, kChunkBytes), C::kIdescG, acc);
-                    mma_ts(tmem + C::kTmDK, tmem + C::kTmDPT + kk * 8,
-                           sdesc_mnmajor_sw128(q_base + kk * 2048, kChunkBytes), C::kIdescG, acc);
+                           sdesc_mnmajor_sw128(do_base + kk * 2048, kChunkBytes), C::kIdescG,
+                           (acc0 || kk > 0) ? 1u : 0u);
+                if (!wait_bounded(&bar_pd, (uint32_t)t & 1u, abort_v, p.timeout_ns)) {
+                    ok = false;
+                    break;
                 }
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < kTileRows / 16; ++kk)
+                    mma_ts(tmem + C::kTmDK, tmem + C::kTmDPT + kk * 8,
+                           sdesc_mnmajor_sw128(q_base + kk * 2048, kChunkBytes), C::kIdescG,
+                           (acc0 || kk > 0) ? 1u : 0u);
                 mma_commit(&bar_qe[st]);
             }
             if (ok) mma_commit(&bar_done);
@@ -172,54 +194,84 @@ __global__ void __launch_bounds__(192, 1) fa_bwd_dkdv_kernel(const __grid_consta
         }
     } else {
         // ------------------------------ elementwise warps ------------------------------
-        const int row = warp * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const int quad = warp & 3;            // TMEM lane quadrant (key rows)
+        const int half = warp >> 2;           // which 64 query columns
+        const uint32_t pair_bar = 1 + quad;   // named barrier shared with the other half
+        const int row = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const int key = kt * kTileRows + row;
+        const int c0 = half * C::kCols;
         bool ok = true;
         for (int t = 0; t < n_it; ++t) {
             const int it = it0 + t;
             const int st = t % C::kStages;
             const uint32_t ph = (uint32_t)(t / C::kStages) & 1u;
+            const float* lse2v =
+                reinterpret_cast<const float*>(smem + C::kOffVec + st * C::kVecBytes) + c0;
+            const float* dltv = lse2v + kTileRows;
+            const int q0 = it * kTileRows + c0;
+            const bool masked = (CAUSAL && it == kt) || (it * kTileRows + kTileRows > p.L);
+            const int qlim = p.L - 1;  // last valid query
+            // Phase 1: P^T = exp2(S^T * scale*log2e - LSE*log2e) on this warp's columns.
             ok = wait_bounded(&bar_qf[st], ph, abort_v, p.timeout_ns) &&
                  wait_bounded(&bar_sf, (uint32_t)t & 1u, abort_v, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after_sync();
-            const float* lse2v = reinterpret_cast<const float*>(smem + C::kOffVec + st * C::kVecBytes);
-            const float* dltv = lse2v + kTileRows;
-            const int q0 = it * kTileRows;
-            const bool masked = (CAUSAL && it == kt) || (q0 + kTileRows > p.L);
-            const int qlim = p.L - 1;  // last valid query
+            float pv[64];
+            if (ok) {
+                tc_fence_after_sync();
+                uint32_t ra[32], rb[32];
+                tmem_ld32x2(tmem + lane_off + C::kTmST + c0, tmem + lane_off + C::kTmST + c0 + 32,
+                            ra, rb);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_off + C::kTmST + c * 32, sr);
-                tmem_ld32(tmem + lane_off + C::kTmDPT + c * 32, dr);
-                uint32_t pp[16], pd[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float pv[2], dsv[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int col = c * 32 + 2 * i + e;
-                        float pr = ex2_approx(
-                            fmaf(__uint_as_float(sr[2 * i + e]), p.scale_log2, -lse2v[col]));
-                        if (masked) {
-                            const int qg = q0 + col;
-                            if (qg > qlim || (CAUSAL && key > qg)) pr = 0.0f;
-                        }
-                        pv[e] = pr;
-                        dsv[e] = pr * (__uint_as_float(dr[2 * i + e]) - dltv[col]);
-                    }
-                    pp[i] = pack2<BF16>(pv[0], pv[1]);
-                    pd[i] = pack2<BF16>(dsv[0], dsv[1]);
+                for (int i = 0; i < 32; ++i) {
+                    pv[i] = ex2_approx(fmaf(__uint_as_float(ra[i]), p.scale_log2, -lse2v[i]));
+                    pv[32 + i] =
+                        ex2_approx(fmaf(__uint_as_float(rb[i]), p.scale_log2, -lse2v[32 + i]));
                 }
-                tmem_st16(tmem + lane_off + C::kTmST + c * 16, pp);
-                tmem_st16(tmem + lane_off + C::kTmDPT + c * 16, pd);
+                if (masked) {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) {
+                        const int qg = q0 + i;
+                        if (qg > qlim || (CAUSAL && key > qg)) pv[i] = 0.0f;
+                    }
+                }
+            }
+            ok = bar_and(pair_bar, 64, ok);  // both halves have read S^T: P^T may overwrite it
+            if (!ok) break;
+            {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
+                tmem_st32(tmem + lane_off + C::kTmST + half * 32, pk);
             }
             tmem_st_wait();
             tc_fence_before_sync();
-            mbar_arrive(&bar_pf);
+            mbar_arrive(&bar_pp);
+            // Phase 2: dS^T = P^T o (dP^T - Delta).
+            ok = wait_bounded(&bar_df, (uint32_t)t & 1u, abort_v, p.timeout_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                tc_fence_after_sync();
+                uint32_t ra[32], rb[32];
+                tmem_ld32x2(tmem + lane_off + C::kTmDPT + c0,
+                            tmem + lane_off + C::kTmDPT + c0 + 32, ra, rb);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    pv[i] = pv[i] * (__uint_as_float(ra[i]) - dltv[i]);
+                    pv[32 + i] = pv[32 + i] * (__uint_as_float(rb[i]) - dltv[32 + i]);
+                }
+            }
+            ok = bar_and(pair_bar, 64, ok);  // both halves have read dP^T
+            if (!ok) break;
+            {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
+                tmem_st32(tmem + lane_off + C::kTmDPT + half * 32, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(&bar_pd);
         }
         if (ok) {
             ok = wait_bounded(&bar_done, 0, abort_v, p.timeout_ns);
@@ -230,14 +282,14 @@ __global__ void __launch_bounds__(192, 1) fa_bwd_dkdv_kernel(const __grid_consta
         } else {
             tc_fence_after_sync();
             const bool valid = key < p.L;
-            const size_t roff = ((size_t)bh * p.L + key) * D * 2;
+            const size_t roff = ((size_t)bh * p.L + key) * D * 2 + half * C::kOutCols * 2;
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
-                const uint32_t col0 = which ? C::kTmDK : C::kTmDV;
+                const uint32_t col0 = (which ? C::kTmDK : C::kTmDV) + half * C::kOutCols;
                 const float mul = which ? p.scale : 1.0f;
                 uint8_t* dst_row = reinterpret_cast<uint8_t*>(which ? p.dk : p.dv) + roff;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < C::kOutCols / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld32(tmem + lane_off + col0 + c * 32, r);
                     if (valid) {
@@ -263,7 +315,7 @@ __global__ void __launch_bounds__(192, 1) fa_bwd_dkdv_kernel(const __grid_consta
 
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == C::kMmaWarp) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, C::kTmemCols);
     }

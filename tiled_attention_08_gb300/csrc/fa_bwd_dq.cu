@@ -9,9 +9,11 @@
 //   dQ_i += dS K_j                                   (A operand = 16-bit dS written to TMEM)
 // dQ_i is scaled by the softmax scale and written once: no atomics, deterministic.
 //
-// CTA roles (192 threads): warps 0-3 elementwise (thread = query row = TMEM lane), warp 4 TMA
-// producer (Q_i, dO_i once; K_j, V_j per stage), warp 5 MMA issuer + TMEM owner.
-// TMEM: S [0,128), dP [128,256), dQ [256,256+D).
+// CTA roles (320 threads): warps 0-7 elementwise (warp w: query rows 32*(w%4).. == TMEM
+// lanes, key columns [64*(w/4), +64)), warp 8 TMA producer (Q_i, dO_i once; K_j, V_j per
+// stage), warp 9 MMA issuer + TMEM owner.  The MMA warp issues S, then dP; the elementwise
+// warps start on P as soon as S lands, so the dP MMA runs under that work.
+// TMEM: S [0,128), dP [128,256), dQ [256,256+D); the 16-bit dS overwrites S's first 64 columns.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -28,7 +30,13 @@ struct DqCfg {
     static constexpr int kOffK = 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
     static constexpr int kSmemBytes = kOffV + kStages * kTileBytes + 1024;
-    static constexpr int kThreads = 192;
+    static constexpr int kEwWarps = 8;
+    static constexpr int kEwThreads = kEwWarps * 32;
+    static constexpr int kProducerWarp = kEwWarps;
+    static constexpr int kMmaWarp = kEwWarps + 1;
+    static constexpr int kThreads = (kEwWarps + 2) * 32;
+    static constexpr int kCols = 64;        // key columns per elementwise warp
+    static constexpr int kOutCols = D / 2;  // dQ columns per elementwise warp
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmDQ = 256;
     static constexpr uint32_t kIdescS = idesc_f16(BF16, 128, 128, false, false);
@@ -36,21 +44,23 @@ struct DqCfg {
 };
 
 template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(192, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = DqCfg<D, BF16, CAUSAL>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    __shared__ uint64_t bar_qd, bar_kvf[C::kStages], bar_kve[C::kStages], bar_sf, bar_pf, bar_done,
-        bar_fin;
+    __shared__ uint64_t bar_qd, bar_kvf[C::kStages], bar_kve[C::kStages], bar_sf, bar_df, bar_pd,
+        bar_done, bar_fin;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int tile_id = blockIdx.x;
-    const int bh = tile_id % p.BH;
-    const int qt = p.n_tiles - 1 - tile_id / p.BH;  // heaviest query tiles first
+    // Heads in L2-sized groups (their K/V are streamed by every query tile); inside a group
+    // the heaviest query tiles first.
+    int bh, rank;
+    tile_coords(blockIdx.x, p.BH, p.n_tiles, p.group, bh, rank);
+    const int qt = p.n_tiles - 1 - rank;
     const int n_kv = CAUSAL ? (qt + 1) : p.n_tiles;
     volatile int* abort_v = &abort_flag;
 
@@ -62,18 +72,19 @@ __global__ void __launch_bounds__(192, 1) fa_bwd_dq_kernel(const __grid_constant
             mbar_init(&bar_kve[s], 1);
         }
         mbar_init(&bar_sf, 1);
-        mbar_init(&bar_pf, 128);
+        mbar_init(&bar_df, 1);
+        mbar_init(&bar_pd, C::kEwThreads);
         mbar_init(&bar_done, 1);
         mbar_init(&bar_fin, 1);
         mbar_fence_init();
     }
-    if (warp == 5) tmem_alloc(&tmem_base_sh, C::kTmemCols);
+    if (warp == C::kMmaWarp) tmem_alloc(&tmem_base_sh, C::kTmemCols);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_base_sh;
 
-    if (warp == 4) {
+    if (warp == C::kProducerWarp) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
             tma_prefetch_desc(&p.tm_q);
@@ -111,7 +122,7 @@ __global__ void __launch_bounds__(192, 1) fa_bwd_dq_kernel(const __grid_constant
                 wait_bounded(&bar_kvf[j % C::kStages], (uint32_t)(j / C::kStages) & 1u, nullptr,
                              p.timeout_ns);
         }
-    } else if (warp == 5) {
+    } else if (warp == C::kMmaWarp) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
             const uint32_t q_base = smem_u32(smem + C::kOffQ);
@@ -133,14 +144,15 @@ __global__ void __launch_bounds__(192, 1) fa_bwd_dq_kernel(const __grid_constant
                     mma_ss(tmem + C::kTmS, sdesc_kmajor_sw128(q_base + off),
                            sdesc_kmajor_sw128(k_base + off), C::kIdescS, kk > 0 ? 1u : 0u);
                 }
+                mma_commit(&bar_sf);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
                     mma_ss(tmem + C::kTmDP, sdesc_kmajor_sw128(do_base + off),
                            sdesc_kmajor_sw128(v_base + off), C::kIdescS, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(&bar_sf);
-                if (!wait_bounded(&bar_pf, (uint32_t)j & 1u, abort_v, p.timeout_ns)) {
+                mma_commit(&bar_df);
+                if (!wait_bounded(&bar_pd, (uint32_t)j & 1u, abort_v, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
@@ -159,43 +171,63 @@ __global__ void __launch_bounds__(192, 1) fa_bwd_dq_kernel(const __grid_constant
         }
     } else {
         // ------------------------------ elementwise warps ------------------------------
-        const int row = warp * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const int quad = warp & 3;            // TMEM lane quadrant (query rows)
+        const int half = warp >> 2;           // which 64 key columns
+        const uint32_t pair_bar = 1 + quad;   // named barrier shared with the other half
+        const int row = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const int q_row = qt * kTileRows + row;  // < Lpad always
+        const int c0 = half * C::kCols;
         const float lse2 = p.lse2_pad[(size_t)bh * p.Lpad + q_row];
         const float dlt = p.delta_pad[(size_t)bh * p.Lpad + q_row];
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
+            const int key0 = j * kTileRows + c0;
+            const bool masked = (CAUSAL && j == n_kv - 1) || (j * kTileRows + kTileRows > p.L);
+            const int klim = CAUSAL ? min(p.L - 1, q_row) : (p.L - 1);
+            float pv[64];
             ok = wait_bounded(&bar_sf, (uint32_t)j & 1u, abort_v, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after_sync();
-            const int key0 = j * kTileRows;
-            const bool masked = (CAUSAL && j == n_kv - 1) || (key0 + kTileRows > p.L);
-            const int klim = CAUSAL ? min(p.L - 1, q_row) : (p.L - 1);
+            if (ok) {
+                tc_fence_after_sync();
+                uint32_t ra[32], rb[32];
+                tmem_ld32x2(tmem + lane_off + C::kTmS + c0, tmem + lane_off + C::kTmS + c0 + 32, ra,
+                            rb);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_off + C::kTmS + c * 32, sr);
-                tmem_ld32(tmem + lane_off + C::kTmDP + c * 32, dr);
-                uint32_t pd[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float dsv[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int col = c * 32 + 2 * i + e;
-                        float pr = ex2_approx(fmaf(__uint_as_float(sr[2 * i + e]), p.scale_log2, -lse2));
-                        if (masked && key0 + col > klim) pr = 0.0f;
-                        dsv[e] = pr * (__uint_as_float(dr[2 * i + e]) - dlt);
-                    }
-                    pd[i] = pack2<BF16>(dsv[0], dsv[1]);
+                for (int i = 0; i < 32; ++i) {
+                    pv[i] = ex2_approx(fmaf(__uint_as_float(ra[i]), p.scale_log2, -lse2));
+                    pv[32 + i] = ex2_approx(fmaf(__uint_as_float(rb[i]), p.scale_log2, -lse2));
                 }
-                tmem_st16(tmem + lane_off + C::kTmS + c * 16, pd);
+                if (masked) {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i)
+                        if (key0 + i > klim) pv[i] = 0.0f;
+                }
+                ok = wait_bounded(&bar_df, (uint32_t)j & 1u, abort_v, p.timeout_ns);
+                ok = __all_sync(0xffffffffu, ok);
+            }
+            if (ok) {
+                tc_fence_after_sync();
+                uint32_t ra[32], rb[32];
+                tmem_ld32x2(tmem + lane_off + C::kTmDP + c0, tmem + lane_off + C::kTmDP + c0 + 32,
+                            ra, rb);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    pv[i] = pv[i] * (__uint_as_float(ra[i]) - dlt);
+                    pv[32 + i] = pv[32 + i] * (__uint_as_float(rb[i]) - dlt);
+                }
+            }
+            ok = bar_and(pair_bar, 64, ok);  // both halves have read S: dS may overwrite it
+            if (!ok) break;
+            {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
+                tmem_st32(tmem + lane_off + C::kTmS + half * 32, pk);
             }
             tmem_st_wait();
             tc_fence_before_sync();
-            mbar_arrive(&bar_pf);
+            mbar_arrive(&bar_pd);
         }
         if (ok) {
             ok = wait_bounded(&bar_done, 0, abort_v, p.timeout_ns);
@@ -206,11 +238,12 @@ __global__ void __launch_bounds__(192, 1) fa_bwd_dq_kernel(const __grid_constant
         } else {
             tc_fence_after_sync();
             const bool valid = q_row < p.L;
-            uint8_t* dst_row = reinterpret_cast<uint8_t*>(p.dq) + ((size_t)bh * p.L + q_row) * D * 2;
+            uint8_t* dst_row = reinterpret_cast<uint8_t*>(p.dq) +
+                               ((size_t)bh * p.L + q_row) * D * 2 + half * C::kOutCols * 2;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < C::kOutCols / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_off + C::kTmDQ + c * 32, r);
+                tmem_ld32(tmem + lane_off + C::kTmDQ + half * C::kOutCols + c * 32, r);
                 if (valid) {
                     uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 64);
 #pragma unroll
@@ -233,7 +266,7 @@ __global__ void __launch_bounds__(192, 1) fa_bwd_dq_kernel(const __grid_constant
 
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == C::kMmaWarp) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, C::kTmemCols);
     }

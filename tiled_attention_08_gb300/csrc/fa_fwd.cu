@@ -8,10 +8,14 @@
 // PV run in this one kernel ("FlashAttention principles and engineering practice",
 // section 1, kernel fusion), so S and P never reach global memory.
 //
-// CTA roles (192 threads, one CTA per (b*h, query tile)):
-//   warps 0-3  softmax: thread t of warp w owns query row 32*w + t == TMEM lane;
-//   warp 4     TMA producer: Q once, then K_j / V_j into a ring of shared-memory stages;
-//   warp 5     MMA issuer (one thread) and TMEM owner.
+// CTA roles (352 threads, one CTA per (b*h, query tile)):
+//   warps 0-7  softmax: warp w owns TMEM lanes 32*(w%4).. (query rows) and the key columns
+//              [64*(w/4), 64*(w/4)+64) of each S tile; the two warps sharing a lane quadrant
+//              combine their partial row maxima through shared memory;
+//   warp 8     TMA producer of Q (once) and the K_j ring;
+//   warp 9     MMA issuer (one thread) and TMEM owner;
+//   warp 10    TMA producer of the V_j ring (V_j is consumed a softmax later than K_j, so the
+//              two rings advance independently and K runs further ahead).
 // TMEM columns: S double buffer at [0,128) and [128,256) (fp32); the 16-bit P of a tile
 // overwrites the first 64 columns of its S buffer and feeds the PV MMA straight from TMEM;
 // O (fp32, D columns) at [256, 256+D).
@@ -33,12 +37,20 @@ template <int D, bool BF16, bool CAUSAL>
 struct FwdCfg {
     static constexpr int kChunks = D / kChunkElems;            // swizzle boxes per tile row
     static constexpr int kTileBytes = kTileRows * D * 2;       // one 128 x D tile
-    static constexpr int kStages = (D == 128) ? 2 : 4;         // K and V ring depth
+    static constexpr int kKStages = (D == 128) ? 3 : 4;        // K ring depth
+    static constexpr int kVStages = (D == 128) ? 2 : 4;        // V ring depth
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kTileBytes;
-    static constexpr int kOffV = kOffK + kStages * kTileBytes;
-    static constexpr int kSmemBytes = kOffV + kStages * kTileBytes + 1024;  // + alignment slack
-    static constexpr int kThreads = 192;
+    static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+    static constexpr int kSmemBytes = kOffV + kVStages * kTileBytes + 1024;  // + alignment slack
+    static constexpr int kSoftmaxWarps = 8;
+    static constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+    static constexpr int kProducerWarp = kSoftmaxWarps;
+    static constexpr int kMmaWarp = kSoftmaxWarps + 1;
+    static constexpr int kVProducerWarp = kSoftmaxWarps + 2;
+    static constexpr int kThreads = (kSoftmaxWarps + 3) * 32;
+    static constexpr int kCols = 64;       // S columns per softmax warp
+    static constexpr int kOCols = D / 2;   // O columns per softmax warp
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kTmS = 0;    // S buffer b at kTmS + 128*b
     static constexpr uint32_t kTmO = 256;  // O accumulator
@@ -47,102 +59,102 @@ struct FwdCfg {
 };
 
 template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(192, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(352, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = FwdCfg<D, BF16, CAUSAL>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    __shared__ uint64_t bar_q, bar_kf[C::kStages], bar_ke[C::kStages], bar_vf[C::kStages],
-        bar_ve[C::kStages], bar_sf[2], bar_pf[2], bar_od, bar_fin;
+    __shared__ uint64_t bar_q, bar_kf[C::kKStages], bar_ke[C::kKStages], bar_vf[C::kVStages],
+        bar_ve[C::kVStages], bar_sf[2], bar_pf[2], bar_od, bar_fin;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
+    __shared__ float red_max[2][2][128];  // [tile parity][column half][row]
+    __shared__ float red_sum[2][128];     // [column half][row]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Heaviest query tiles (most key tiles under the causal mask) are scheduled first.
-    const int tile_id = blockIdx.x;
-    const int bh = tile_id % p.BH;
-    const int qt = p.n_tiles - 1 - tile_id / p.BH;
+    // Heads in L2-sized groups; inside a group the heaviest query tiles (most key tiles under
+    // the causal mask) go first.
+    int bh, rank;
+    tile_coords(blockIdx.x, p.BH, p.n_tiles, p.group, bh, rank);
+    const int qt = p.n_tiles - 1 - rank;
     const int n_kv = CAUSAL ? (qt + 1) : p.n_tiles;
     volatile int* abort_v = &abort_flag;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(&bar_q, 1);
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(&bar_kf[s], 1);
             mbar_init(&bar_ke[s], 1);
+        }
+        for (int s = 0; s < C::kVStages; ++s) {
             mbar_init(&bar_vf[s], 1);
             mbar_init(&bar_ve[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bar_sf[b], 1);
-            mbar_init(&bar_pf[b], 128);
+            mbar_init(&bar_pf[b], C::kSoftmaxThreads);
         }
         mbar_init(&bar_od, 1);
         mbar_init(&bar_fin, 1);
         mbar_fence_init();
     }
-    if (warp == 5) tmem_alloc(&tmem_base_sh, C::kTmemCols);
+    if (warp == C::kMmaWarp) tmem_alloc(&tmem_base_sh, C::kTmemCols);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_base_sh;
 
-    if (warp == 4) {
-        // ------------------------------ TMA producer ------------------------------
+    if (warp == C::kProducerWarp || warp == C::kVProducerWarp) {
+        // ------------------------------ TMA producers ------------------------------
+        // One ring per warp: Q + K on kProducerWarp, V on kVProducerWarp.
         if (lane == 0) {
-            tma_prefetch_desc(&p.tm_q);
-            tma_prefetch_desc(&p.tm_k);
-            tma_prefetch_desc(&p.tm_v);
-            mbar_arrive_expect_tx(&bar_q, C::kTileBytes);
-            for (int c = 0; c < C::kChunks; ++c)
-                tma_load_3d(smem + C::kOffQ + c * kChunkBytes, &p.tm_q, &bar_q, c * kChunkElems,
-                            qt * kTileRows, bh);
+            const bool is_k = warp == C::kProducerWarp;
+            const CUtensorMap* map = is_k ? &p.tm_k : &p.tm_v;
+            const int stages = is_k ? C::kKStages : C::kVStages;
+            uint64_t* full = is_k ? bar_kf : bar_vf;
+            uint64_t* empty = is_k ? bar_ke : bar_ve;
+            uint8_t* ring = smem + (is_k ? C::kOffK : C::kOffV);
+            tma_prefetch_desc(map);
+            if (is_k) {
+                tma_prefetch_desc(&p.tm_q);
+                mbar_arrive_expect_tx(&bar_q, C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(smem + C::kOffQ + c * kChunkBytes, &p.tm_q, &bar_q,
+                                c * kChunkElems, qt * kTileRows, bh);
+            }
             bool ok = true;
-            int issued_k = 0, issued_v = 0;  // fills handed to the TMA unit
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int st = j % C::kStages;
-                const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
-                if (j >= C::kStages && !wait_bounded(&bar_ke[st], ph ^ 1u, abort_v, p.timeout_ns)) {
+            int issued = 0;  // fills handed to the TMA unit
+            for (int j = 0; j < n_kv; ++j) {
+                const int st = j % stages;
+                const uint32_t ph = (uint32_t)(j / stages) & 1u;
+                if (j >= stages && !wait_bounded(&empty[st], ph ^ 1u, abort_v, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&bar_kf[st], C::kTileBytes);
+                mbar_arrive_expect_tx(&full[st], C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(smem + C::kOffK + st * C::kTileBytes + c * kChunkBytes, &p.tm_k,
-                                &bar_kf[st], c * kChunkElems, j * kTileRows, bh);
-                issued_k = j + 1;
-                if (j >= C::kStages && !wait_bounded(&bar_ve[st], ph ^ 1u, abort_v, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&bar_vf[st], C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(smem + C::kOffV + st * C::kTileBytes + c * kChunkBytes, &p.tm_v,
-                                &bar_vf[st], c * kChunkElems, j * kTileRows, bh);
-                issued_v = j + 1;
+                    tma_load_3d(ring + st * C::kTileBytes + c * kChunkBytes, map, &full[st],
+                                c * kChunkElems, j * kTileRows, bh);
+                issued = j + 1;
             }
             if (!ok) record_timeout(p.status, abort_v);
             // Drain: the newest fill of every stage must have landed before the CTA exits.
             // (These waits return at once on the normal path.)
-            wait_bounded(&bar_q, 0, nullptr, p.timeout_ns);
-            for (int j = issued_k - 1; j >= 0 && j >= issued_k - C::kStages; --j)
-                wait_bounded(&bar_kf[j % C::kStages], (uint32_t)(j / C::kStages) & 1u, nullptr,
-                             p.timeout_ns);
-            for (int j = issued_v - 1; j >= 0 && j >= issued_v - C::kStages; --j)
-                wait_bounded(&bar_vf[j % C::kStages], (uint32_t)(j / C::kStages) & 1u, nullptr,
-                             p.timeout_ns);
+            if (is_k) wait_bounded(&bar_q, 0, nullptr, p.timeout_ns);
+            for (int j = issued - 1; j >= 0 && j >= issued - stages; --j)
+                wait_bounded(&full[j % stages], (uint32_t)(j / stages) & 1u, nullptr, p.timeout_ns);
         }
-    } else if (warp == 5) {
+    } else if (warp == C::kMmaWarp) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
             const uint32_t q_base = smem_u32(smem + C::kOffQ);
             bool ok = wait_bounded(&bar_q, 0, abort_v, p.timeout_ns);
             auto issue_pv = [&](int jj) -> bool {
                 const int b = jj & 1;
-                const int st = jj % C::kStages;
-                const uint32_t ph = (uint32_t)(jj / C::kStages) & 1u;
+                const int st = jj % C::kVStages;
+                const uint32_t ph = (uint32_t)(jj / C::kVStages) & 1u;
                 if (!wait_bounded(&bar_pf[b], (uint32_t)(jj >> 1) & 1u, abort_v, p.timeout_ns))
                     return false;
                 if (!wait_bounded(&bar_vf[st], ph, abort_v, p.timeout_ns)) return false;
@@ -159,8 +171,8 @@ __global__ void __launch_bounds__(192, 1) fa_fwd_kernel(const __grid_constant__ 
                 return true;
             };
             for (int j = 0; j < n_kv && ok; ++j) {
-                const int st = j % C::kStages;
-                const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
+                const int st = j % C::kKStages;
+                const uint32_t ph = (uint32_t)(j / C::kKStages) & 1u;
                 const int b = j & 1;
                 if (!wait_bounded(&bar_kf[st], ph, abort_v, p.timeout_ns)) {
                     ok = false;
@@ -186,37 +198,48 @@ __global__ void __launch_bounds__(192, 1) fa_fwd_kernel(const __grid_constant__ 
         }
     } else {
         // ------------------------------ softmax warps ------------------------------
-        const int row = warp * 32 + lane;  // row inside the tile == TMEM lane
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const int quad = warp & 3;       // TMEM lane quadrant
+        const int half = warp >> 2;      // which 64 key columns of the tile
+        const uint32_t pair_bar = 1 + quad;  // named barrier shared with the other half
+        const int row = quad * 32 + lane;    // row inside the tile == TMEM lane
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const int q_row = qt * kTileRows + row;
+        const int c0 = half * C::kCols;
         float m_ref = -INFINITY;
-        float l_sum = 0.0f;
+        float l_sum = 0.0f;  // over this warp's columns only
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             const int b = j & 1;
             ok = wait_bounded(&bar_sf[b], (uint32_t)(j >> 1) & 1u, abort_v, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after_sync();
             const uint32_t s_addr = tmem + lane_off + C::kTmS + 128 * b;
-            float s[128];
+            float s[64];
+            float mx = -INFINITY;
+            if (ok) {
+                tc_fence_after_sync();
+                uint32_t ra[32], rb[32];
+                tmem_ld32x2(s_addr + c0, s_addr + c0 + 32, ra, rb);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld32(s_addr + c * 32, r);
+                for (int i = 0; i < 32; ++i) {
+                    s[i] = __uint_as_float(ra[i]);
+                    s[32 + i] = __uint_as_float(rb[i]);
+                }
+                const int key0 = j * kTileRows + c0;
+                if ((CAUSAL && j == n_kv - 1) || j * kTileRows + kTileRows > p.L) {
+                    const int lim = CAUSAL ? min(p.L - 1, q_row) : (p.L - 1);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+                    for (int c = 0; c < 64; ++c)
+                        if (key0 + c > lim) s[c] = -INFINITY;
+                }
+#pragma unroll
+                for (int c = 0; c < 64; ++c) mx = fmaxf(mx, s[c]);
+                red_max[b][half][row] = mx;
             }
-            const int key0 = j * kTileRows;
-            if ((CAUSAL && j == n_kv - 1) || key0 + kTileRows > p.L) {
-                const int lim = CAUSAL ? min(p.L - 1, q_row) : (p.L - 1);
-#pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (key0 + c > lim) s[c] = -INFINITY;
-            }
-            float mx = s[0];
-#pragma unroll
-            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+            // Both halves have read their S columns (P may now overwrite them) and published
+            // their partial maxima.
+            ok = bar_and(pair_bar, 64, ok);
+            if (!ok) break;
+            mx = fmaxf(mx, red_max[b][half ^ 1][row]);
             const float m_cand = mx * p.scale_log2;
             float m_new = m_ref;
             if (m_cand > m_ref + kRescaleThreshold) m_new = m_cand;
@@ -224,38 +247,39 @@ __global__ void __launch_bounds__(192, 1) fa_fwd_kernel(const __grid_constant__ 
             const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
             const float alpha = rescale ? ex2_approx(m_ref - m_new) : 1.0f;
             float sum = 0.0f;
+            uint32_t pk[32];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float p0 = ex2_approx(fmaf(s[h * 64 + 2 * i], p.scale_log2, -m_use));
-                    const float p1 = ex2_approx(fmaf(s[h * 64 + 2 * i + 1], p.scale_log2, -m_use));
-                    sum += p0 + p1;
-                    pk[i] = pack2<BF16>(p0, p1);
-                }
-                tmem_st32(s_addr + h * 32, pk);
+            for (int i = 0; i < 32; ++i) {
+                const float p0 = ex2_approx(fmaf(s[2 * i], p.scale_log2, -m_use));
+                const float p1 = ex2_approx(fmaf(s[2 * i + 1], p.scale_log2, -m_use));
+                sum += p0 + p1;
+                pk[i] = pack2<BF16>(p0, p1);
             }
+            tmem_st32(tmem + lane_off + C::kTmS + 128 * b + half * 32, pk);
             l_sum = l_sum * alpha + sum;
+            bool okr = true;
             if (__any_sync(0xffffffffu, rescale)) {
                 // O holds the sum up to tile j-1: wait for that PV, then rescale in place.
-                bool okw = wait_bounded(&bar_od, (uint32_t)(j - 1) & 1u, abort_v, p.timeout_ns);
-                okw = __all_sync(0xffffffffu, okw);
-                if (!okw) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                const uint32_t o_addr = tmem + lane_off + C::kTmO;
+                okr = wait_bounded(&bar_od, (uint32_t)(j - 1) & 1u, abort_v, p.timeout_ns);
+                okr = __all_sync(0xffffffffu, okr);
+                if (okr) {
+                    tc_fence_after_sync();
+                    const uint32_t o_addr = tmem + lane_off + C::kTmO + half * C::kOCols;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(o_addr + c * 32, r);
+                    for (int c = 0; c < C::kOCols / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(o_addr + c * 32, r);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                    tmem_st32(o_addr + c * 32, r);
+                        for (int i = 0; i < 32; ++i)
+                            r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st32(o_addr + c * 32, r);
+                    }
                 }
+            }
+            okr = bar_and(pair_bar, 64, okr);
+            if (!okr) {
+                ok = false;
+                break;
             }
             tmem_st_wait();
             tc_fence_before_sync();
@@ -266,17 +290,21 @@ __global__ void __launch_bounds__(192, 1) fa_fwd_kernel(const __grid_constant__ 
             ok = wait_bounded(&bar_od, (uint32_t)(n_kv - 1) & 1u, abort_v, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
         }
+        red_sum[half][row] = l_sum;
+        ok = bar_and(pair_bar, 64, ok);
         if (!ok) {
             if (lane == 0) record_timeout(p.status, abort_v);
         } else {
             tc_fence_after_sync();
+            const float l_tot = l_sum + red_sum[half ^ 1][row];
             const bool valid = q_row < p.L;
-            const float inv_l = 1.0f / l_sum;
-            if (valid) p.lse[(size_t)bh * p.L + q_row] = (m_ref + log2f(l_sum)) * kLn2;
-            uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) + ((size_t)bh * p.L + q_row) * D * 2;
-            const uint32_t o_addr = tmem + lane_off + C::kTmO;
+            const float inv_l = 1.0f / l_tot;
+            if (valid && half == 0) p.lse[(size_t)bh * p.L + q_row] = (m_ref + log2f(l_tot)) * kLn2;
+            uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) + ((size_t)bh * p.L + q_row) * D * 2 +
+                            half * C::kOCols * 2;
+            const uint32_t o_addr = tmem + lane_off + C::kTmO + half * C::kOCols;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < C::kOCols / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld32(o_addr + c * 32, r);
                 if (valid) {
@@ -301,7 +329,7 @@ __global__ void __launch_bounds__(192, 1) fa_fwd_kernel(const __grid_constant__ 
 
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == C::kMmaWarp) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, C::kTmemCols);
     }

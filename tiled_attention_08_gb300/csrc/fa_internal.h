@@ -19,6 +19,21 @@ constexpr int kTileRows = 128;
 constexpr int kChunkElems = 64;
 constexpr int kChunkBytes = kTileRows * kChunkElems * 2;  // 16 KiB per box
 
+// Tile schedule shared by the attention kernels.  Heads are taken in groups of `group`
+// (chosen on the host so that a group's streamed operands fit in L2 with room to spare);
+// inside a group, tiles go heaviest first across all of the group's heads.  Returns the head
+// and the tile's rank by weight (0 = heaviest: the last query tile, or key tile 0, under the
+// causal mask).
+__host__ __device__ __forceinline__ void tile_coords(int tile_id, int BH, int n_tiles, int group,
+                                                     int& bh, int& rank) {
+    const int span = group * n_tiles;
+    const int g = tile_id / span;
+    const int r = tile_id - g * span;
+    const int heads = (BH - g * group) < group ? (BH - g * group) : group;
+    rank = r / heads;
+    bh = g * group + (r - rank * heads);
+}
+
 struct FwdParams {
     CUtensorMap tm_q, tm_k, tm_v;  // [BH, L, D] 16-bit, box {64, 128, 1}
     void* o;                       // [BH, L, D] 16-bit
@@ -26,6 +41,7 @@ struct FwdParams {
     int L;
     int BH;
     int n_tiles;        // ceil(L / 128)
+    int group;          // heads per schedule group (tile_coords)
     float scale_log2;   // scale * log2(e)
     int* status;        // device status word
     uint64_t timeout_ns;
@@ -49,6 +65,7 @@ struct BwdParams {
     void* dk;
     void* dv;
     int L, Lpad, BH, n_tiles;
+    int group;          // heads per schedule group (tile_coords)
     float scale;        // softmax scale (applied to dQ and dK)
     float scale_log2;   // scale * log2(e)
     int* status;
