@@ -11,9 +11,9 @@
 //   dV_j += P^T dO_i,  dK_j += dS^T Q_i   (A operand = 16-bit P^T / dS^T written back to TMEM)
 // and at the end dK_j is multiplied by the softmax scale.
 //
-// CTA roles (320 threads): warps 0-7 elementwise (warp w: key rows 32*(w%4).. == TMEM lanes,
-// query columns [64*(w/4), +64)), warp 8 TMA producer (K_j, V_j once; Q_i, dO_i, LSE_i,
-// Delta_i per stage), warp 9 MMA issuer + TMEM owner.  Per query tile the MMA warp issues
+// CTA roles: 4*kSplit elementwise warps (warp w: key rows 32*(w%4).. == TMEM lanes, query
+// columns [kCols*(w/4), +kCols)), then one TMA producer warp (K_j, V_j once; Q_i, dO_i,
+// LSE_i, Delta_i per stage) and one MMA-issuer warp that also owns TMEM.  Per query tile the MMA warp issues
 // S^T, then dP^T; the elementwise warps turn S^T into P^T (which releases the dV MMA) and
 // then dP^T into dS^T (which releases the dK MMA), so dP^T and dV run under the elementwise
 // work.  TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D); the 16-bit
@@ -36,13 +36,14 @@ struct DkdvCfg {
     static constexpr int kOffDO = kOffQ + kStages * kTileBytes;
     static constexpr int kOffVec = kOffDO + kStages * kTileBytes;
     static constexpr int kSmemBytes = kOffVec + kStages * kVecBytes + 1024;
-    static constexpr int kEwWarps = 8;
+    static constexpr int kSplit = 4;  // elementwise warps per TMEM lane quadrant
+    static constexpr int kEwWarps = 4 * kSplit;
     static constexpr int kEwThreads = kEwWarps * 32;
     static constexpr int kProducerWarp = kEwWarps;
     static constexpr int kMmaWarp = kEwWarps + 1;
     static constexpr int kThreads = (kEwWarps + 2) * 32;
-    static constexpr int kCols = 64;      // query columns per elementwise warp
-    static constexpr int kOutCols = D / 2;  // dK/dV columns per elementwise warp
+    static constexpr int kCols = 128 / kSplit;  // query columns per elementwise warp
+    static constexpr int kOutCols = D / kSplit;  // dK/dV columns per elementwise warp
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kTmST = 0, kTmDPT = 128, kTmDV = 256, kTmDK = 256 + D;
     static constexpr uint32_t kIdescS = idesc_f16(BF16, 128, 128, false, false);
@@ -50,7 +51,8 @@ struct DkdvCfg {
 };
 
 template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = DkdvCfg<D, BF16, CAUSAL>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -194,13 +196,15 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
         }
     } else {
         // ------------------------------ elementwise warps ------------------------------
-        const int quad = warp & 3;            // TMEM lane quadrant (key rows)
-        const int half = warp >> 2;           // which 64 query columns
-        const uint32_t pair_bar = 1 + quad;   // named barrier shared with the other half
+        constexpr int kC = C::kCols;
+        const int quad = warp & 3;              // TMEM lane quadrant (key rows)
+        const int part = warp >> 2;             // which kC query columns
+        const uint32_t grp_bar = 1 + quad;      // named barrier of the quadrant
+        constexpr uint32_t kGrpThreads = 32 * C::kSplit;
         const int row = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const int key = kt * kTileRows + row;
-        const int c0 = half * C::kCols;
+        const int c0 = part * kC;
         bool ok = true;
         for (int t = 0; t < n_it; ++t) {
             const int it = it0 + t;
@@ -216,33 +220,29 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
             ok = wait_bounded(&bar_qf[st], ph, abort_v, p.timeout_ns) &&
                  wait_bounded(&bar_sf, (uint32_t)t & 1u, abort_v, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
-            float pv[64];
+            float pv[kC];
             if (ok) {
                 tc_fence_after_sync();
-                uint32_t ra[32], rb[32];
-                tmem_ld32x2(tmem + lane_off + C::kTmST + c0, tmem + lane_off + C::kTmST + c0 + 32,
-                            ra, rb);
+                uint32_t r[kC];
+                tmem_ld_cols<kC>(tmem + lane_off + C::kTmST + c0, r);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    pv[i] = ex2_approx(fmaf(__uint_as_float(ra[i]), p.scale_log2, -lse2v[i]));
-                    pv[32 + i] =
-                        ex2_approx(fmaf(__uint_as_float(rb[i]), p.scale_log2, -lse2v[32 + i]));
-                }
+                for (int i = 0; i < kC; ++i)
+                    pv[i] = ex2_approx(fmaf(__uint_as_float(r[i]), p.scale_log2, -lse2v[i]));
                 if (masked) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) {
+                    for (int i = 0; i < kC; ++i) {
                         const int qg = q0 + i;
                         if (qg > qlim || (CAUSAL && key > qg)) pv[i] = 0.0f;
                     }
                 }
             }
-            ok = bar_and(pair_bar, 64, ok);  // both halves have read S^T: P^T may overwrite it
+            ok = bar_and(grp_bar, kGrpThreads, ok);  // all slices read S^T: P^T may overwrite it
             if (!ok) break;
             {
-                uint32_t pk[32];
+                uint32_t pk[kC / 2];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
-                tmem_st32(tmem + lane_off + C::kTmST + half * 32, pk);
+                for (int i = 0; i < kC / 2; ++i) pk[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
+                tmem_st<kC / 2>(tmem + lane_off + C::kTmST + part * (kC / 2), pk);
             }
             tmem_st_wait();
             tc_fence_before_sync();
@@ -252,22 +252,18 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after_sync();
-                uint32_t ra[32], rb[32];
-                tmem_ld32x2(tmem + lane_off + C::kTmDPT + c0,
-                            tmem + lane_off + C::kTmDPT + c0 + 32, ra, rb);
+                uint32_t r[kC];
+                tmem_ld_cols<kC>(tmem + lane_off + C::kTmDPT + c0, r);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    pv[i] = pv[i] * (__uint_as_float(ra[i]) - dltv[i]);
-                    pv[32 + i] = pv[32 + i] * (__uint_as_float(rb[i]) - dltv[32 + i]);
-                }
+                for (int i = 0; i < kC; ++i) pv[i] = pv[i] * (__uint_as_float(r[i]) - dltv[i]);
             }
-            ok = bar_and(pair_bar, 64, ok);  // both halves have read dP^T
+            ok = bar_and(grp_bar, kGrpThreads, ok);  // all slices have read dP^T
             if (!ok) break;
             {
-                uint32_t pk[32];
+                uint32_t pk[kC / 2];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
-                tmem_st32(tmem + lane_off + C::kTmDPT + half * 32, pk);
+                for (int i = 0; i < kC / 2; ++i) pk[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
+                tmem_st<kC / 2>(tmem + lane_off + C::kTmDPT + part * (kC / 2), pk);
             }
             tmem_st_wait();
             tc_fence_before_sync();
@@ -282,34 +278,13 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
         } else {
             tc_fence_after_sync();
             const bool valid = key < p.L;
-            const size_t roff = ((size_t)bh * p.L + key) * D * 2 + half * C::kOutCols * 2;
-#pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t col0 = (which ? C::kTmDK : C::kTmDV) + half * C::kOutCols;
-                const float mul = which ? p.scale : 1.0f;
-                uint8_t* dst_row = reinterpret_cast<uint8_t*>(which ? p.dk : p.dv) + roff;
-#pragma unroll
-                for (int c = 0; c < C::kOutCols / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_off + col0 + c * 32, r);
-                    if (valid) {
-                        uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 64);
-#pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4) {
-                            uint4 w;
-                            w.x = pack2<BF16>(__uint_as_float(r[v4 * 8 + 0]) * mul,
-                                              __uint_as_float(r[v4 * 8 + 1]) * mul);
-                            w.y = pack2<BF16>(__uint_as_float(r[v4 * 8 + 2]) * mul,
-                                              __uint_as_float(r[v4 * 8 + 3]) * mul);
-                            w.z = pack2<BF16>(__uint_as_float(r[v4 * 8 + 4]) * mul,
-                                              __uint_as_float(r[v4 * 8 + 5]) * mul);
-                            w.w = pack2<BF16>(__uint_as_float(r[v4 * 8 + 6]) * mul,
-                                              __uint_as_float(r[v4 * 8 + 7]) * mul);
-                            dst[v4] = w;
-                        }
-                    }
-                }
-            }
+            const size_t roff = ((size_t)bh * p.L + key) * D * 2 + part * C::kOutCols * 2;
+            tmem_row_to_global<BF16, C::kOutCols>(
+                tmem + lane_off + C::kTmDV + part * C::kOutCols,
+                reinterpret_cast<uint8_t*>(p.dv) + roff, 1.0f, valid);
+            tmem_row_to_global<BF16, C::kOutCols>(
+                tmem + lane_off + C::kTmDK + part * C::kOutCols,
+                reinterpret_cast<uint8_t*>(p.dk) + roff, p.scale, valid);
         }
     }
 

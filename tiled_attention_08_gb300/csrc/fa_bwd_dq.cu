@@ -9,9 +9,9 @@
 //   dQ_i += dS K_j                                   (A operand = 16-bit dS written to TMEM)
 // dQ_i is scaled by the softmax scale and written once: no atomics, deterministic.
 //
-// CTA roles (320 threads): warps 0-7 elementwise (warp w: query rows 32*(w%4).. == TMEM
-// lanes, key columns [64*(w/4), +64)), warp 8 TMA producer (Q_i, dO_i once; K_j, V_j per
-// stage), warp 9 MMA issuer + TMEM owner.  The MMA warp issues S, then dP; the elementwise
+// CTA roles: 4*kSplit elementwise warps (warp w: query rows 32*(w%4).. == TMEM lanes, key
+// columns [kCols*(w/4), +kCols)), then one TMA producer warp (Q_i, dO_i once; K_j, V_j per
+// stage) and one MMA-issuer warp that also owns TMEM.  The MMA warp issues S, then dP; the elementwise
 // warps start on P as soon as S lands, so the dP MMA runs under that work.
 // TMEM: S [0,128), dP [128,256), dQ [256,256+D); the 16-bit dS overwrites S's first 64 columns.
 #include "fa_internal.h"
@@ -30,13 +30,14 @@ struct DqCfg {
     static constexpr int kOffK = 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
     static constexpr int kSmemBytes = kOffV + kStages * kTileBytes + 1024;
-    static constexpr int kEwWarps = 8;
+    static constexpr int kSplit = 4;  // elementwise warps per TMEM lane quadrant
+    static constexpr int kEwWarps = 4 * kSplit;
     static constexpr int kEwThreads = kEwWarps * 32;
     static constexpr int kProducerWarp = kEwWarps;
     static constexpr int kMmaWarp = kEwWarps + 1;
     static constexpr int kThreads = (kEwWarps + 2) * 32;
-    static constexpr int kCols = 64;        // key columns per elementwise warp
-    static constexpr int kOutCols = D / 2;  // dQ columns per elementwise warp
+    static constexpr int kCols = 128 / kSplit;   // key columns per elementwise warp
+    static constexpr int kOutCols = D / kSplit;  // dQ columns per elementwise warp
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmDQ = 256;
     static constexpr uint32_t kIdescS = idesc_f16(BF16, 128, 128, false, false);
@@ -44,7 +45,8 @@ struct DqCfg {
 };
 
 template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = DqCfg<D, BF16, CAUSAL>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -171,13 +173,15 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
         }
     } else {
         // ------------------------------ elementwise warps ------------------------------
-        const int quad = warp & 3;            // TMEM lane quadrant (query rows)
-        const int half = warp >> 2;           // which 64 key columns
-        const uint32_t pair_bar = 1 + quad;   // named barrier shared with the other half
+        constexpr int kC = C::kCols;
+        const int quad = warp & 3;              // TMEM lane quadrant (query rows)
+        const int part = warp >> 2;             // which kC key columns
+        const uint32_t grp_bar = 1 + quad;      // named barrier of the quadrant
+        constexpr uint32_t kGrpThreads = 32 * C::kSplit;
         const int row = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const int q_row = qt * kTileRows + row;  // < Lpad always
-        const int c0 = half * C::kCols;
+        const int c0 = part * kC;
         const float lse2 = p.lse2_pad[(size_t)bh * p.Lpad + q_row];
         const float dlt = p.delta_pad[(size_t)bh * p.Lpad + q_row];
         bool ok = true;
@@ -185,22 +189,19 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
             const int key0 = j * kTileRows + c0;
             const bool masked = (CAUSAL && j == n_kv - 1) || (j * kTileRows + kTileRows > p.L);
             const int klim = CAUSAL ? min(p.L - 1, q_row) : (p.L - 1);
-            float pv[64];
+            float pv[kC];
             ok = wait_bounded(&bar_sf, (uint32_t)j & 1u, abort_v, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after_sync();
-                uint32_t ra[32], rb[32];
-                tmem_ld32x2(tmem + lane_off + C::kTmS + c0, tmem + lane_off + C::kTmS + c0 + 32, ra,
-                            rb);
+                uint32_t r[kC];
+                tmem_ld_cols<kC>(tmem + lane_off + C::kTmS + c0, r);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    pv[i] = ex2_approx(fmaf(__uint_as_float(ra[i]), p.scale_log2, -lse2));
-                    pv[32 + i] = ex2_approx(fmaf(__uint_as_float(rb[i]), p.scale_log2, -lse2));
-                }
+                for (int i = 0; i < kC; ++i)
+                    pv[i] = ex2_approx(fmaf(__uint_as_float(r[i]), p.scale_log2, -lse2));
                 if (masked) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i)
+                    for (int i = 0; i < kC; ++i)
                         if (key0 + i > klim) pv[i] = 0.0f;
                 }
                 ok = wait_bounded(&bar_df, (uint32_t)j & 1u, abort_v, p.timeout_ns);
@@ -208,22 +209,18 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
             }
             if (ok) {
                 tc_fence_after_sync();
-                uint32_t ra[32], rb[32];
-                tmem_ld32x2(tmem + lane_off + C::kTmDP + c0, tmem + lane_off + C::kTmDP + c0 + 32,
-                            ra, rb);
+                uint32_t r[kC];
+                tmem_ld_cols<kC>(tmem + lane_off + C::kTmDP + c0, r);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    pv[i] = pv[i] * (__uint_as_float(ra[i]) - dlt);
-                    pv[32 + i] = pv[32 + i] * (__uint_as_float(rb[i]) - dlt);
-                }
+                for (int i = 0; i < kC; ++i) pv[i] = pv[i] * (__uint_as_float(r[i]) - dlt);
             }
-            ok = bar_and(pair_bar, 64, ok);  // both halves have read S: dS may overwrite it
+            ok = bar_and(grp_bar, kGrpThreads, ok);  // all slices have read S: dS may overwrite it
             if (!ok) break;
             {
-                uint32_t pk[32];
+                uint32_t pk[kC / 2];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
-                tmem_st32(tmem + lane_off + C::kTmS + half * 32, pk);
+                for (int i = 0; i < kC / 2; ++i) pk[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
+                tmem_st<kC / 2>(tmem + lane_off + C::kTmS + part * (kC / 2), pk);
             }
             tmem_st_wait();
             tc_fence_before_sync();
@@ -237,30 +234,10 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
             if (lane == 0) record_timeout(p.status, abort_v);
         } else {
             tc_fence_after_sync();
-            const bool valid = q_row < p.L;
             uint8_t* dst_row = reinterpret_cast<uint8_t*>(p.dq) +
-                               ((size_t)bh * p.L + q_row) * D * 2 + half * C::kOutCols * 2;
-#pragma unroll
-            for (int c = 0; c < C::kOutCols / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_off + C::kTmDQ + half * C::kOutCols + c * 32, r);
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 64);
-#pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        uint4 w;
-                        w.x = pack2<BF16>(__uint_as_float(r[v4 * 8 + 0]) * p.scale,
-                                          __uint_as_float(r[v4 * 8 + 1]) * p.scale);
-                        w.y = pack2<BF16>(__uint_as_float(r[v4 * 8 + 2]) * p.scale,
-                                          __uint_as_float(r[v4 * 8 + 3]) * p.scale);
-                        w.z = pack2<BF16>(__uint_as_float(r[v4 * 8 + 4]) * p.scale,
-                                          __uint_as_float(r[v4 * 8 + 5]) * p.scale);
-                        w.w = pack2<BF16>(__uint_as_float(r[v4 * 8 + 6]) * p.scale,
-                                          __uint_as_float(r[v4 * 8 + 7]) * p.scale);
-                        dst[v4] = w;
-                    }
-                }
-            }
+                               ((size_t)bh * p.L + q_row) * D * 2 + part * C::kOutCols * 2;
+            tmem_row_to_global<BF16, C::kOutCols>(tmem + lane_off + C::kTmDQ + part * C::kOutCols,
+                                                  dst_row, p.scale, q_row < p.L);
         }
     }
 

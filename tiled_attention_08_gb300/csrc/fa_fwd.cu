@@ -8,13 +8,14 @@
 // PV run in this one kernel ("FlashAttention principles and engineering practice",
 // section 1, kernel fusion), so S and P never reach global memory.
 //
-// CTA roles (352 threads, one CTA per (b*h, query tile)):
-//   warps 0-7  softmax: warp w owns TMEM lanes 32*(w%4).. (query rows) and the key columns
-//              [64*(w/4), 64*(w/4)+64) of each S tile; the two warps sharing a lane quadrant
-//              combine their partial row maxima through shared memory;
-//   warp 8     TMA producer of Q (once) and the K_j ring;
-//   warp 9     MMA issuer (one thread) and TMEM owner;
-//   warp 10    TMA producer of the V_j ring (V_j is consumed a softmax later than K_j, so the
+// CTA roles (one CTA per (b*h, query tile)), with kSplit softmax warps per TMEM lane quadrant:
+//   warps 0 .. 4*kSplit-1  softmax: warp w owns TMEM lanes 32*(w%4).. (query rows) and the
+//              key columns [kCols*(w/4), +kCols) of each S tile (kCols = 128/kSplit); the
+//              kSplit warps sharing a lane quadrant combine their partial row maxima through
+//              shared memory at a named barrier;
+//   next warp  TMA producer of Q (once) and the K_j ring;
+//   next warp  MMA issuer (one thread) and TMEM owner;
+//   last warp  TMA producer of the V_j ring (V_j is consumed a softmax later than K_j, so the
 //              two rings advance independently and K runs further ahead).
 // TMEM columns: S double buffer at [0,128) and [128,256) (fp32); the 16-bit P of a tile
 // overwrites the first 64 columns of its S buffer and feeds the PV MMA straight from TMEM;
@@ -43,14 +44,15 @@ struct FwdCfg {
     static constexpr int kOffK = kOffQ + kTileBytes;
     static constexpr int kOffV = kOffK + kKStages * kTileBytes;
     static constexpr int kSmemBytes = kOffV + kVStages * kTileBytes + 1024;  // + alignment slack
-    static constexpr int kSoftmaxWarps = 8;
+    static constexpr int kSplit = 4;                          // softmax warps per lane quadrant
+    static constexpr int kSoftmaxWarps = 4 * kSplit;
     static constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
     static constexpr int kProducerWarp = kSoftmaxWarps;
     static constexpr int kMmaWarp = kSoftmaxWarps + 1;
     static constexpr int kVProducerWarp = kSoftmaxWarps + 2;
     static constexpr int kThreads = (kSoftmaxWarps + 3) * 32;
-    static constexpr int kCols = 64;       // S columns per softmax warp
-    static constexpr int kOCols = D / 2;   // O columns per softmax warp
+    static constexpr int kCols = 128 / kSplit;                // S columns per softmax warp
+    static constexpr int kOCols = D / kSplit;                 // O columns per softmax warp
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kTmS = 0;    // S buffer b at kTmS + 128*b
     static constexpr uint32_t kTmO = 256;  // O accumulator
@@ -59,17 +61,18 @@ struct FwdCfg {
 };
 
 template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(352, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = FwdCfg<D, BF16, CAUSAL>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     __shared__ uint64_t bar_q, bar_kf[C::kKStages], bar_ke[C::kKStages], bar_vf[C::kVStages],
-        bar_ve[C::kVStages], bar_sf[2], bar_pf[2], bar_od, bar_fin;
+        bar_ve[C::kVStages], bar_sf[2], bar_pf[2], bar_od, bar_oready, bar_fin;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
-    __shared__ float red_max[2][2][128];  // [tile parity][column half][row]
-    __shared__ float red_sum[2][128];     // [column half][row]
+    __shared__ float red_max[2][C::kSplit][128];  // [tile parity][column slice][row]
+    __shared__ float red_sum[C::kSplit][128];     // [column slice][row]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -97,6 +100,7 @@ __global__ void __launch_bounds__(352, 1) fa_fwd_kernel(const __grid_constant__ 
             mbar_init(&bar_pf[b], C::kSoftmaxThreads);
         }
         mbar_init(&bar_od, 1);
+        mbar_init(&bar_oready, 1);
         mbar_init(&bar_fin, 1);
         mbar_fence_init();
     }
@@ -191,6 +195,10 @@ __global__ void __launch_bounds__(352, 1) fa_fwd_kernel(const __grid_constant__ 
                 if (j > 0 && !issue_pv(j - 1)) ok = false;
             }
             if (ok && n_kv > 0 && !issue_pv(n_kv - 1)) ok = false;
+            // O is final once every PV has completed.  The epilogue cannot use bar_od for
+            // this: S_{n-1} is issued before PV_{n-2}, so when the softmax finishes the last
+            // tile bar_od may still be two phases short, and its parity cannot tell n-2 from n.
+            if (ok) mma_commit(&bar_oready);
             if (!ok) record_timeout(p.status, abort_v);
             // Every issued MMA must finish before TMEM is released.
             mma_commit(&bar_fin);
@@ -198,13 +206,15 @@ __global__ void __launch_bounds__(352, 1) fa_fwd_kernel(const __grid_constant__ 
         }
     } else {
         // ------------------------------ softmax warps ------------------------------
-        const int quad = warp & 3;       // TMEM lane quadrant
-        const int half = warp >> 2;      // which 64 key columns of the tile
-        const uint32_t pair_bar = 1 + quad;  // named barrier shared with the other half
-        const int row = quad * 32 + lane;    // row inside the tile == TMEM lane
+        constexpr int kC = C::kCols;
+        const int quad = warp & 3;                       // TMEM lane quadrant
+        const int part = warp >> 2;                      // which kC key columns of the tile
+        const uint32_t grp_bar = 1 + quad;               // named barrier of the quadrant
+        constexpr uint32_t kGrpThreads = 32 * C::kSplit;
+        const int row = quad * 32 + lane;                // row inside the tile == TMEM lane
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const int q_row = qt * kTileRows + row;
-        const int c0 = half * C::kCols;
+        const int c0 = part * kC;
         float m_ref = -INFINITY;
         float l_sum = 0.0f;  // over this warp's columns only
         bool ok = true;
@@ -213,50 +223,53 @@ __global__ void __launch_bounds__(352, 1) fa_fwd_kernel(const __grid_constant__ 
             ok = wait_bounded(&bar_sf[b], (uint32_t)(j >> 1) & 1u, abort_v, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
             const uint32_t s_addr = tmem + lane_off + C::kTmS + 128 * b;
-            float s[64];
+            float s[kC];
             float mx = -INFINITY;
             if (ok) {
                 tc_fence_after_sync();
-                uint32_t ra[32], rb[32];
-                tmem_ld32x2(s_addr + c0, s_addr + c0 + 32, ra, rb);
+                uint32_t r[kC];
+                tmem_ld_cols<kC>(s_addr + c0, r);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    s[i] = __uint_as_float(ra[i]);
-                    s[32 + i] = __uint_as_float(rb[i]);
-                }
+                for (int i = 0; i < kC; ++i) s[i] = __uint_as_float(r[i]);
                 const int key0 = j * kTileRows + c0;
                 if ((CAUSAL && j == n_kv - 1) || j * kTileRows + kTileRows > p.L) {
                     const int lim = CAUSAL ? min(p.L - 1, q_row) : (p.L - 1);
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
+                    for (int c = 0; c < kC; ++c)
                         if (key0 + c > lim) s[c] = -INFINITY;
                 }
+                float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-                for (int c = 0; c < 64; ++c) mx = fmaxf(mx, s[c]);
-                red_max[b][half][row] = mx;
+                for (int c = 4; c < kC; c += 4) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) m4[u] = fmaxf(m4[u], s[c + u]);
+                }
+                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             }
-            // Both halves have read their S columns (P may now overwrite them) and published
+            red_max[b][part][row] = mx;
+            // All slices have read their S columns (P may now overwrite them) and published
             // their partial maxima.
-            ok = bar_and(pair_bar, 64, ok);
+            ok = bar_and(grp_bar, kGrpThreads, ok);
             if (!ok) break;
-            mx = fmaxf(mx, red_max[b][half ^ 1][row]);
+#pragma unroll
+            for (int q = 0; q < C::kSplit; ++q) mx = fmaxf(mx, red_max[b][q][row]);
             const float m_cand = mx * p.scale_log2;
             float m_new = m_ref;
             if (m_cand > m_ref + kRescaleThreshold) m_new = m_cand;
             const bool rescale = (j > 0) && (m_new != m_ref);
             const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
             const float alpha = rescale ? ex2_approx(m_ref - m_new) : 1.0f;
-            float sum = 0.0f;
-            uint32_t pk[32];
+            float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            uint32_t pk[kC / 2];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < kC / 2; ++i) {
                 const float p0 = ex2_approx(fmaf(s[2 * i], p.scale_log2, -m_use));
                 const float p1 = ex2_approx(fmaf(s[2 * i + 1], p.scale_log2, -m_use));
-                sum += p0 + p1;
+                sum4[i & 3] += p0 + p1;
                 pk[i] = pack2<BF16>(p0, p1);
             }
-            tmem_st32(tmem + lane_off + C::kTmS + 128 * b + half * 32, pk);
-            l_sum = l_sum * alpha + sum;
+            tmem_st<kC / 2>(tmem + lane_off + C::kTmS + 128 * b + part * (kC / 2), pk);
+            l_sum = l_sum * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
             bool okr = true;
             if (__any_sync(0xffffffffu, rescale)) {
                 // O holds the sum up to tile j-1: wait for that PV, then rescale in place.
@@ -264,19 +277,10 @@ __global__ void __launch_bounds__(352, 1) fa_fwd_kernel(const __grid_constant__ 
                 okr = __all_sync(0xffffffffu, okr);
                 if (okr) {
                     tc_fence_after_sync();
-                    const uint32_t o_addr = tmem + lane_off + C::kTmO + half * C::kOCols;
-#pragma unroll
-                    for (int c = 0; c < C::kOCols / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(o_addr + c * 32, r);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(o_addr + c * 32, r);
-                    }
+                    tmem_row_scale<C::kOCols>(tmem + lane_off + C::kTmO + part * C::kOCols, alpha);
                 }
             }
-            okr = bar_and(pair_bar, 64, okr);
+            okr = bar_and(grp_bar, kGrpThreads, okr);
             if (!okr) {
                 ok = false;
                 break;
@@ -287,43 +291,24 @@ __global__ void __launch_bounds__(352, 1) fa_fwd_kernel(const __grid_constant__ 
             m_ref = m_new;
         }
         if (ok && n_kv > 0) {
-            ok = wait_bounded(&bar_od, (uint32_t)(n_kv - 1) & 1u, abort_v, p.timeout_ns);
+            ok = wait_bounded(&bar_oready, 0, abort_v, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
         }
-        red_sum[half][row] = l_sum;
-        ok = bar_and(pair_bar, 64, ok);
+        red_sum[part][row] = l_sum;
+        ok = bar_and(grp_bar, kGrpThreads, ok);
         if (!ok) {
             if (lane == 0) record_timeout(p.status, abort_v);
         } else {
             tc_fence_after_sync();
-            const float l_tot = l_sum + red_sum[half ^ 1][row];
+            float l_tot = 0.0f;
+#pragma unroll
+            for (int q = 0; q < C::kSplit; ++q) l_tot += red_sum[q][row];
             const bool valid = q_row < p.L;
-            const float inv_l = 1.0f / l_tot;
-            if (valid && half == 0) p.lse[(size_t)bh * p.L + q_row] = (m_ref + log2f(l_tot)) * kLn2;
+            if (valid && part == 0) p.lse[(size_t)bh * p.L + q_row] = (m_ref + log2f(l_tot)) * kLn2;
             uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) + ((size_t)bh * p.L + q_row) * D * 2 +
-                            half * C::kOCols * 2;
-            const uint32_t o_addr = tmem + lane_off + C::kTmO + half * C::kOCols;
-#pragma unroll
-            for (int c = 0; c < C::kOCols / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(o_addr + c * 32, r);
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
-#pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        uint4 w;
-                        w.x = pack2<BF16>(__uint_as_float(r[v4 * 8 + 0]) * inv_l,
-                                          __uint_as_float(r[v4 * 8 + 1]) * inv_l);
-                        w.y = pack2<BF16>(__uint_as_float(r[v4 * 8 + 2]) * inv_l,
-                                          __uint_as_float(r[v4 * 8 + 3]) * inv_l);
-                        w.z = pack2<BF16>(__uint_as_float(r[v4 * 8 + 4]) * inv_l,
-                                          __uint_as_float(r[v4 * 8 + 5]) * inv_l);
-                        w.w = pack2<BF16>(__uint_as_float(r[v4 * 8 + 6]) * inv_l,
-                                          __uint_as_float(r[v4 * 8 + 7]) * inv_l);
-                        dst[v4] = w;
-                    }
-                }
-            }
+                            part * C::kOCols * 2;
+            tmem_row_to_global<BF16, C::kOCols>(tmem + lane_off + C::kTmO + part * C::kOCols, orow,
+                                                1.0f / l_tot, valid);
         }
     }
 

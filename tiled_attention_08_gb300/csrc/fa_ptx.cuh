@@ -216,6 +216,31 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
+// Warp-wide: thread t reads 16 consecutive 32-bit columns of lane (lane_base + t), and waits.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Column-count generic forms (N = 16 or 32) used by kernels whose per-warp slice width is a
+// compile-time constant.
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]) {
+    static_assert(N == 16 || N == 32, "16 or 32 columns");
+    if constexpr (N == 16) tmem_ld16(taddr, r);
+    else tmem_ld32(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&r)[N]) {
+    static_assert(N == 16 || N == 32, "16 or 32 columns");
+    if constexpr (N == 16) tmem_st16(taddr, r);
+    else tmem_st32(taddr, r);
+}
+
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -278,6 +303,18 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
         : "memory");
 }
 
+// Warp-wide load of N = 32 or 64 consecutive columns (one wait for all of them).
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
+    static_assert(N == 32 || N == 64, "32 or 64 columns");
+    if constexpr (N == 32) {
+        tmem_ld32(taddr, r);
+    } else {
+        tmem_ld32x2(taddr, taddr + 32, reinterpret_cast<uint32_t(&)[32]>(r[0]),
+                    reinterpret_cast<uint32_t(&)[32]>(r[32]));
+    }
+}
+
 // ---------------------------------------------------------------------------------------
 // Math helpers
 // ---------------------------------------------------------------------------------------
@@ -306,6 +343,76 @@ __device__ __forceinline__ float2 unpack2(uint32_t u) {
     } else {
         __half2 h = *reinterpret_cast<__half2*>(&u);
         return __half22float2(h);
+    }
+}
+
+}  // namespace fa
+
+namespace fa {
+
+// Scales N fp32 values (as raw bits) by `mul`, rounds them to the 16-bit type and writes
+// them as N*2 contiguous bytes at `dst` (16-byte aligned) with 16-byte stores.
+template <bool BF16, int N>
+__device__ __forceinline__ void store_row16(uint8_t* dst, const uint32_t (&r)[N], float mul) {
+    static_assert(N % 8 == 0, "whole 16-byte stores");
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int v = 0; v < N / 8; ++v) {
+        uint4 w;
+        w.x = pack2<BF16>(__uint_as_float(r[v * 8 + 0]) * mul, __uint_as_float(r[v * 8 + 1]) * mul);
+        w.y = pack2<BF16>(__uint_as_float(r[v * 8 + 2]) * mul, __uint_as_float(r[v * 8 + 3]) * mul);
+        w.z = pack2<BF16>(__uint_as_float(r[v * 8 + 4]) * mul, __uint_as_float(r[v * 8 + 5]) * mul);
+        w.w = pack2<BF16>(__uint_as_float(r[v * 8 + 6]) * mul, __uint_as_float(r[v * 8 + 7]) * mul);
+        d[v] = w;
+    }
+}
+
+// Reads NCOLS (a multiple of 16) fp32 columns of this thread's TMEM lane, scales them and
+// stores them as 16-bit values at `dst`; skips the stores (not the warp-wide loads) when
+// `valid` is false.
+template <bool BF16, int NCOLS>
+__device__ __forceinline__ void tmem_row_to_global(uint32_t taddr, uint8_t* dst, float mul,
+                                                   bool valid) {
+    static_assert(NCOLS % 16 == 0, "16-column granularity");
+    if constexpr (NCOLS % 32 == 0) {
+#pragma unroll
+        for (int c = 0; c < NCOLS / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c * 32, r);
+            if (valid) store_row16<BF16, 32>(dst + c * 64, r, mul);
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < NCOLS / 16; ++c) {
+            uint32_t r[16];
+            tmem_ld16(taddr + c * 16, r);
+            if (valid) store_row16<BF16, 16>(dst + c * 32, r, mul);
+        }
+    }
+}
+
+// Multiplies NCOLS fp32 TMEM columns of this thread's lane by `mul` in place.
+template <int NCOLS>
+__device__ __forceinline__ void tmem_row_scale(uint32_t taddr, float mul) {
+    static_assert(NCOLS % 16 == 0, "16-column granularity");
+    if constexpr (NCOLS % 32 == 0) {
+#pragma unroll
+        for (int c = 0; c < NCOLS / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c * 32, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * mul);
+            tmem_st32(taddr + c * 32, r);
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < NCOLS / 16; ++c) {
+            uint32_t r[16];
+            tmem_ld16(taddr + c * 16, r);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * mul);
+            tmem_st16(taddr + c * 16, r);
+        }
     }
 }
 
