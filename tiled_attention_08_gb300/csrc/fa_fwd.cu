@@ -8,18 +8,27 @@
 // PV run in this one kernel ("FlashAttention principles and engineering practice",
 // section 1, kernel fusion), so S and P never reach global memory.
 //
-// CTA roles (one CTA per (b*h, query tile)), with kSplit softmax warps per TMEM lane quadrant:
-//   warps 0 .. 4*kSplit-1  softmax: warp w owns TMEM lanes 32*(w%4).. (query rows) and the
-//              key columns [kCols*(w/4), +kCols) of each S tile (kCols = 128/kSplit); the
-//              kSplit warps sharing a lane quadrant combine their partial row maxima through
-//              shared memory at a named barrier;
-//   next warp  TMA producer of Q (once) and the K_j ring;
-//   next warp  MMA issuer (one thread) and TMEM owner;
-//   last warp  TMA producer of the V_j ring (V_j is consumed a softmax later than K_j, so the
-//              two rings advance independently and K runs further ahead).
-// TMEM columns: S double buffer at [0,128) and [128,256) (fp32); the 16-bit P of a tile
-// overwrites the first 64 columns of its S buffer and feeds the PV MMA straight from TMEM;
-// O (fp32, D columns) at [256, 256+D).
+// GB300 layout.  One CTA owns TWO consecutive 128-row query tiles (A = 2p, B = 2p+1) of one
+// head, so every K/V tile brought into shared memory feeds two tiles' worth of MMAs: the L2 ->
+// SM traffic per FLOP is half of a one-tile CTA's, and each ring slot has twice as long to
+// arrive.  The two tiles also give the tensor core independent work to interleave: while the
+// softmax of tile A runs, the MMA warp computes tile B's PV and S, and the other way round.
+//
+// CTA roles (kSplit = 1: 352 threads):
+//   softmax warps, one group of 4*kSplit per query tile (tile A first).  In a group, warp w
+//                owns TMEM lanes 32*(w%4).. (query rows) and key columns
+//                [kCols*(w/4), +kCols) of the tile's S (kCols = 128/kSplit); with kSplit > 1
+//                the warps of a lane quadrant combine partial row maxima through shared memory
+//                at a named barrier, with kSplit = 1 every thread owns a whole row;
+//   next warp    TMA producer of Q_A, Q_B (once) and the K_j ring;
+//   next warp    MMA issuer (one thread) and TMEM owner;
+//   last warp    TMA producer of the V_j ring.
+// TMEM columns: S_A [0,128), S_B [128,256) (fp32; the 16-bit P of a tile overwrites the first
+// 64 columns of its S and feeds the PV MMA straight from TMEM), O_A [256, 256+D),
+// O_B [256+D, 256+2D).  MMA order: S_A0, S_B0, then for each key tile j: PV_Aj, S_A(j+1),
+// PV_Bj, S_B(j+1).  S_t(j+1) is issued after PV_tj, so (tcgen05 MMAs of one thread run in
+// issue order) it never overwrites a P still being read, and once the softmax sees S_t(j+1)
+// every PV before it has finished: O_t may be rescaled in place with no further wait.
 //
 // Online softmax in the log2 domain: y = s * scale * log2(e).  The running reference max m
 // is only raised when a tile's max exceeds it by more than kRescaleThreshold (2^8 headroom
@@ -38,24 +47,26 @@ template <int D, bool BF16, bool CAUSAL>
 struct FwdCfg {
     static constexpr int kChunks = D / kChunkElems;            // swizzle boxes per tile row
     static constexpr int kTileBytes = kTileRows * D * 2;       // one 128 x D tile
-    static constexpr int kKStages = (D == 128) ? 3 : 4;        // K ring depth
+    static constexpr int kKStages = (D == 128) ? 2 : 4;        // K ring depth
     static constexpr int kVStages = (D == 128) ? 2 : 4;        // V ring depth
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kTileBytes;
+    static constexpr int kOffQ = 0;                            // Q_A, then Q_B
+    static constexpr int kOffK = kOffQ + 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kKStages * kTileBytes;
     static constexpr int kSmemBytes = kOffV + kVStages * kTileBytes + 1024;  // + alignment slack
-    static constexpr int kSplit = 4;                          // softmax warps per lane quadrant
-    static constexpr int kSoftmaxWarps = 4 * kSplit;
-    static constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+    static constexpr int kSplit = 1;                           // softmax warps per lane quadrant
+    static constexpr int kGroupWarps = 4 * kSplit;             // softmax warps per query tile
+    static constexpr int kGroupThreads = kGroupWarps * 32;
+    static constexpr int kSoftmaxWarps = 2 * kGroupWarps;
     static constexpr int kProducerWarp = kSoftmaxWarps;
     static constexpr int kMmaWarp = kSoftmaxWarps + 1;
     static constexpr int kVProducerWarp = kSoftmaxWarps + 2;
     static constexpr int kThreads = (kSoftmaxWarps + 3) * 32;
-    static constexpr int kCols = 128 / kSplit;                // S columns per softmax warp
-    static constexpr int kOCols = D / kSplit;                 // O columns per softmax warp
+    static constexpr int kCols = 128 / kSplit;                 // S columns per softmax warp
+    static constexpr int kOCols = D / kSplit;                  // O columns per softmax warp
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kTmS = 0;    // S buffer b at kTmS + 128*b
-    static constexpr uint32_t kTmO = 256;  // O accumulator
+    static constexpr uint32_t kTmS = 0;        // S of tile t at kTmS + 128*t
+    static constexpr uint32_t kTmO = 256;      // O of tile t at kTmO + D*t
+    static_assert(kTmO + 2 * D <= kTmemCols, "TMEM budget");
     static constexpr uint32_t kIdescS = idesc_f16(BF16, 128, 128, false, false);
     static constexpr uint32_t kIdescO = idesc_f16(BF16, 128, D, false, true);
 };
@@ -68,20 +79,25 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     __shared__ uint64_t bar_q, bar_kf[C::kKStages], bar_ke[C::kKStages], bar_vf[C::kVStages],
-        bar_ve[C::kVStages], bar_sf[2], bar_pf[2], bar_od, bar_oready, bar_fin;
+        bar_ve[C::kVStages], bar_sf[2], bar_pf[2], bar_oready[2], bar_fin;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
-    __shared__ float red_max[2][C::kSplit][128];  // [tile parity][column slice][row]
-    __shared__ float red_sum[C::kSplit][128];     // [column slice][row]
+    __shared__ float red_max[2][2][C::kSplit][128];  // [tile][parity][column slice][row]
+    __shared__ float red_sum[2][C::kSplit][128];     // [tile][column slice][row]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Heads in L2-sized groups; inside a group the heaviest query tiles (most key tiles under
+    // Heads in L2-sized groups; inside a group the heaviest tile pairs (most key tiles under
     // the causal mask) go first.
+    const int n_pairs = (p.n_tiles + 1) >> 1;
     int bh, rank;
-    tile_coords(blockIdx.x, p.BH, p.n_tiles, p.group, bh, rank);
-    const int qt = p.n_tiles - 1 - rank;
-    const int n_kv = CAUSAL ? (qt + 1) : p.n_tiles;
+    tile_coords(blockIdx.x, p.BH, n_pairs, p.group, bh, rank);
+    const int pair = n_pairs - 1 - rank;
+    const int q_a = 2 * pair, q_b = 2 * pair + 1;  // the two query tiles
+    const bool has_b = q_b < p.n_tiles;
+    const int n_kv_a = CAUSAL ? q_a + 1 : p.n_tiles;  // key tiles each query tile sees
+    const int n_kv_b = has_b ? (CAUSAL ? q_b + 1 : p.n_tiles) : 0;
+    const int n_kv = has_b ? n_kv_b : n_kv_a;  // n_kv_a <= n_kv_b
     volatile int* abort_v = &abort_flag;
 
     if (threadIdx.x == 0) {
@@ -95,12 +111,11 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
             mbar_init(&bar_vf[s], 1);
             mbar_init(&bar_ve[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&bar_sf[b], 1);
-            mbar_init(&bar_pf[b], C::kSoftmaxThreads);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&bar_sf[t], 1);
+            mbar_init(&bar_pf[t], C::kGroupThreads);
+            mbar_init(&bar_oready[t], 1);
         }
-        mbar_init(&bar_od, 1);
-        mbar_init(&bar_oready, 1);
         mbar_init(&bar_fin, 1);
         mbar_fence_init();
     }
@@ -123,10 +138,11 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
             tma_prefetch_desc(map);
             if (is_k) {
                 tma_prefetch_desc(&p.tm_q);
-                mbar_arrive_expect_tx(&bar_q, C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(smem + C::kOffQ + c * kChunkBytes, &p.tm_q, &bar_q,
-                                c * kChunkElems, qt * kTileRows, bh);
+                mbar_arrive_expect_tx(&bar_q, (has_b ? 2 : 1) * C::kTileBytes);
+                for (int t = 0; t < (has_b ? 2 : 1); ++t)
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + c * kChunkBytes, &p.tm_q,
+                                    &bar_q, c * kChunkElems, (t ? q_b : q_a) * kTileRows, bh);
             }
             bool ok = true;
             int issued = 0;  // fills handed to the TMA unit
@@ -153,52 +169,78 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
     } else if (warp == C::kMmaWarp) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
-            const uint32_t q_base = smem_u32(smem + C::kOffQ);
             bool ok = wait_bounded(&bar_q, 0, abort_v, p.timeout_ns);
-            auto issue_pv = [&](int jj) -> bool {
-                const int b = jj & 1;
-                const int st = jj % C::kVStages;
-                const uint32_t ph = (uint32_t)(jj / C::kVStages) & 1u;
-                if (!wait_bounded(&bar_pf[b], (uint32_t)(jj >> 1) & 1u, abort_v, p.timeout_ns))
+            int k_ready = -1;  // newest K tile known to have landed
+            auto wait_k = [&](int j) -> bool {
+                if (k_ready >= j) return true;
+                const int st = j % C::kKStages;
+                if (!wait_bounded(&bar_kf[st], (uint32_t)(j / C::kKStages) & 1u, abort_v,
+                                  p.timeout_ns))
                     return false;
-                if (!wait_bounded(&bar_vf[st], ph, abort_v, p.timeout_ns)) return false;
+                tc_fence_after_sync();
+                k_ready = j;
+                return true;
+            };
+            auto issue_s = [&](int t, int j) {
+                const uint32_t q_base = smem_u32(smem + C::kOffQ + t * C::kTileBytes);
+                const uint32_t k_base =
+                    smem_u32(smem + C::kOffK + (j % C::kKStages) * C::kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                    mma_ss(tmem + C::kTmS + 128 * t, sdesc_kmajor_sw128(q_base + off),
+                           sdesc_kmajor_sw128(k_base + off), C::kIdescS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar_sf[t]);
+            };
+            auto issue_pv = [&](int t, int j) -> bool {
+                const int st = j % C::kVStages;
+                if (!wait_bounded(&bar_pf[t], (uint32_t)j & 1u, abort_v, p.timeout_ns))
+                    return false;
+                if (!wait_bounded(&bar_vf[st], (uint32_t)(j / C::kVStages) & 1u, abort_v,
+                                  p.timeout_ns))
+                    return false;
                 tc_fence_after_sync();
                 const uint32_t v_base = smem_u32(smem + C::kOffV + st * C::kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < kTileRows / 16; ++kk) {
                     const uint64_t bd = sdesc_mnmajor_sw128(v_base + kk * 2048, kChunkBytes);
-                    mma_ts(tmem + C::kTmO, tmem + C::kTmS + 128 * b + kk * 8, bd, C::kIdescO,
-                           (jj > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem + C::kTmO + D * t, tmem + C::kTmS + 128 * t + kk * 8, bd,
+                           C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(&bar_ve[st]);
-                mma_commit(&bar_od);
+                if (j + 1 == (t ? n_kv_b : n_kv_a)) mma_commit(&bar_oready[t]);  // O_t is final
                 return true;
             };
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int st = j % C::kKStages;
-                const uint32_t ph = (uint32_t)(j / C::kKStages) & 1u;
-                const int b = j & 1;
-                if (!wait_bounded(&bar_kf[st], ph, abort_v, p.timeout_ns)) {
-                    ok = false;
-                    break;
+            if (ok && n_kv > 0) {
+                ok = wait_k(0);
+                if (ok) {
+                    issue_s(0, 0);
+                    if (n_kv_b > 0) issue_s(1, 0);
+                    mma_commit(&bar_ke[0]);
                 }
-                tc_fence_after_sync();
-                const uint32_t k_base = smem_u32(smem + C::kOffK + st * C::kTileBytes);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    mma_ss(tmem + C::kTmS + 128 * b, sdesc_kmajor_sw128(q_base + off),
-                           sdesc_kmajor_sw128(k_base + off), C::kIdescS, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&bar_ke[st]);
-                mma_commit(&bar_sf[b]);
-                if (j > 0 && !issue_pv(j - 1)) ok = false;
             }
-            if (ok && n_kv > 0 && !issue_pv(n_kv - 1)) ok = false;
-            // O is final once every PV has completed.  The epilogue cannot use bar_od for
-            // this: S_{n-1} is issued before PV_{n-2}, so when the softmax finishes the last
-            // tile bar_od may still be two phases short, and its parity cannot tell n-2 from n.
-            if (ok) mma_commit(&bar_oready);
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const bool next = j + 1 < n_kv;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int n_t = t ? n_kv_b : n_kv_a;
+                    if (!ok) break;
+                    if (j < n_t && !issue_pv(t, j)) {
+                        ok = false;
+                        break;
+                    }
+                    if (next && j + 1 < n_t) {
+                        if (!wait_k(j + 1)) {
+                            ok = false;
+                            break;
+                        }
+                        issue_s(t, j + 1);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&bar_ve[j % C::kVStages]);                // V_j read by both PVs
+                if (next) mma_commit(&bar_ke[(j + 1) % C::kKStages]);  // K_{j+1} read by both S
+            }
             if (!ok) record_timeout(p.status, abort_v);
             // Every issued MMA must finish before TMEM is released.
             mma_commit(&bar_fin);
@@ -207,22 +249,26 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
     } else {
         // ------------------------------ softmax warps ------------------------------
         constexpr int kC = C::kCols;
-        const int quad = warp & 3;                       // TMEM lane quadrant
-        const int part = warp >> 2;                      // which kC key columns of the tile
-        const uint32_t grp_bar = 1 + quad;               // named barrier of the quadrant
+        const int t = warp / C::kGroupWarps;             // query tile of this group
+        const int gw = warp % C::kGroupWarps;
+        const int quad = gw & 3;                         // TMEM lane quadrant
+        const int part = gw >> 2;                        // which kC key columns of the tile
+        const uint32_t grp_bar = 1 + t * 4 + quad;       // named barrier of the quadrant
         constexpr uint32_t kGrpThreads = 32 * C::kSplit;
         const int row = quad * 32 + lane;                // row inside the tile == TMEM lane
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        const int q_row = qt * kTileRows + row;
+        const int q_row = (t ? q_b : q_a) * kTileRows + row;
+        const int n_mine = t ? n_kv_b : n_kv_a;
         const int c0 = part * kC;
+        const uint32_t s_addr = tmem + lane_off + C::kTmS + 128 * t;
+        const uint32_t o_addr = tmem + lane_off + C::kTmO + D * t + part * C::kOCols;
         float m_ref = -INFINITY;
         float l_sum = 0.0f;  // over this warp's columns only
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            const int b = j & 1;
-            ok = wait_bounded(&bar_sf[b], (uint32_t)(j >> 1) & 1u, abort_v, p.timeout_ns);
+        for (int j = 0; j < n_mine; ++j) {
+            const int par = j & 1;  // parity slot of the shared-memory max exchange
+            ok = wait_bounded(&bar_sf[t], (uint32_t)j & 1u, abort_v, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
-            const uint32_t s_addr = tmem + lane_off + C::kTmS + 128 * b;
             float s[kC];
             float mx = -INFINITY;
             if (ok) {
@@ -232,7 +278,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < kC; ++i) s[i] = __uint_as_float(r[i]);
                 const int key0 = j * kTileRows + c0;
-                if ((CAUSAL && j == n_kv - 1) || j * kTileRows + kTileRows > p.L) {
+                if ((CAUSAL && j == n_mine - 1) || j * kTileRows + kTileRows > p.L) {
                     const int lim = CAUSAL ? min(p.L - 1, q_row) : (p.L - 1);
 #pragma unroll
                     for (int c = 0; c < kC; ++c)
@@ -246,13 +292,17 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                 }
                 mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             }
-            red_max[b][part][row] = mx;
-            // All slices have read their S columns (P may now overwrite them) and published
-            // their partial maxima.
-            ok = bar_and(grp_bar, kGrpThreads, ok);
-            if (!ok) break;
+            if constexpr (C::kSplit > 1) {
+                red_max[t][par][part][row] = mx;
+                // All slices have read their S columns (P may now overwrite them) and
+                // published their partial maxima.
+                ok = bar_and(grp_bar, kGrpThreads, ok);
+                if (!ok) break;
 #pragma unroll
-            for (int q = 0; q < C::kSplit; ++q) mx = fmaxf(mx, red_max[b][q][row]);
+                for (int q = 0; q < C::kSplit; ++q) mx = fmaxf(mx, red_max[t][par][q][row]);
+            } else {
+                if (!ok) break;  // warp-uniform: the warp owns its rows alone
+            }
             const float m_cand = mx * p.scale_log2;
             float m_new = m_ref;
             if (m_cand > m_ref + kRescaleThreshold) m_new = m_cand;
@@ -260,55 +310,50 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
             const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
             const float alpha = rescale ? ex2_approx(m_ref - m_new) : 1.0f;
             float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            uint32_t pk[kC / 2];
 #pragma unroll
-            for (int i = 0; i < kC / 2; ++i) {
-                const float p0 = ex2_approx(fmaf(s[2 * i], p.scale_log2, -m_use));
-                const float p1 = ex2_approx(fmaf(s[2 * i + 1], p.scale_log2, -m_use));
-                sum4[i & 3] += p0 + p1;
-                pk[i] = pack2<BF16>(p0, p1);
-            }
-            tmem_st<kC / 2>(tmem + lane_off + C::kTmS + 128 * b + part * (kC / 2), pk);
-            l_sum = l_sum * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
-            bool okr = true;
-            if (__any_sync(0xffffffffu, rescale)) {
-                // O holds the sum up to tile j-1: wait for that PV, then rescale in place.
-                okr = wait_bounded(&bar_od, (uint32_t)(j - 1) & 1u, abort_v, p.timeout_ns);
-                okr = __all_sync(0xffffffffu, okr);
-                if (okr) {
-                    tc_fence_after_sync();
-                    tmem_row_scale<C::kOCols>(tmem + lane_off + C::kTmO + part * C::kOCols, alpha);
+            for (int h = 0; h < kC / 32; ++h) {  // 32 columns -> 16 packed TMEM columns at a time
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ex2_approx(fmaf(s[h * 32 + 2 * i], p.scale_log2, -m_use));
+                    const float p1 = ex2_approx(fmaf(s[h * 32 + 2 * i + 1], p.scale_log2, -m_use));
+                    sum4[i & 3] += p0 + p1;
+                    pk[i] = pack2<BF16>(p0, p1);
                 }
+                tmem_st16(s_addr + part * (kC / 2) + h * 16, pk);
             }
-            okr = bar_and(grp_bar, kGrpThreads, okr);
-            if (!okr) {
-                ok = false;
-                break;
-            }
+            l_sum = l_sum * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+            // S_t(j) was issued after PV_t(j-1), so every PV into O_t has completed: rescale
+            // in place without waiting.
+            if (__any_sync(0xffffffffu, rescale)) tmem_row_scale<C::kOCols>(o_addr, alpha);
             tmem_st_wait();
             tc_fence_before_sync();
-            mbar_arrive(&bar_pf[b]);
+            mbar_arrive(&bar_pf[t]);
             m_ref = m_new;
         }
-        if (ok && n_kv > 0) {
-            ok = wait_bounded(&bar_oready, 0, abort_v, p.timeout_ns);
+        if (ok && n_mine > 0) {
+            ok = wait_bounded(&bar_oready[t], 0, abort_v, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
         }
-        red_sum[part][row] = l_sum;
-        ok = bar_and(grp_bar, kGrpThreads, ok);
+        if constexpr (C::kSplit > 1) {
+            red_sum[t][part][row] = l_sum;
+            ok = bar_and(grp_bar, kGrpThreads, ok);
+        }
         if (!ok) {
             if (lane == 0) record_timeout(p.status, abort_v);
-        } else {
+        } else if (n_mine > 0) {
             tc_fence_after_sync();
-            float l_tot = 0.0f;
+            float l_tot = l_sum;
+            if constexpr (C::kSplit > 1) {
+                l_tot = 0.0f;
 #pragma unroll
-            for (int q = 0; q < C::kSplit; ++q) l_tot += red_sum[q][row];
+                for (int q = 0; q < C::kSplit; ++q) l_tot += red_sum[t][q][row];
+            }
             const bool valid = q_row < p.L;
             if (valid && part == 0) p.lse[(size_t)bh * p.L + q_row] = (m_ref + log2f(l_tot)) * kLn2;
             uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) + ((size_t)bh * p.L + q_row) * D * 2 +
                             part * C::kOCols * 2;
-            tmem_row_to_global<BF16, C::kOCols>(tmem + lane_off + C::kTmO + part * C::kOCols, orow,
-                                                1.0f / l_tot, valid);
+            tmem_row_to_global<BF16, C::kOCols>(o_addr, orow, 1.0f / l_tot, valid);
         }
     }
 
@@ -327,7 +372,7 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)p.n_tiles * (unsigned)p.BH;
+    const unsigned grid = (unsigned)((p.n_tiles + 1) / 2) * (unsigned)p.BH;
     kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }

@@ -303,15 +303,19 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
         : "memory");
 }
 
-// Warp-wide load of N = 32 or 64 consecutive columns (one wait for all of them).
+// Warp-wide load of N = 32, 64 or 128 consecutive columns (loads issued in pairs, one wait
+// per pair).
 template <int N>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
-    static_assert(N == 32 || N == 64, "32 or 64 columns");
+    static_assert(N == 32 || N == 64 || N == 128, "32, 64 or 128 columns");
     if constexpr (N == 32) {
         tmem_ld32(taddr, r);
     } else {
-        tmem_ld32x2(taddr, taddr + 32, reinterpret_cast<uint32_t(&)[32]>(r[0]),
-                    reinterpret_cast<uint32_t(&)[32]>(r[32]));
+#pragma unroll
+        for (int h = 0; h < N / 64; ++h)
+            tmem_ld32x2(taddr + 64 * h, taddr + 64 * h + 32,
+                        reinterpret_cast<uint32_t(&)[32]>(r[64 * h]),
+                        reinterpret_cast<uint32_t(&)[32]>(r[64 * h + 32]));
     }
 }
 
