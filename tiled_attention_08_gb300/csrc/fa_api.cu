@@ -280,6 +280,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
         return FA_ERR_CUDA;
     float* lse2_pad = static_cast<float*>(workspace);
     float* delta_pad = lse2_pad + (size_t)sh.BH * sh.Lpad;
+    p.q = q;
+    p.dout = dout;
     p.lse2_pad = lse2_pad;
     p.delta_pad = delta_pad;
     p.dq = dq;

@@ -13,11 +13,15 @@
 //
 // CTA roles: 4*kSplit elementwise warps (warp w: key rows 32*(w%4).. == TMEM lanes, query
 // columns [kCols*(w/4), +kCols)), then one TMA producer warp (K_j, V_j once; Q_i, dO_i,
-// LSE_i, Delta_i per stage) and one MMA-issuer warp that also owns TMEM.  Per query tile the MMA warp issues
-// S^T, then dP^T; the elementwise warps turn S^T into P^T (which releases the dV MMA) and
-// then dP^T into dS^T (which releases the dK MMA), so dP^T and dV run under the elementwise
-// work.  TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D); the 16-bit
-// P^T and dS^T overwrite the first 64 columns of S^T and dP^T.
+// LSE_i, Delta_i per stage) and one MMA-issuer warp that also owns TMEM.
+// TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D).
+//
+// Pipeline.  The elementwise warps read S^T into registers (P^T stays there) and at once
+// release the S^T columns, so the MMA warp issues S^T of the NEXT query tile right away.
+// Once dP^T has been read too, the 16-bit P^T and dS^T are written side by side into the
+// dP^T columns (P^T at [128,192), dS^T at [192,256)), which feed the dV and dK MMAs; the next
+// dP^T is issued after those.  So the P phase of query tile i+1 runs while the tensor core
+// does dV_i, dK_i and dP^T_{i+1}, instead of waiting for them.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -57,8 +61,8 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    __shared__ uint64_t bar_kv, bar_qf[C::kStages], bar_qe[C::kStages], bar_sf, bar_df, bar_pp,
-        bar_pd, bar_done, bar_fin;
+    __shared__ uint64_t bar_kv, bar_qf[C::kStages], bar_qe[C::kStages], bar_sf, bar_df, bar_sr,
+        bar_ppd, bar_done, bar_fin;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
@@ -81,8 +85,8 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
         }
         mbar_init(&bar_sf, 1);
         mbar_init(&bar_df, 1);
-        mbar_init(&bar_pp, C::kEwThreads);
-        mbar_init(&bar_pd, C::kEwThreads);
+        mbar_init(&bar_sr, C::kEwThreads);   // S^T read: its columns may be overwritten
+        mbar_init(&bar_ppd, C::kEwThreads);  // P^T and dS^T written into the dP^T columns
         mbar_init(&bar_done, 1);
         mbar_init(&bar_fin, 1);
         mbar_fence_init();
@@ -141,53 +145,76 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
         if (lane == 0) {
             const uint32_t k_base = smem_u32(smem + C::kOffK);
             const uint32_t v_base = smem_u32(smem + C::kOffV);
-            bool ok = wait_bounded(&bar_kv, 0, abort_v, p.timeout_ns);
-            for (int t = 0; t < n_it && ok; ++t) {
-                const int st = t % C::kStages;
-                const uint32_t ph = (uint32_t)(t / C::kStages) & 1u;
-                if (!wait_bounded(&bar_qf[st], ph, abort_v, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
+            auto q_base = [&](int t) {
+                return smem_u32(smem + C::kOffQ + (t % C::kStages) * C::kTileBytes);
+            };
+            auto do_base = [&](int t) {
+                return smem_u32(smem + C::kOffDO + (t % C::kStages) * C::kTileBytes);
+            };
+            auto wait_stage = [&](int t) {
+                const bool r = wait_bounded(&bar_qf[t % C::kStages],
+                                            (uint32_t)(t / C::kStages) & 1u, abort_v, p.timeout_ns);
                 tc_fence_after_sync();
-                const uint32_t q_base = smem_u32(smem + C::kOffQ + st * C::kTileBytes);
-                const uint32_t do_base = smem_u32(smem + C::kOffDO + st * C::kTileBytes);
+                return r;
+            };
+            const uint64_t kdesc = sdesc_kmajor_sw128(k_base);
+            const uint64_t vdesc = sdesc_kmajor_sw128(v_base);
+            auto issue_st = [&](int t) {  // S^T = K Q_t^T
+                const uint64_t qd = sdesc_kmajor_sw128(q_base(t));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    mma_ss(tmem + C::kTmST, sdesc_kmajor_sw128(k_base + off),
-                           sdesc_kmajor_sw128(q_base + off), C::kIdescS, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + C::kTmST, sdesc_advance(kdesc, off), sdesc_advance(qd, off),
+                           C::kIdescS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bar_sf);
+            };
+            auto issue_dpt = [&](int t) {  // dP^T = V dO_t^T
+                const uint64_t dd = sdesc_kmajor_sw128(do_base(t));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    mma_ss(tmem + C::kTmDPT, sdesc_kmajor_sw128(v_base + off),
-                           sdesc_kmajor_sw128(do_base + off), C::kIdescS, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + C::kTmDPT, sdesc_advance(vdesc, off), sdesc_advance(dd, off),
+                           C::kIdescS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bar_df);
+            };
+            bool ok = wait_bounded(&bar_kv, 0, abort_v, p.timeout_ns);
+            if (ok && n_it > 0) {
+                ok = wait_stage(0);
+                if (ok) {
+                    issue_st(0);
+                    issue_dpt(0);
+                }
+            }
+            for (int t = 0; t < n_it && ok; ++t) {
+                const uint32_t par = (uint32_t)t & 1u;
+                if (t + 1 < n_it) {
+                    // S^T of the next query tile as soon as this one's S^T has been read.
+                    if (!wait_bounded(&bar_sr, par, abort_v, p.timeout_ns) || !wait_stage(t + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    issue_st(t + 1);
+                }
+                if (!wait_bounded(&bar_ppd, par, abort_v, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
                 const uint32_t acc0 = t > 0 ? 1u : 0u;
-                if (!wait_bounded(&bar_pp, (uint32_t)t & 1u, abort_v, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
+                const uint64_t dod = sdesc_mnmajor_sw128(do_base(t), kChunkBytes);
+                const uint64_t qmd = sdesc_mnmajor_sw128(q_base(t), kChunkBytes);
 #pragma unroll
                 for (int kk = 0; kk < kTileRows / 16; ++kk)
-                    mma_ts(tmem + C::kTmDV, tmem + C::kTmST + kk * 8,
-                           sdesc_mnmajor_sw128(do_base + kk * 2048, kChunkBytes), C::kIdescG,
-                           (acc0 || kk > 0) ? 1u : 0u);
-                if (!wait_bounded(&bar_pd, (uint32_t)t & 1u, abort_v, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
+                    mma_ts(tmem + C::kTmDV, tmem + C::kTmDPT + kk * 8,
+                           sdesc_advance(dod, kk * 2048), C::kIdescG, (acc0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < kTileRows / 16; ++kk)
-                    mma_ts(tmem + C::kTmDK, tmem + C::kTmDPT + kk * 8,
-                           sdesc_mnmajor_sw128(q_base + kk * 2048, kChunkBytes), C::kIdescG,
-                           (acc0 || kk > 0) ? 1u : 0u);
-                mma_commit(&bar_qe[st]);
+                    mma_ts(tmem + C::kTmDK, tmem + C::kTmDPT + 64 + kk * 8,
+                           sdesc_advance(qmd, kk * 2048), C::kIdescG, (acc0 || kk > 0) ? 1u : 0u);
+                mma_commit(&bar_qe[t % C::kStages]);  // stage t fully read
+                if (t + 1 < n_it) issue_dpt(t + 1);     // after dV_t, dK_t read the dP^T columns
             }
             if (ok) mma_commit(&bar_done);
             if (!ok) record_timeout(p.status, abort_v);
@@ -216,15 +243,19 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
             const int q0 = it * kTileRows + c0;
             const bool masked = (CAUSAL && it == kt) || (it * kTileRows + kTileRows > p.L);
             const int qlim = p.L - 1;  // last valid query
-            // Phase 1: P^T = exp2(S^T * scale*log2e - LSE*log2e) on this warp's columns.
+            // Phase 1: P^T = exp2(S^T * scale*log2e - LSE*log2e) on this warp's columns; kept
+            // in registers, and the S^T columns are released at once.
             ok = wait_bounded(&bar_qf[st], ph, abort_v, p.timeout_ns) &&
                  wait_bounded(&bar_sf, (uint32_t)t & 1u, abort_v, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
             float pv[kC];
+            uint32_t pk_p[kC / 2];  // P^T, packed to 16 bits
             if (ok) {
                 tc_fence_after_sync();
                 uint32_t r[kC];
                 tmem_ld_cols<kC>(tmem + lane_off + C::kTmST + c0, r);
+                tc_fence_before_sync();
+                mbar_arrive(&bar_sr);
 #pragma unroll
                 for (int i = 0; i < kC; ++i)
                     pv[i] = ex2_approx(fmaf(__uint_as_float(r[i]), p.scale_log2, -lse2v[i]));
@@ -235,39 +266,38 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                         if (qg > qlim || (CAUSAL && key > qg)) pv[i] = 0.0f;
                     }
                 }
-            }
-            ok = bar_and(grp_bar, kGrpThreads, ok);  // all slices read S^T: P^T may overwrite it
-            if (!ok) break;
-            {
-                uint32_t pk[kC / 2];
 #pragma unroll
-                for (int i = 0; i < kC / 2; ++i) pk[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
-                tmem_st<kC / 2>(tmem + lane_off + C::kTmST + part * (kC / 2), pk);
+                for (int i = 0; i < kC / 2; ++i) pk_p[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
+                // Phase 2: dS^T = P^T o (dP^T - Delta).
+                ok = wait_bounded(&bar_df, (uint32_t)t & 1u, abort_v, p.timeout_ns);
+                ok = __all_sync(0xffffffffu, ok);
             }
-            tmem_st_wait();
-            tc_fence_before_sync();
-            mbar_arrive(&bar_pp);
-            // Phase 2: dS^T = P^T o (dP^T - Delta).
-            ok = wait_bounded(&bar_df, (uint32_t)t & 1u, abort_v, p.timeout_ns);
-            ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after_sync();
-                uint32_t r[kC];
-                tmem_ld_cols<kC>(tmem + lane_off + C::kTmDPT + c0, r);
+                constexpr int kLd = kC >= 64 ? 32 : 16;  // dP^T columns per load (registers)
 #pragma unroll
-                for (int i = 0; i < kC; ++i) pv[i] = pv[i] * (__uint_as_float(r[i]) - dltv[i]);
+                for (int h = 0; h < kC / kLd; ++h) {
+                    uint32_t r[kLd];
+                    tmem_ld<kLd>(tmem + lane_off + C::kTmDPT + c0 + h * kLd, r);
+#pragma unroll
+                    for (int i = 0; i < kLd; ++i)
+                        pv[h * kLd + i] *= __uint_as_float(r[i]) - dltv[h * kLd + i];
+                }
             }
-            ok = bar_and(grp_bar, kGrpThreads, ok);  // all slices have read dP^T
+            // Every slice of the quadrant has read its dP^T columns before any is overwritten.
+            // (All warps reach this barrier once per query tile on every path.)
+            ok = bar_and(grp_bar, kGrpThreads, ok);
             if (!ok) break;
             {
+                tmem_st<kC / 2>(tmem + lane_off + C::kTmDPT + part * (kC / 2), pk_p);
                 uint32_t pk[kC / 2];
 #pragma unroll
                 for (int i = 0; i < kC / 2; ++i) pk[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
-                tmem_st<kC / 2>(tmem + lane_off + C::kTmDPT + part * (kC / 2), pk);
+                tmem_st<kC / 2>(tmem + lane_off + C::kTmDPT + 64 + part * (kC / 2), pk);
             }
             tmem_st_wait();
             tc_fence_before_sync();
-            mbar_arrive(&bar_pd);
+            mbar_arrive(&bar_ppd);
         }
         if (ok) {
             ok = wait_bounded(&bar_done, 0, abort_v, p.timeout_ns);

@@ -4,16 +4,27 @@
 // tile j it can see (j <= i under the causal mask), P and dS are recomputed from the saved
 // log-sum-exp ("FlashAttention data-flow optimisation: MI50 memory and bandwidth
 // bottlenecks", section 2.2, third layer) and
-//   S  = Q_i K_j^T,  dP = dO_i V_j^T                 (tcgen05, K-major operands)
+//   S  = Q_i K_j^T,  dP = dO_i V_j^T
 //   P  = exp2(S * scale*log2e - LSE_i*log2e),  dS = P o (dP - Delta_i)   (per row: scalars)
-//   dQ_i += dS K_j                                   (A operand = 16-bit dS written to TMEM)
+//   dQ_i += dS K_j
 // dQ_i is scaled by the softmax scale and written once: no atomics, deterministic.
 //
+// GB300 layout.  A tcgen05 MMA that takes both operands from shared memory is limited by the
+// shared-memory operand path (about half the tensor rate at M = N = 128), while one whose A
+// operand sits in tensor memory runs at the full rate.  Q_i and dO_i are the A operands of S
+// and dP for every key tile, so they are staged once into TMEM (16-bit, two values per
+// column) and all three contractions here run with A in TMEM; shared memory holds only the
+// K_j / V_j ring.
+//
 // CTA roles: 4*kSplit elementwise warps (warp w: query rows 32*(w%4).. == TMEM lanes, key
-// columns [kCols*(w/4), +kCols)), then one TMA producer warp (Q_i, dO_i once; K_j, V_j per
-// stage) and one MMA-issuer warp that also owns TMEM.  The MMA warp issues S, then dP; the elementwise
-// warps start on P as soon as S lands, so the dP MMA runs under that work.
-// TMEM: S [0,128), dP [128,256), dQ [256,256+D); the 16-bit dS overwrites S's first 64 columns.
+// columns [kCols*(w/4), +kCols)), then one TMA producer warp (the K_j / V_j ring) and one
+// MMA-issuer warp that also owns TMEM.
+// TMEM: S [0,128), dP [128,256), dQ [256,256+D), Q [256+D, 256+3D/2), dO [256+3D/2, 256+2D).
+//
+// Pipeline.  The elementwise warps read S into registers and release its columns at once, so
+// the MMA warp issues S for the next key tile right away; once dP has been read, the 16-bit
+// dS is written over dP's first 64 columns and feeds the dQ MMA; the next dP is issued after
+// it.  The P phase of key tile j+1 therefore runs while the tensor core does dQ_j and dP_{j+1}.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -24,13 +35,11 @@ template <int D, bool BF16, bool CAUSAL>
 struct DqCfg {
     static constexpr int kChunks = D / kChunkElems;
     static constexpr int kTileBytes = kTileRows * D * 2;
-    static constexpr int kStages = (D == 128) ? 2 : 4;
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffDO = kTileBytes;
-    static constexpr int kOffK = 2 * kTileBytes;
+    static constexpr int kStages = (D == 128) ? 3 : 6;  // K/V ring depth
+    static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
     static constexpr int kSmemBytes = kOffV + kStages * kTileBytes + 1024;
-    static constexpr int kSplit = 4;  // elementwise warps per TMEM lane quadrant
+    static constexpr int kSplit = 2;  // elementwise warps per TMEM lane quadrant
     static constexpr int kEwWarps = 4 * kSplit;
     static constexpr int kEwThreads = kEwWarps * 32;
     static constexpr int kProducerWarp = kEwWarps;
@@ -38,8 +47,11 @@ struct DqCfg {
     static constexpr int kThreads = (kEwWarps + 2) * 32;
     static constexpr int kCols = 128 / kSplit;   // key columns per elementwise warp
     static constexpr int kOutCols = D / kSplit;  // dQ columns per elementwise warp
+    static constexpr int kStageCols = D / 2 / kSplit;  // packed Q / dO columns each warp stages
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmDQ = 256;
+    static constexpr uint32_t kTmQ = 256 + D, kTmDO = 256 + D + D / 2;
+    static_assert(kTmDO + D / 2 <= kTmemCols, "TMEM budget");
     static constexpr uint32_t kIdescS = idesc_f16(BF16, 128, 128, false, false);
     static constexpr uint32_t kIdescG = idesc_f16(BF16, 128, D, false, true);
 };
@@ -51,8 +63,8 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    __shared__ uint64_t bar_qd, bar_kvf[C::kStages], bar_kve[C::kStages], bar_sf, bar_df, bar_pd,
-        bar_done, bar_fin;
+    __shared__ uint64_t bar_qt, bar_kvf[C::kStages], bar_kve[C::kStages], bar_sf, bar_df, bar_sr,
+        bar_pd, bar_done, bar_fin;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
@@ -68,14 +80,15 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(&bar_qd, 1);
+        mbar_init(&bar_qt, C::kEwThreads);  // Q_i and dO_i staged into TMEM
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&bar_kvf[s], 1);
             mbar_init(&bar_kve[s], 1);
         }
         mbar_init(&bar_sf, 1);
         mbar_init(&bar_df, 1);
-        mbar_init(&bar_pd, C::kEwThreads);
+        mbar_init(&bar_sr, C::kEwThreads);  // S read: its columns may be overwritten
+        mbar_init(&bar_pd, C::kEwThreads);  // dS written over dP
         mbar_init(&bar_done, 1);
         mbar_init(&bar_fin, 1);
         mbar_fence_init();
@@ -89,17 +102,8 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
     if (warp == C::kProducerWarp) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
-            tma_prefetch_desc(&p.tm_q);
             tma_prefetch_desc(&p.tm_k);
             tma_prefetch_desc(&p.tm_v);
-            tma_prefetch_desc(&p.tm_do);
-            mbar_arrive_expect_tx(&bar_qd, 2 * C::kTileBytes);
-            for (int c = 0; c < C::kChunks; ++c) {
-                tma_load_3d(smem + C::kOffQ + c * kChunkBytes, &p.tm_q, &bar_qd, c * kChunkElems,
-                            qt * kTileRows, bh);
-                tma_load_3d(smem + C::kOffDO + c * kChunkBytes, &p.tm_do, &bar_qd, c * kChunkElems,
-                            qt * kTileRows, bh);
-            }
             bool ok = true;
             int issued = 0;
             for (int j = 0; j < n_kv; ++j) {
@@ -119,7 +123,6 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
                 issued = j + 1;
             }
             if (!ok) record_timeout(p.status, abort_v);
-            wait_bounded(&bar_qd, 0, nullptr, p.timeout_ns);
             for (int j = issued - 1; j >= 0 && j >= issued - C::kStages; --j)
                 wait_bounded(&bar_kvf[j % C::kStages], (uint32_t)(j / C::kStages) & 1u, nullptr,
                              p.timeout_ns);
@@ -127,44 +130,69 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
     } else if (warp == C::kMmaWarp) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
-            const uint32_t q_base = smem_u32(smem + C::kOffQ);
-            const uint32_t do_base = smem_u32(smem + C::kOffDO);
-            bool ok = wait_bounded(&bar_qd, 0, abort_v, p.timeout_ns);
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int st = j % C::kStages;
-                const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
-                if (!wait_bounded(&bar_kvf[st], ph, abort_v, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
+            auto k_base = [&](int j) {
+                return smem_u32(smem + C::kOffK + (j % C::kStages) * C::kTileBytes);
+            };
+            auto v_base = [&](int j) {
+                return smem_u32(smem + C::kOffV + (j % C::kStages) * C::kTileBytes);
+            };
+            auto wait_stage = [&](int j) {
+                const bool r = wait_bounded(&bar_kvf[j % C::kStages],
+                                            (uint32_t)(j / C::kStages) & 1u, abort_v, p.timeout_ns);
                 tc_fence_after_sync();
-                const uint32_t k_base = smem_u32(smem + C::kOffK + st * C::kTileBytes);
-                const uint32_t v_base = smem_u32(smem + C::kOffV + st * C::kTileBytes);
+                return r;
+            };
+            auto issue_s = [&](int j) {  // S = Q K_j^T, Q from TMEM
+                const uint64_t kd = sdesc_kmajor_sw128(k_base(j));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    mma_ss(tmem + C::kTmS, sdesc_kmajor_sw128(q_base + off),
-                           sdesc_kmajor_sw128(k_base + off), C::kIdescS, kk > 0 ? 1u : 0u);
+                    mma_ts(tmem + C::kTmS, tmem + C::kTmQ + kk * 8, sdesc_advance(kd, off),
+                           C::kIdescS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bar_sf);
+            };
+            auto issue_dp = [&](int j) {  // dP = dO V_j^T, dO from TMEM
+                const uint64_t vd = sdesc_kmajor_sw128(v_base(j));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    mma_ss(tmem + C::kTmDP, sdesc_kmajor_sw128(do_base + off),
-                           sdesc_kmajor_sw128(v_base + off), C::kIdescS, kk > 0 ? 1u : 0u);
+                    mma_ts(tmem + C::kTmDP, tmem + C::kTmDO + kk * 8, sdesc_advance(vd, off),
+                           C::kIdescS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bar_df);
-                if (!wait_bounded(&bar_pd, (uint32_t)j & 1u, abort_v, p.timeout_ns)) {
+            };
+            bool ok = wait_bounded(&bar_qt, 0, abort_v, p.timeout_ns);
+            tc_fence_after_sync();
+            if (ok && n_kv > 0) {
+                ok = wait_stage(0);
+                if (ok) {
+                    issue_s(0);
+                    issue_dp(0);
+                }
+            }
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const uint32_t par = (uint32_t)j & 1u;
+                if (j + 1 < n_kv) {
+                    // S of the next key tile as soon as this one's S has been read.
+                    if (!wait_bounded(&bar_sr, par, abort_v, p.timeout_ns) || !wait_stage(j + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    issue_s(j + 1);
+                }
+                if (!wait_bounded(&bar_pd, par, abort_v, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
+                const uint64_t kmd = sdesc_mnmajor_sw128(k_base(j), kChunkBytes);
 #pragma unroll
                 for (int kk = 0; kk < kTileRows / 16; ++kk)
-                    mma_ts(tmem + C::kTmDQ, tmem + C::kTmS + kk * 8,
-                           sdesc_mnmajor_sw128(k_base + kk * 2048, kChunkBytes), C::kIdescG,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(&bar_kve[st]);
+                    mma_ts(tmem + C::kTmDQ, tmem + C::kTmDP + kk * 8, sdesc_advance(kmd, kk * 2048),
+                           C::kIdescG, (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&bar_kve[j % C::kStages]);  // K_j, V_j fully read
+                if (j + 1 < n_kv) issue_dp(j + 1);     // after dQ_j read the dS columns
             }
             if (ok) mma_commit(&bar_done);
             if (!ok) record_timeout(p.status, abort_v);
@@ -182,6 +210,33 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const int q_row = qt * kTileRows + row;  // < Lpad always
         const int c0 = part * kC;
+        // Stage this warp's slice (D/kSplit elements) of the Q and dO rows into TMEM as
+        // packed 16-bit pairs; rows past L are zeros.
+        {
+            constexpr int kE = D / C::kSplit;       // elements per warp slice
+            constexpr int kW = C::kStageCols;       // packed 32-bit columns per slice
+            const bool valid = q_row < p.L;
+            const size_t eoff = ((size_t)bh * p.L + q_row) * D + part * kE;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint4* src =
+                    reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(
+                                                       which ? p.dout : p.q) + eoff * 2);
+                uint32_t w[kW];
+#pragma unroll
+                for (int v = 0; v < kW / 4; ++v) {
+                    const uint4 x = valid ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+                    w[4 * v + 0] = x.x;
+                    w[4 * v + 1] = x.y;
+                    w[4 * v + 2] = x.z;
+                    w[4 * v + 3] = x.w;
+                }
+                tmem_st<kW>(tmem + lane_off + (which ? C::kTmDO : C::kTmQ) + part * kW, w);
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(&bar_qt);
+        }
         const float lse2 = p.lse2_pad[(size_t)bh * p.Lpad + q_row];
         const float dlt = p.delta_pad[(size_t)bh * p.Lpad + q_row];
         bool ok = true;
@@ -189,13 +244,16 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
             const int key0 = j * kTileRows + c0;
             const bool masked = (CAUSAL && j == n_kv - 1) || (j * kTileRows + kTileRows > p.L);
             const int klim = CAUSAL ? min(p.L - 1, q_row) : (p.L - 1);
+            const uint32_t par = (uint32_t)j & 1u;
             float pv[kC];
-            ok = wait_bounded(&bar_sf, (uint32_t)j & 1u, abort_v, p.timeout_ns);
+            ok = wait_bounded(&bar_sf, par, abort_v, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after_sync();
                 uint32_t r[kC];
                 tmem_ld_cols<kC>(tmem + lane_off + C::kTmS + c0, r);
+                tc_fence_before_sync();
+                mbar_arrive(&bar_sr);
 #pragma unroll
                 for (int i = 0; i < kC; ++i)
                     pv[i] = ex2_approx(fmaf(__uint_as_float(r[i]), p.scale_log2, -lse2));
@@ -204,23 +262,29 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
                     for (int i = 0; i < kC; ++i)
                         if (key0 + i > klim) pv[i] = 0.0f;
                 }
-                ok = wait_bounded(&bar_df, (uint32_t)j & 1u, abort_v, p.timeout_ns);
+                ok = wait_bounded(&bar_df, par, abort_v, p.timeout_ns);
                 ok = __all_sync(0xffffffffu, ok);
             }
             if (ok) {
                 tc_fence_after_sync();
-                uint32_t r[kC];
-                tmem_ld_cols<kC>(tmem + lane_off + C::kTmDP + c0, r);
+                constexpr int kLd = kC >= 64 ? 32 : 16;  // dP columns per load (registers)
 #pragma unroll
-                for (int i = 0; i < kC; ++i) pv[i] = pv[i] * (__uint_as_float(r[i]) - dlt);
+                for (int h = 0; h < kC / kLd; ++h) {
+                    uint32_t r[kLd];
+                    tmem_ld<kLd>(tmem + lane_off + C::kTmDP + c0 + h * kLd, r);
+#pragma unroll
+                    for (int i = 0; i < kLd; ++i) pv[h * kLd + i] *= __uint_as_float(r[i]) - dlt;
+                }
             }
-            ok = bar_and(grp_bar, kGrpThreads, ok);  // all slices have read S: dS may overwrite it
+            // Every slice of the quadrant has read its dP columns before dS overwrites them.
+            // (All warps reach this barrier once per key tile on every path.)
+            ok = bar_and(grp_bar, kGrpThreads, ok);
             if (!ok) break;
             {
                 uint32_t pk[kC / 2];
 #pragma unroll
                 for (int i = 0; i < kC / 2; ++i) pk[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
-                tmem_st<kC / 2>(tmem + lane_off + C::kTmS + part * (kC / 2), pk);
+                tmem_st<kC / 2>(tmem + lane_off + C::kTmDP + part * (kC / 2), pk);
             }
             tmem_st_wait();
             tc_fence_before_sync();

@@ -182,14 +182,14 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                 return true;
             };
             auto issue_s = [&](int t, int j) {
-                const uint32_t q_base = smem_u32(smem + C::kOffQ + t * C::kTileBytes);
-                const uint32_t k_base =
-                    smem_u32(smem + C::kOffK + (j % C::kKStages) * C::kTileBytes);
+                const uint64_t qd = sdesc_kmajor_sw128(smem_u32(smem + C::kOffQ + t * C::kTileBytes));
+                const uint64_t kd =
+                    sdesc_kmajor_sw128(smem_u32(smem + C::kOffK + (j % C::kKStages) * C::kTileBytes));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    mma_ss(tmem + C::kTmS + 128 * t, sdesc_kmajor_sw128(q_base + off),
-                           sdesc_kmajor_sw128(k_base + off), C::kIdescS, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + C::kTmS + 128 * t, sdesc_advance(qd, off), sdesc_advance(kd, off),
+                           C::kIdescS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bar_sf[t]);
             };
@@ -201,10 +201,11 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                                   p.timeout_ns))
                     return false;
                 tc_fence_after_sync();
-                const uint32_t v_base = smem_u32(smem + C::kOffV + st * C::kTileBytes);
+                const uint64_t vd =
+                    sdesc_mnmajor_sw128(smem_u32(smem + C::kOffV + st * C::kTileBytes), kChunkBytes);
 #pragma unroll
                 for (int kk = 0; kk < kTileRows / 16; ++kk) {
-                    const uint64_t bd = sdesc_mnmajor_sw128(v_base + kk * 2048, kChunkBytes);
+                    const uint64_t bd = sdesc_advance(vd, kk * 2048);
                     mma_ts(tmem + C::kTmO + D * t, tmem + C::kTmS + 128 * t + kk * 8, bd,
                            C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
                 }

@@ -129,6 +129,44 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 }
 
 // ---------------------------------------------------------------------------------------
+// Thread-block clusters (all data stays in this GPU's own memory)
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster arrives and waits (release/acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// TMA tile load whose data (and complete_tx on the mbarrier at the same offset) lands in
+// every CTA of `cta_mask`, at the same shared-memory offsets as in the issuing CTA.
+__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                               int x, int y, int z, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// Untiled bulk copy multicast to the CTAs of `cta_mask` (same rules as bulk_load).
+__device__ __forceinline__ void bulk_load_mc(void* dst, const void* src, uint32_t bytes,
+                                             uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "h"(cta_mask)
+        : "memory");
+}
+
+// ---------------------------------------------------------------------------------------
 // Tensor memory
 // ---------------------------------------------------------------------------------------
 // Whole warp: allocates `ncols` TMEM columns (power of two, 32..512); base address -> *dst.
@@ -226,8 +264,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "memory");
 }
 
-// Column-count generic forms (N = 16 or 32) used by kernels whose per-warp slice width is a
-// compile-time constant.
+// Warp-wide: thread t writes 8 consecutive 32-bit columns of lane (lane_base + t).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+        : "memory");
+}
+
+// Column-count generic forms (N = 16 or 32; stores also 8) used by kernels whose per-warp
+// slice width is a compile-time constant.
 template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]) {
     static_assert(N == 16 || N == 32, "16 or 32 columns");
@@ -236,8 +283,9 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]) {
 }
 template <int N>
 __device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&r)[N]) {
-    static_assert(N == 16 || N == 32, "16 or 32 columns");
-    if constexpr (N == 16) tmem_st16(taddr, r);
+    static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 columns");
+    if constexpr (N == 8) tmem_st8(taddr, r);
+    else if constexpr (N == 16) tmem_st16(taddr, r);
     else tmem_st32(taddr, r);
 }
 
@@ -262,6 +310,12 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
 __device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t chunk_bytes) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((chunk_bytes >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)(1024u >> 4) << 32) | ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
+}
+
+// The same matrix descriptor with its start address moved by `bytes` (a multiple of 16; the
+// resulting address stays below 256 KiB, so only the 14-bit start field changes).
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t bytes) {
+    return desc + (uint64_t)(bytes >> 4);
 }
 
 // Instruction descriptor: fp32 accumulate, A/B both bf16 (or both fp16), dense.
@@ -317,6 +371,16 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
                         reinterpret_cast<uint32_t(&)[32]>(r[64 * h]),
                         reinterpret_cast<uint32_t(&)[32]>(r[64 * h + 32]));
     }
+}
+
+// Like mma_commit, but arrives on the mbarrier at the same offset in every CTA of
+// `cta_mask` (used to release a multicast-filled shared-memory stage in all its readers).
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // ---------------------------------------------------------------------------------------
