@@ -142,85 +142,84 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------ MMA issuer ------------------------------
-        if (lane == 0) {
-            const uint32_t k_base = smem_u32(smem + C::kOffK);
-            const uint32_t v_base = smem_u32(smem + C::kOffV);
-            auto q_base = [&](int t) {
-                return smem_u32(smem + C::kOffQ + (t % C::kStages) * C::kTileBytes);
-            };
-            auto do_base = [&](int t) {
-                return smem_u32(smem + C::kOffDO + (t % C::kStages) * C::kTileBytes);
-            };
-            auto wait_stage = [&](int t) {
-                const bool r = wait_bounded(&bar_qf[t % C::kStages],
-                                            (uint32_t)(t / C::kStages) & 1u, abort_v, p.timeout_ns);
-                tc_fence_after_sync();
-                return r;
-            };
-            const uint64_t kdesc = sdesc_kmajor_sw128(k_base);
-            const uint64_t vdesc = sdesc_kmajor_sw128(v_base);
-            auto issue_st = [&](int t) {  // S^T = K Q_t^T
-                const uint64_t qd = sdesc_kmajor_sw128(q_base(t));
+        // The whole warp walks the loop (warp-uniform values); one elected lane issues.
+        const uint32_t k_base = smem_u32(smem + C::kOffK);
+        const uint32_t v_base = smem_u32(smem + C::kOffV);
+        auto q_base = [&](int t) {
+            return smem_u32(smem + C::kOffQ + (t % C::kStages) * C::kTileBytes);
+        };
+        auto do_base = [&](int t) {
+            return smem_u32(smem + C::kOffDO + (t % C::kStages) * C::kTileBytes);
+        };
+        auto wait_stage = [&](int t) {
+            const bool r = wait_warp(&bar_qf[t % C::kStages],
+                                        (uint32_t)(t / C::kStages) & 1u, abort_v, p.timeout_ns);
+            tc_fence_after_sync();
+            return r;
+        };
+        const uint64_t kdesc = sdesc_kmajor_sw128(k_base);
+        const uint64_t vdesc = sdesc_kmajor_sw128(v_base);
+        auto issue_st = [&](int t) {  // S^T = K Q_t^T
+            const uint64_t qd = sdesc_kmajor_sw128(q_base(t));
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    mma_ss(tmem + C::kTmST, sdesc_advance(kdesc, off), sdesc_advance(qd, off),
-                           C::kIdescS, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&bar_sf);
-            };
-            auto issue_dpt = [&](int t) {  // dP^T = V dO_t^T
-                const uint64_t dd = sdesc_kmajor_sw128(do_base(t));
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    mma_ss(tmem + C::kTmDPT, sdesc_advance(vdesc, off), sdesc_advance(dd, off),
-                           C::kIdescS, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&bar_df);
-            };
-            bool ok = wait_bounded(&bar_kv, 0, abort_v, p.timeout_ns);
-            if (ok && n_it > 0) {
-                ok = wait_stage(0);
-                if (ok) {
-                    issue_st(0);
-                    issue_dpt(0);
-                }
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                mma_ss_w(tmem + C::kTmST, sdesc_advance(kdesc, off), sdesc_advance(qd, off),
+                       C::kIdescS, kk > 0 ? 1u : 0u);
             }
-            for (int t = 0; t < n_it && ok; ++t) {
-                const uint32_t par = (uint32_t)t & 1u;
-                if (t + 1 < n_it) {
-                    // S^T of the next query tile as soon as this one's S^T has been read.
-                    if (!wait_bounded(&bar_sr, par, abort_v, p.timeout_ns) || !wait_stage(t + 1)) {
-                        ok = false;
-                        break;
-                    }
-                    issue_st(t + 1);
-                }
-                if (!wait_bounded(&bar_ppd, par, abort_v, p.timeout_ns)) {
+            mma_commit_w(&bar_sf);
+        };
+        auto issue_dpt = [&](int t) {  // dP^T = V dO_t^T
+            const uint64_t dd = sdesc_kmajor_sw128(do_base(t));
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                mma_ss_w(tmem + C::kTmDPT, sdesc_advance(vdesc, off), sdesc_advance(dd, off),
+                       C::kIdescS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit_w(&bar_df);
+        };
+        bool ok = wait_warp(&bar_kv, 0, abort_v, p.timeout_ns);
+        if (ok && n_it > 0) {
+            ok = wait_stage(0);
+            if (ok) {
+                issue_st(0);
+                issue_dpt(0);
+            }
+        }
+        for (int t = 0; t < n_it && ok; ++t) {
+            const uint32_t par = (uint32_t)t & 1u;
+            if (t + 1 < n_it) {
+                // S^T of the next query tile as soon as this one's S^T has been read.
+                if (!wait_warp(&bar_sr, par, abort_v, p.timeout_ns) || !wait_stage(t + 1)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after_sync();
-                const uint32_t acc0 = t > 0 ? 1u : 0u;
-                const uint64_t dod = sdesc_mnmajor_sw128(do_base(t), kChunkBytes);
-                const uint64_t qmd = sdesc_mnmajor_sw128(q_base(t), kChunkBytes);
-#pragma unroll
-                for (int kk = 0; kk < kTileRows / 16; ++kk)
-                    mma_ts(tmem + C::kTmDV, tmem + C::kTmDPT + kk * 8,
-                           sdesc_advance(dod, kk * 2048), C::kIdescG, (acc0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < kTileRows / 16; ++kk)
-                    mma_ts(tmem + C::kTmDK, tmem + C::kTmDPT + 64 + kk * 8,
-                           sdesc_advance(qmd, kk * 2048), C::kIdescG, (acc0 || kk > 0) ? 1u : 0u);
-                mma_commit(&bar_qe[t % C::kStages]);  // stage t fully read
-                if (t + 1 < n_it) issue_dpt(t + 1);     // after dV_t, dK_t read the dP^T columns
+                issue_st(t + 1);
             }
-            if (ok) mma_commit(&bar_done);
-            if (!ok) record_timeout(p.status, abort_v);
-            mma_commit(&bar_fin);
-            wait_bounded(&bar_fin, 0, nullptr, p.timeout_ns);
+            if (!wait_warp(&bar_ppd, par, abort_v, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t acc0 = t > 0 ? 1u : 0u;
+            const uint64_t dod = sdesc_mnmajor_sw128(do_base(t), kChunkBytes);
+            const uint64_t qmd = sdesc_mnmajor_sw128(q_base(t), kChunkBytes);
+#pragma unroll
+            for (int kk = 0; kk < kTileRows / 16; ++kk)
+                mma_ts_w(tmem + C::kTmDV, tmem + C::kTmDPT + kk * 8,
+                       sdesc_advance(dod, kk * 2048), C::kIdescG, (acc0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < kTileRows / 16; ++kk)
+                mma_ts_w(tmem + C::kTmDK, tmem + C::kTmDPT + 64 + kk * 8,
+                       sdesc_advance(qmd, kk * 2048), C::kIdescG, (acc0 || kk > 0) ? 1u : 0u);
+            mma_commit_w(&bar_qe[t % C::kStages]);  // stage t fully read
+            if (t + 1 < n_it) issue_dpt(t + 1);     // after dV_t, dK_t read the dP^T columns
         }
+        if (ok) mma_commit_w(&bar_done);
+        if (!ok && lane == 0) record_timeout(p.status, abort_v);
+        mma_commit_w(&bar_fin);
+        wait_warp(&bar_fin, 0, nullptr, p.timeout_ns);
     } else {
         // ------------------------------ elementwise warps ------------------------------
         constexpr int kC = C::kCols;

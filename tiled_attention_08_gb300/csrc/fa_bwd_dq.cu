@@ -129,76 +129,75 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------ MMA issuer ------------------------------
-        if (lane == 0) {
-            auto k_base = [&](int j) {
-                return smem_u32(smem + C::kOffK + (j % C::kStages) * C::kTileBytes);
-            };
-            auto v_base = [&](int j) {
-                return smem_u32(smem + C::kOffV + (j % C::kStages) * C::kTileBytes);
-            };
-            auto wait_stage = [&](int j) {
-                const bool r = wait_bounded(&bar_kvf[j % C::kStages],
-                                            (uint32_t)(j / C::kStages) & 1u, abort_v, p.timeout_ns);
-                tc_fence_after_sync();
-                return r;
-            };
-            auto issue_s = [&](int j) {  // S = Q K_j^T, Q from TMEM
-                const uint64_t kd = sdesc_kmajor_sw128(k_base(j));
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    mma_ts(tmem + C::kTmS, tmem + C::kTmQ + kk * 8, sdesc_advance(kd, off),
-                           C::kIdescS, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&bar_sf);
-            };
-            auto issue_dp = [&](int j) {  // dP = dO V_j^T, dO from TMEM
-                const uint64_t vd = sdesc_kmajor_sw128(v_base(j));
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    mma_ts(tmem + C::kTmDP, tmem + C::kTmDO + kk * 8, sdesc_advance(vd, off),
-                           C::kIdescS, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&bar_df);
-            };
-            bool ok = wait_bounded(&bar_qt, 0, abort_v, p.timeout_ns);
+        // The whole warp walks the loop (warp-uniform values); one elected lane issues.
+        auto k_base = [&](int j) {
+            return smem_u32(smem + C::kOffK + (j % C::kStages) * C::kTileBytes);
+        };
+        auto v_base = [&](int j) {
+            return smem_u32(smem + C::kOffV + (j % C::kStages) * C::kTileBytes);
+        };
+        auto wait_stage = [&](int j) {
+            const bool r = wait_warp(&bar_kvf[j % C::kStages],
+                                        (uint32_t)(j / C::kStages) & 1u, abort_v, p.timeout_ns);
             tc_fence_after_sync();
-            if (ok && n_kv > 0) {
-                ok = wait_stage(0);
-                if (ok) {
-                    issue_s(0);
-                    issue_dp(0);
-                }
+            return r;
+        };
+        auto issue_s = [&](int j) {  // S = Q K_j^T, Q from TMEM
+            const uint64_t kd = sdesc_kmajor_sw128(k_base(j));
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                mma_ts_w(tmem + C::kTmS, tmem + C::kTmQ + kk * 8, sdesc_advance(kd, off),
+                       C::kIdescS, kk > 0 ? 1u : 0u);
             }
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const uint32_t par = (uint32_t)j & 1u;
-                if (j + 1 < n_kv) {
-                    // S of the next key tile as soon as this one's S has been read.
-                    if (!wait_bounded(&bar_sr, par, abort_v, p.timeout_ns) || !wait_stage(j + 1)) {
-                        ok = false;
-                        break;
-                    }
-                    issue_s(j + 1);
-                }
-                if (!wait_bounded(&bar_pd, par, abort_v, p.timeout_ns)) {
+            mma_commit_w(&bar_sf);
+        };
+        auto issue_dp = [&](int j) {  // dP = dO V_j^T, dO from TMEM
+            const uint64_t vd = sdesc_kmajor_sw128(v_base(j));
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                mma_ts_w(tmem + C::kTmDP, tmem + C::kTmDO + kk * 8, sdesc_advance(vd, off),
+                       C::kIdescS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit_w(&bar_df);
+        };
+        bool ok = wait_warp(&bar_qt, 0, abort_v, p.timeout_ns);
+        tc_fence_after_sync();
+        if (ok && n_kv > 0) {
+            ok = wait_stage(0);
+            if (ok) {
+                issue_s(0);
+                issue_dp(0);
+            }
+        }
+        for (int j = 0; j < n_kv && ok; ++j) {
+            const uint32_t par = (uint32_t)j & 1u;
+            if (j + 1 < n_kv) {
+                // S of the next key tile as soon as this one's S has been read.
+                if (!wait_warp(&bar_sr, par, abort_v, p.timeout_ns) || !wait_stage(j + 1)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after_sync();
-                const uint64_t kmd = sdesc_mnmajor_sw128(k_base(j), kChunkBytes);
-#pragma unroll
-                for (int kk = 0; kk < kTileRows / 16; ++kk)
-                    mma_ts(tmem + C::kTmDQ, tmem + C::kTmDP + kk * 8, sdesc_advance(kmd, kk * 2048),
-                           C::kIdescG, (j > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(&bar_kve[j % C::kStages]);  // K_j, V_j fully read
-                if (j + 1 < n_kv) issue_dp(j + 1);     // after dQ_j read the dS columns
+                issue_s(j + 1);
             }
-            if (ok) mma_commit(&bar_done);
-            if (!ok) record_timeout(p.status, abort_v);
-            mma_commit(&bar_fin);
-            wait_bounded(&bar_fin, 0, nullptr, p.timeout_ns);
+            if (!wait_warp(&bar_pd, par, abort_v, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint64_t kmd = sdesc_mnmajor_sw128(k_base(j), kChunkBytes);
+#pragma unroll
+            for (int kk = 0; kk < kTileRows / 16; ++kk)
+                mma_ts_w(tmem + C::kTmDQ, tmem + C::kTmDP + kk * 8, sdesc_advance(kmd, kk * 2048),
+                       C::kIdescG, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit_w(&bar_kve[j % C::kStages]);  // K_j, V_j fully read
+            if (j + 1 < n_kv) issue_dp(j + 1);     // after dQ_j read the dS columns
         }
+        if (ok) mma_commit_w(&bar_done);
+        if (!ok && lane == 0) record_timeout(p.status, abort_v);
+        mma_commit_w(&bar_fin);
+        wait_warp(&bar_fin, 0, nullptr, p.timeout_ns);
     } else {
         // ------------------------------ elementwise warps ------------------------------
         constexpr int kC = C::kCols;

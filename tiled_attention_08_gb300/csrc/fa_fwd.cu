@@ -168,85 +168,84 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
         }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------ MMA issuer ------------------------------
-        if (lane == 0) {
-            bool ok = wait_bounded(&bar_q, 0, abort_v, p.timeout_ns);
-            int k_ready = -1;  // newest K tile known to have landed
-            auto wait_k = [&](int j) -> bool {
-                if (k_ready >= j) return true;
-                const int st = j % C::kKStages;
-                if (!wait_bounded(&bar_kf[st], (uint32_t)(j / C::kKStages) & 1u, abort_v,
-                                  p.timeout_ns))
-                    return false;
-                tc_fence_after_sync();
-                k_ready = j;
-                return true;
-            };
-            auto issue_s = [&](int t, int j) {
-                const uint64_t qd = sdesc_kmajor_sw128(smem_u32(smem + C::kOffQ + t * C::kTileBytes));
-                const uint64_t kd =
-                    sdesc_kmajor_sw128(smem_u32(smem + C::kOffK + (j % C::kKStages) * C::kTileBytes));
+        // The whole warp walks the loop (warp-uniform values); one elected lane issues.
+        bool ok = wait_warp(&bar_q, 0, abort_v, p.timeout_ns);
+        int k_ready = -1;  // newest K tile known to have landed
+        auto wait_k = [&](int j) -> bool {
+            if (k_ready >= j) return true;
+            const int st = j % C::kKStages;
+            if (!wait_warp(&bar_kf[st], (uint32_t)(j / C::kKStages) & 1u, abort_v,
+                              p.timeout_ns))
+                return false;
+            tc_fence_after_sync();
+            k_ready = j;
+            return true;
+        };
+        auto issue_s = [&](int t, int j) {
+            const uint64_t qd = sdesc_kmajor_sw128(smem_u32(smem + C::kOffQ + t * C::kTileBytes));
+            const uint64_t kd =
+                sdesc_kmajor_sw128(smem_u32(smem + C::kOffK + (j % C::kKStages) * C::kTileBytes));
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    mma_ss(tmem + C::kTmS + 128 * t, sdesc_advance(qd, off), sdesc_advance(kd, off),
-                           C::kIdescS, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&bar_sf[t]);
-            };
-            auto issue_pv = [&](int t, int j) -> bool {
-                const int st = j % C::kVStages;
-                if (!wait_bounded(&bar_pf[t], (uint32_t)j & 1u, abort_v, p.timeout_ns))
-                    return false;
-                if (!wait_bounded(&bar_vf[st], (uint32_t)(j / C::kVStages) & 1u, abort_v,
-                                  p.timeout_ns))
-                    return false;
-                tc_fence_after_sync();
-                const uint64_t vd =
-                    sdesc_mnmajor_sw128(smem_u32(smem + C::kOffV + st * C::kTileBytes), kChunkBytes);
-#pragma unroll
-                for (int kk = 0; kk < kTileRows / 16; ++kk) {
-                    const uint64_t bd = sdesc_advance(vd, kk * 2048);
-                    mma_ts(tmem + C::kTmO + D * t, tmem + C::kTmS + 128 * t + kk * 8, bd,
-                           C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                if (j + 1 == (t ? n_kv_b : n_kv_a)) mma_commit(&bar_oready[t]);  // O_t is final
-                return true;
-            };
-            if (ok && n_kv > 0) {
-                ok = wait_k(0);
-                if (ok) {
-                    issue_s(0, 0);
-                    if (n_kv_b > 0) issue_s(1, 0);
-                    mma_commit(&bar_ke[0]);
-                }
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                mma_ss_w(tmem + C::kTmS + 128 * t, sdesc_advance(qd, off), sdesc_advance(kd, off),
+                       C::kIdescS, kk > 0 ? 1u : 0u);
             }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const bool next = j + 1 < n_kv;
+            mma_commit_w(&bar_sf[t]);
+        };
+        auto issue_pv = [&](int t, int j) -> bool {
+            const int st = j % C::kVStages;
+            if (!wait_warp(&bar_pf[t], (uint32_t)j & 1u, abort_v, p.timeout_ns))
+                return false;
+            if (!wait_warp(&bar_vf[st], (uint32_t)(j / C::kVStages) & 1u, abort_v,
+                              p.timeout_ns))
+                return false;
+            tc_fence_after_sync();
+            const uint64_t vd =
+                sdesc_mnmajor_sw128(smem_u32(smem + C::kOffV + st * C::kTileBytes), kChunkBytes);
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const int n_t = t ? n_kv_b : n_kv_a;
-                    if (!ok) break;
-                    if (j < n_t && !issue_pv(t, j)) {
+            for (int kk = 0; kk < kTileRows / 16; ++kk) {
+                const uint64_t bd = sdesc_advance(vd, kk * 2048);
+                mma_ts_w(tmem + C::kTmO + D * t, tmem + C::kTmS + 128 * t + kk * 8, bd,
+                       C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (j + 1 == (t ? n_kv_b : n_kv_a)) mma_commit_w(&bar_oready[t]);  // O_t is final
+            return true;
+        };
+        if (ok && n_kv > 0) {
+            ok = wait_k(0);
+            if (ok) {
+                issue_s(0, 0);
+                if (n_kv_b > 0) issue_s(1, 0);
+                mma_commit_w(&bar_ke[0]);
+            }
+        }
+        for (int j = 0; ok && j < n_kv; ++j) {
+            const bool next = j + 1 < n_kv;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int n_t = t ? n_kv_b : n_kv_a;
+                if (!ok) break;
+                if (j < n_t && !issue_pv(t, j)) {
+                    ok = false;
+                    break;
+                }
+                if (next && j + 1 < n_t) {
+                    if (!wait_k(j + 1)) {
                         ok = false;
                         break;
                     }
-                    if (next && j + 1 < n_t) {
-                        if (!wait_k(j + 1)) {
-                            ok = false;
-                            break;
-                        }
-                        issue_s(t, j + 1);
-                    }
+                    issue_s(t, j + 1);
                 }
-                if (!ok) break;
-                mma_commit(&bar_ve[j % C::kVStages]);                // V_j read by both PVs
-                if (next) mma_commit(&bar_ke[(j + 1) % C::kKStages]);  // K_{j+1} read by both S
             }
-            if (!ok) record_timeout(p.status, abort_v);
-            // Every issued MMA must finish before TMEM is released.
-            mma_commit(&bar_fin);
-            wait_bounded(&bar_fin, 0, nullptr, p.timeout_ns);
+            if (!ok) break;
+            mma_commit_w(&bar_ve[j % C::kVStages]);                // V_j read by both PVs
+            if (next) mma_commit_w(&bar_ke[(j + 1) % C::kKStages]);  // K_{j+1} read by both S
         }
+        if (!ok && lane == 0) record_timeout(p.status, abort_v);
+        // Every issued MMA must finish before TMEM is released.
+        mma_commit_w(&bar_fin);
+        wait_warp(&bar_fin, 0, nullptr, p.timeout_ns);
     } else {
         // ------------------------------ softmax warps ------------------------------
         constexpr int kC = C::kCols;

@@ -44,6 +44,10 @@ __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t nthreads, bool pre
     return r != 0;
 }
 
+// Bounded wait by every lane of a warp, with a warp-uniform result.
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                          uint64_t timeout_ns);
+
 // Records a timeout in the device status word (first error wins) and tells the other roles
 // of the CTA to stop.
 __device__ __forceinline__ void record_timeout(int* status, volatile int* abort_flag) {
@@ -99,6 +103,11 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
         if (abort != nullptr && *abort) return false;
         if (global_timer_ns() - t0 > timeout_ns) return false;
     }
+}
+
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                          uint64_t timeout_ns) {
+    return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort, timeout_ns));
 }
 
 // ---------------------------------------------------------------------------------------
@@ -346,6 +355,38 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Warp-converged forms: every lane of the warp executes the call with the same (warp-uniform)
+// arguments, and one lane chosen by elect.sync issues the instruction.  Keeping the issuing
+// warp converged lets the descriptors stay warp-uniform values.
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+            smem_u32(bar))
         : "memory");
 }
 
