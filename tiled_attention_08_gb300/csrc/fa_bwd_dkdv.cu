@@ -236,9 +236,9 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
             const int it = it0 + t;
             const int st = t % C::kStages;
             const uint32_t ph = (uint32_t)(t / C::kStages) & 1u;
-            const float* lse2v =
-                reinterpret_cast<const float*>(smem + C::kOffVec + st * C::kVecBytes) + c0;
-            const float* dltv = lse2v + kTileRows;
+            // LSE*log2e and Delta of this warp's query columns (broadcast shared reads).
+            const uint32_t lse2_addr = smem_u32(smem + C::kOffVec + st * C::kVecBytes) + c0 * 4;
+            const uint32_t dlt_addr = lse2_addr + kTileRows * 4;
             const int q0 = it * kTileRows + c0;
             const bool masked = (CAUSAL && it == kt) || (it * kTileRows + kTileRows > p.L);
             const int qlim = p.L - 1;  // last valid query
@@ -256,8 +256,13 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                 tc_fence_before_sync();
                 mbar_arrive(&bar_sr);
 #pragma unroll
-                for (int i = 0; i < kC; ++i)
-                    pv[i] = ex2_approx(fmaf(__uint_as_float(r[i]), p.scale_log2, -lse2v[i]));
+                for (int i = 0; i < kC; i += 4) {
+                    const float4 l = lds_f32x4(lse2_addr + i * 4);
+                    pv[i + 0] = ex2_approx(fmaf(__uint_as_float(r[i + 0]), p.scale_log2, -l.x));
+                    pv[i + 1] = ex2_approx(fmaf(__uint_as_float(r[i + 1]), p.scale_log2, -l.y));
+                    pv[i + 2] = ex2_approx(fmaf(__uint_as_float(r[i + 2]), p.scale_log2, -l.z));
+                    pv[i + 3] = ex2_approx(fmaf(__uint_as_float(r[i + 3]), p.scale_log2, -l.w));
+                }
                 if (masked) {
 #pragma unroll
                     for (int i = 0; i < kC; ++i) {
@@ -279,8 +284,13 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                     uint32_t r[kLd];
                     tmem_ld<kLd>(tmem + lane_off + C::kTmDPT + c0 + h * kLd, r);
 #pragma unroll
-                    for (int i = 0; i < kLd; ++i)
-                        pv[h * kLd + i] *= __uint_as_float(r[i]) - dltv[h * kLd + i];
+                    for (int i = 0; i < kLd; i += 4) {
+                        const float4 d = lds_f32x4(dlt_addr + (h * kLd + i) * 4);
+                        pv[h * kLd + i + 0] *= __uint_as_float(r[i + 0]) - d.x;
+                        pv[h * kLd + i + 1] *= __uint_as_float(r[i + 1]) - d.y;
+                        pv[h * kLd + i + 2] *= __uint_as_float(r[i + 2]) - d.z;
+                        pv[h * kLd + i + 3] *= __uint_as_float(r[i + 3]) - d.w;
+                    }
                 }
             }
             // Every slice of the quadrant has read its dP^T columns before any is overwritten.

@@ -424,6 +424,18 @@ __device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) 
         : "memory");
 }
 
+// Four consecutive fp32 values from shared memory (16-byte aligned shared address).  The
+// kernels align their dynamic shared memory through an integer round trip, which leaves the
+// compiler with generic pointers; an explicit ld.shared keeps these reads on the shared path.
+__device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------------------------------
 // Math helpers
 // ---------------------------------------------------------------------------------------
