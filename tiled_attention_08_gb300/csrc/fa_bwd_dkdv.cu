@@ -61,8 +61,10 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    __shared__ uint64_t bar_kv, bar_qf[C::kStages], bar_qe[C::kStages], bar_sf, bar_df, bar_sr,
-        bar_ppd, bar_done, bar_fin;
+    // Q_i (+ LSE_i) and dO_i (+ Delta_i) have their own full/empty barriers: Q_i is released
+    // by dK_i, issued first, so the load of a later Q tile (needed early, by S^T) starts sooner.
+    __shared__ uint64_t bar_kv, bar_qf[C::kStages], bar_qe[C::kStages], bar_of[C::kStages],
+        bar_oe[C::kStages], bar_sf, bar_df, bar_sr, bar_ppd, bar_done, bar_fin;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
@@ -82,6 +84,8 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&bar_qf[s], 1);
             mbar_init(&bar_qe[s], 1);
+            mbar_init(&bar_of[s], 1);
+            mbar_init(&bar_oe[s], 1);
         }
         mbar_init(&bar_sf, 1);
         mbar_init(&bar_df, 1);
@@ -112,32 +116,42 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                             kt * kTileRows, bh);
             }
             bool ok = true;
-            int issued = 0;
+            int issued_q = 0, issued_o = 0;
             for (int t = 0; t < n_it; ++t) {
                 const int it = it0 + t;
                 const int st = t % C::kStages;
                 const uint32_t ph = (uint32_t)(t / C::kStages) & 1u;
+                const size_t voff = (size_t)bh * p.Lpad + (size_t)it * kTileRows;
+                uint8_t* vec = smem + C::kOffVec + st * C::kVecBytes;
                 if (t >= C::kStages && !wait_bounded(&bar_qe[st], ph ^ 1u, abort_v, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&bar_qf[st], 2 * C::kTileBytes + C::kVecBytes);
-                for (int c = 0; c < C::kChunks; ++c) {
+                mbar_arrive_expect_tx(&bar_qf[st], C::kTileBytes + kTileRows * 4);
+                for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(smem + C::kOffQ + st * C::kTileBytes + c * kChunkBytes, &p.tm_q,
                                 &bar_qf[st], c * kChunkElems, it * kTileRows, bh);
-                    tma_load_3d(smem + C::kOffDO + st * C::kTileBytes + c * kChunkBytes, &p.tm_do,
-                                &bar_qf[st], c * kChunkElems, it * kTileRows, bh);
-                }
-                const size_t voff = (size_t)bh * p.Lpad + (size_t)it * kTileRows;
-                uint8_t* vec = smem + C::kOffVec + st * C::kVecBytes;
                 bulk_load(vec, p.lse2_pad + voff, kTileRows * 4, &bar_qf[st]);
-                bulk_load(vec + kTileRows * 4, p.delta_pad + voff, kTileRows * 4, &bar_qf[st]);
-                issued = t + 1;
+                issued_q = t + 1;
+                if (t >= C::kStages && !wait_bounded(&bar_oe[st], ph ^ 1u, abort_v, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bar_of[st], C::kTileBytes + kTileRows * 4);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(smem + C::kOffDO + st * C::kTileBytes + c * kChunkBytes, &p.tm_do,
+                                &bar_of[st], c * kChunkElems, it * kTileRows, bh);
+                bulk_load(vec + kTileRows * 4, p.delta_pad + voff, kTileRows * 4, &bar_of[st]);
+                issued_o = t + 1;
             }
             if (!ok) record_timeout(p.status, abort_v);
+            // Drain: no copy may still be landing when the CTA exits.
             wait_bounded(&bar_kv, 0, nullptr, p.timeout_ns);
-            for (int t = issued - 1; t >= 0 && t >= issued - C::kStages; --t)
+            for (int t = issued_q - 1; t >= 0 && t >= issued_q - C::kStages; --t)
                 wait_bounded(&bar_qf[t % C::kStages], (uint32_t)(t / C::kStages) & 1u, nullptr,
+                             p.timeout_ns);
+            for (int t = issued_o - 1; t >= 0 && t >= issued_o - C::kStages; --t)
+                wait_bounded(&bar_of[t % C::kStages], (uint32_t)(t / C::kStages) & 1u, nullptr,
                              p.timeout_ns);
         }
     } else if (warp == C::kMmaWarp) {
@@ -151,9 +165,15 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
         auto do_base = [&](int t) {
             return smem_u32(smem + C::kOffDO + (t % C::kStages) * C::kTileBytes);
         };
-        auto wait_stage = [&](int t) {
-            const bool r = wait_warp(&bar_qf[t % C::kStages],
-                                        (uint32_t)(t / C::kStages) & 1u, abort_v, p.timeout_ns);
+        auto wait_q = [&](int t) {  // Q_t landed
+            const bool r = wait_warp(&bar_qf[t % C::kStages], (uint32_t)(t / C::kStages) & 1u,
+                                     abort_v, p.timeout_ns);
+            tc_fence_after_sync();
+            return r;
+        };
+        auto wait_do = [&](int t) {  // dO_t landed
+            const bool r = wait_warp(&bar_of[t % C::kStages], (uint32_t)(t / C::kStages) & 1u,
+                                     abort_v, p.timeout_ns);
             tc_fence_after_sync();
             return r;
         };
@@ -181,17 +201,16 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
         };
         bool ok = wait_warp(&bar_kv, 0, abort_v, p.timeout_ns);
         if (ok && n_it > 0) {
-            ok = wait_stage(0);
-            if (ok) {
-                issue_st(0);
-                issue_dpt(0);
-            }
+            ok = wait_q(0);
+            if (ok) issue_st(0);
+            ok = ok && wait_do(0);
+            if (ok) issue_dpt(0);
         }
         for (int t = 0; t < n_it && ok; ++t) {
             const uint32_t par = (uint32_t)t & 1u;
             if (t + 1 < n_it) {
                 // S^T of the next query tile as soon as this one's S^T has been read.
-                if (!wait_warp(&bar_sr, par, abort_v, p.timeout_ns) || !wait_stage(t + 1)) {
+                if (!wait_warp(&bar_sr, par, abort_v, p.timeout_ns) || !wait_q(t + 1)) {
                     ok = false;
                     break;
                 }
@@ -207,14 +226,21 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
             const uint64_t qmd = sdesc_mnmajor_sw128(q_base(t), kChunkBytes);
 #pragma unroll
             for (int kk = 0; kk < kTileRows / 16; ++kk)
-                mma_ts_w(tmem + C::kTmDV, tmem + C::kTmDPT + kk * 8,
-                       sdesc_advance(dod, kk * 2048), C::kIdescG, (acc0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < kTileRows / 16; ++kk)
                 mma_ts_w(tmem + C::kTmDK, tmem + C::kTmDPT + 64 + kk * 8,
                        sdesc_advance(qmd, kk * 2048), C::kIdescG, (acc0 || kk > 0) ? 1u : 0u);
-            mma_commit_w(&bar_qe[t % C::kStages]);  // stage t fully read
-            if (t + 1 < n_it) issue_dpt(t + 1);     // after dV_t, dK_t read the dP^T columns
+            mma_commit_w(&bar_qe[t % C::kStages]);  // Q_t fully read
+#pragma unroll
+            for (int kk = 0; kk < kTileRows / 16; ++kk)
+                mma_ts_w(tmem + C::kTmDV, tmem + C::kTmDPT + kk * 8,
+                       sdesc_advance(dod, kk * 2048), C::kIdescG, (acc0 || kk > 0) ? 1u : 0u);
+            mma_commit_w(&bar_oe[t % C::kStages]);  // dO_t fully read
+            if (t + 1 < n_it) {                     // after dV_t, dK_t read the dP^T columns
+                if (!wait_do(t + 1)) {
+                    ok = false;
+                    break;
+                }
+                issue_dpt(t + 1);
+            }
         }
         if (ok) mma_commit_w(&bar_done);
         if (!ok && lane == 0) record_timeout(p.status, abort_v);
@@ -273,7 +299,8 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < kC / 2; ++i) pk_p[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
                 // Phase 2: dS^T = P^T o (dP^T - Delta).
-                ok = wait_bounded(&bar_df, (uint32_t)t & 1u, abort_v, p.timeout_ns);
+                ok = wait_bounded(&bar_of[st], ph, abort_v, p.timeout_ns) &&
+                     wait_bounded(&bar_df, (uint32_t)t & 1u, abort_v, p.timeout_ns);
                 ok = __all_sync(0xffffffffu, ok);
             }
             if (ok) {
