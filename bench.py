@@ -165,9 +165,15 @@ def gpu_selector(dev) -> str:
         return str(dev.index)
 
 
-def file_sha(path: str) -> str:
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def kernel_sha(kernel: str) -> str:
+    """Hash of everything that shapes a kernel's memory traffic: its source file, the shared
+    device headers and the host launcher (tile schedule, tensor maps)."""
+    csrc = os.path.join(ROOT, "tiled_attention_08_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in (KERNEL_SOURCES[kernel], "fa_internal.h", "fa_ptx.cuh", "fa_api.cu"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel: str, workload: str):
@@ -182,8 +188,7 @@ def profiled_traffic(kernel: str, workload: str):
     rec = d.get(kernel, {}).get(workload)
     if not rec:
         return None, "no ncu capture for this kernel/workload"
-    src = os.path.join(ROOT, "tiled_attention_08_gb300", "csrc", KERNEL_SOURCES[kernel])
-    if rec.get("source_sha") != file_sha(src):
+    if rec.get("source_sha") != kernel_sha(kernel):
         return None, "kernel changed since the ncu capture"
     return float(rec["dram_bytes_per_launch"]), rec.get("note", "")
 

@@ -9,12 +9,12 @@
 //   dQ_i += dS K_j
 // dQ_i is scaled by the softmax scale and written once: no atomics, deterministic.
 //
-// GB300 layout.  A tcgen05 MMA that takes both operands from shared memory is limited by the
-// shared-memory operand path (about half the tensor rate at M = N = 128), while one whose A
-// operand sits in tensor memory runs at the full rate.  Q_i and dO_i are the A operands of S
-// and dP for every key tile, so they are staged once into TMEM (16-bit, two values per
-// column) and all three contractions here run with A in TMEM; shared memory holds only the
-// K_j / V_j ring.
+// GB300 layout.  Q_i and dO_i are the A operands of S and dP for every key tile, so they are
+// staged once into TMEM (16-bit, two values per column) and all three contractions here run
+// with A in TMEM; shared memory holds only the K_j / V_j ring.  With A in TMEM an M = N = 128
+// step reads 4 KB of shared memory instead of 8 KB (the latter is the SM's whole
+// shared-memory bandwidth over the 64 cycles a step takes), which leaves room for the TMA
+// copies that refill the ring.
 //
 // CTA roles: 4*kSplit elementwise warps (warp w: query rows 32*(w%4).. == TMEM lanes, key
 // columns [kCols*(w/4), +kCols)), then one TMA producer warp (the K_j / V_j ring) and one
