@@ -284,13 +284,16 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                     for (int c = 0; c < kC; ++c)
                         if (key0 + c > lim) s[c] = -INFINITY;
                 }
-                float m4[4] = {s[0], s[1], s[2], s[3]};
+                // Row max: four independent chains of three-input maxima.
+                float m4[4];
 #pragma unroll
-                for (int c = 4; c < kC; c += 4) {
+                for (int u = 0; u < 4; ++u) m4[u] = fmaxf(s[u], s[u + 4]);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) m4[u] = fmaxf(m4[u], s[c + u]);
+                for (int c = 8; c < kC; c += 8) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) m4[u] = fmax3(m4[u], s[c + u], s[c + 4 + u]);
                 }
-                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
             }
             if constexpr (C::kSplit > 1) {
                 red_max[t][par][part][row] = mx;
@@ -309,20 +312,30 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
             const bool rescale = (j > 0) && (m_new != m_ref);
             const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
             const float alpha = rescale ? ex2_approx(m_ref - m_new) : 1.0f;
-            float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            // Two columns per instruction for the scale-and-shift and the running sum.
+            const uint64_t scale2 = f2_make(p.scale_log2, p.scale_log2);
+            const uint64_t shift2 = f2_make(-m_use, -m_use);
+            uint64_t sum2[2] = {0ull, 0ull};  // (+0.0f, +0.0f)
 #pragma unroll
             for (int h = 0; h < kC / 32; ++h) {  // 32 columns -> 16 packed TMEM columns at a time
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2_approx(fmaf(s[h * 32 + 2 * i], p.scale_log2, -m_use));
-                    const float p1 = ex2_approx(fmaf(s[h * 32 + 2 * i + 1], p.scale_log2, -m_use));
-                    sum4[i & 3] += p0 + p1;
+                    float y0, y1;
+                    f2_split(f2_fma(f2_make(s[h * 32 + 2 * i], s[h * 32 + 2 * i + 1]), scale2,
+                                    shift2),
+                             y0, y1);
+                    const float p0 = ex2_approx(y0);
+                    const float p1 = ex2_approx(y1);
+                    sum2[i & 1] = f2_add(sum2[i & 1], f2_make(p0, p1));
                     pk[i] = pack2<BF16>(p0, p1);
                 }
                 tmem_st16(s_addr + part * (kC / 2) + h * 16, pk);
             }
-            l_sum = l_sum * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+            float sa, sb, sc, sd;
+            f2_split(sum2[0], sa, sb);
+            f2_split(sum2[1], sc, sd);
+            l_sum = l_sum * alpha + ((sa + sb) + (sc + sd));
             // S_t(j) was issued after PV_t(j-1), so every PV into O_t has completed: rescale
             // in place without waiting.
             if (__any_sync(0xffffffffu, rescale)) tmem_row_scale<C::kOCols>(o_addr, alpha);
