@@ -58,7 +58,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
 /*
  * Bytes of device workspace fa_bwd needs for this shape: two fp32 vectors per head padded to
- * a whole number of 128-row tiles (LSE * log2(e) and Delta = rowsum(dO * O)).
+ * a whole number of 128-row tiles (-LSE * log2(e) and Delta = rowsum(dO * O)).
  * Returns 0 for an empty problem or invalid sizes.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int L, int D);

@@ -278,11 +278,11 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     if (!make_map(&p.tm_q, q, sh.BH, L, D, bf16) || !make_map(&p.tm_k, k, sh.BH, L, D, bf16) ||
         !make_map(&p.tm_v, v, sh.BH, L, D, bf16) || !make_map(&p.tm_do, dout, sh.BH, L, D, bf16))
         return FA_ERR_CUDA;
-    float* lse2_pad = static_cast<float*>(workspace);
-    float* delta_pad = lse2_pad + (size_t)sh.BH * sh.Lpad;
+    float* nlse2_pad = static_cast<float*>(workspace);
+    float* delta_pad = nlse2_pad + (size_t)sh.BH * sh.Lpad;
     p.q = q;
     p.dout = dout;
-    p.lse2_pad = lse2_pad;
+    p.nlse2_pad = nlse2_pad;
     p.delta_pad = delta_pad;
     p.dq = dq;
     p.dk = dk;
@@ -302,7 +302,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     pp.o = o;
     pp.dout = dout;
     pp.lse = lse;
-    pp.lse2_pad = lse2_pad;
+    pp.nlse2_pad = nlse2_pad;
     pp.delta_pad = delta_pad;
     pp.L = L;
     pp.Lpad = sh.Lpad;

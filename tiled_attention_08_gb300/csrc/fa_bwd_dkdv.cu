@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(smem + C::kOffQ + st * C::kTileBytes + c * kChunkBytes, &p.tm_q,
                                 &bar_qf[st], c * kChunkElems, it * kTileRows, bh);
-                bulk_load(vec, p.lse2_pad + voff, kTileRows * 4, &bar_qf[st]);
+                bulk_load(vec, p.nlse2_pad + voff, kTileRows * 4, &bar_qf[st]);
                 issued_q = t + 1;
                 if (t >= C::kStages && !wait_bounded(&bar_oe[st], ph ^ 1u, abort_v, p.timeout_ns)) {
                     ok = false;
@@ -262,9 +262,9 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
             const int it = it0 + t;
             const int st = t % C::kStages;
             const uint32_t ph = (uint32_t)(t / C::kStages) & 1u;
-            // LSE*log2e and Delta of this warp's query columns (broadcast shared reads).
-            const uint32_t lse2_addr = smem_u32(smem + C::kOffVec + st * C::kVecBytes) + c0 * 4;
-            const uint32_t dlt_addr = lse2_addr + kTileRows * 4;
+            // -LSE*log2e and Delta of this warp's query columns (broadcast shared reads).
+            const uint32_t nlse2_addr = smem_u32(smem + C::kOffVec + st * C::kVecBytes) + c0 * 4;
+            const uint32_t dlt_addr = nlse2_addr + kTileRows * 4;
             const int q0 = it * kTileRows + c0;
             const bool masked = (CAUSAL && it == kt) || (it * kTileRows + kTileRows > p.L);
             const int qlim = p.L - 1;  // last valid query
@@ -281,13 +281,21 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                 tmem_ld_cols<kC>(tmem + lane_off + C::kTmST + c0, r);
                 tc_fence_before_sync();
                 mbar_arrive(&bar_sr);
+                const uint64_t scale2 = f2_make(p.scale_log2, p.scale_log2);
 #pragma unroll
-                for (int i = 0; i < kC; i += 4) {
-                    const float4 l = lds_f32x4(lse2_addr + i * 4);
-                    pv[i + 0] = ex2_approx(fmaf(__uint_as_float(r[i + 0]), p.scale_log2, -l.x));
-                    pv[i + 1] = ex2_approx(fmaf(__uint_as_float(r[i + 1]), p.scale_log2, -l.y));
-                    pv[i + 2] = ex2_approx(fmaf(__uint_as_float(r[i + 2]), p.scale_log2, -l.z));
-                    pv[i + 3] = ex2_approx(fmaf(__uint_as_float(r[i + 3]), p.scale_log2, -l.w));
+                for (int i = 0; i < kC; i += 4) {  // two columns per f32x2 instruction
+                    const float4 l = lds_f32x4(nlse2_addr + i * 4);
+                    float y0, y1, y2, y3;
+                    f2_split(f2_fma(f2_make(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                    scale2, f2_make(l.x, l.y)),
+                             y0, y1);
+                    f2_split(f2_fma(f2_make(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])),
+                                    scale2, f2_make(l.z, l.w)),
+                             y2, y3);
+                    pv[i + 0] = ex2_approx(y0);
+                    pv[i + 1] = ex2_approx(y1);
+                    pv[i + 2] = ex2_approx(y2);
+                    pv[i + 3] = ex2_approx(y3);
                 }
                 if (masked) {
 #pragma unroll
@@ -311,12 +319,19 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                     uint32_t r[kLd];
                     tmem_ld<kLd>(tmem + lane_off + C::kTmDPT + c0 + h * kLd, r);
 #pragma unroll
-                    for (int i = 0; i < kLd; i += 4) {
+                    for (int i = 0; i < kLd; i += 4) {  // P o (dP - Delta), two per instruction
                         const float4 d = lds_f32x4(dlt_addr + (h * kLd + i) * 4);
-                        pv[h * kLd + i + 0] *= __uint_as_float(r[i + 0]) - d.x;
-                        pv[h * kLd + i + 1] *= __uint_as_float(r[i + 1]) - d.y;
-                        pv[h * kLd + i + 2] *= __uint_as_float(r[i + 2]) - d.z;
-                        pv[h * kLd + i + 3] *= __uint_as_float(r[i + 3]) - d.w;
+                        float* q = pv + h * kLd + i;
+                        f2_split(f2_mul(f2_make(q[0], q[1]),
+                                        f2_sub(f2_make(__uint_as_float(r[i]),
+                                                       __uint_as_float(r[i + 1])),
+                                               f2_make(d.x, d.y))),
+                                 q[0], q[1]);
+                        f2_split(f2_mul(f2_make(q[2], q[3]),
+                                        f2_sub(f2_make(__uint_as_float(r[i + 2]),
+                                                       __uint_as_float(r[i + 3])),
+                                               f2_make(d.z, d.w))),
+                                 q[2], q[3]);
                     }
                 }
             }

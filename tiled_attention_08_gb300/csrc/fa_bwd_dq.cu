@@ -236,8 +236,9 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
             tc_fence_before_sync();
             mbar_arrive(&bar_qt);
         }
-        const float lse2 = p.lse2_pad[(size_t)bh * p.Lpad + q_row];
+        const float nlse2 = p.nlse2_pad[(size_t)bh * p.Lpad + q_row];  // -LSE * log2(e)
         const float dlt = p.delta_pad[(size_t)bh * p.Lpad + q_row];
+        const uint64_t dlt2 = f2_make(dlt, dlt);
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             const int key0 = j * kTileRows + c0;
@@ -253,9 +254,17 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
                 tmem_ld_cols<kC>(tmem + lane_off + C::kTmS + c0, r);
                 tc_fence_before_sync();
                 mbar_arrive(&bar_sr);
+                const uint64_t scale2 = f2_make(p.scale_log2, p.scale_log2);
+                const uint64_t shift2 = f2_make(nlse2, nlse2);
 #pragma unroll
-                for (int i = 0; i < kC; ++i)
-                    pv[i] = ex2_approx(fmaf(__uint_as_float(r[i]), p.scale_log2, -lse2));
+                for (int i = 0; i < kC; i += 2) {  // two columns per f32x2 instruction
+                    float y0, y1;
+                    f2_split(f2_fma(f2_make(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                    scale2, shift2),
+                             y0, y1);
+                    pv[i] = ex2_approx(y0);
+                    pv[i + 1] = ex2_approx(y1);
+                }
                 if (masked) {
 #pragma unroll
                     for (int i = 0; i < kC; ++i)
@@ -272,7 +281,14 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
                     uint32_t r[kLd];
                     tmem_ld<kLd>(tmem + lane_off + C::kTmDP + c0 + h * kLd, r);
 #pragma unroll
-                    for (int i = 0; i < kLd; ++i) pv[h * kLd + i] *= __uint_as_float(r[i]) - dlt;
+                    for (int i = 0; i < kLd; i += 2) {  // P o (dP - Delta), two per instruction
+                        float* q = pv + h * kLd + i;
+                        f2_split(f2_mul(f2_make(q[0], q[1]),
+                                        f2_sub(f2_make(__uint_as_float(r[i]),
+                                                       __uint_as_float(r[i + 1])),
+                                               dlt2)),
+                                 q[0], q[1]);
+                    }
                 }
             }
             // Every slice of the quadrant has read its dP columns before dS overwrites them.

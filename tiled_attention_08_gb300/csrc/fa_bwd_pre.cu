@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdPreParams p) {
         for (int w = G / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w, G);
         if (g == 0 && row < total) {
             p.delta_pad[row] = acc;
-            p.lse2_pad[row] = (i < p.L) ? p.lse[(size_t)bh * p.L + i] * kLog2e : 0.0f;
+            p.nlse2_pad[row] = (i < p.L) ? -(p.lse[(size_t)bh * p.L + i] * kLog2e) : 0.0f;
         }
     }
 }

@@ -51,7 +51,7 @@ struct BwdPreParams {
     const void* o;       // [BH, L, D]
     const void* dout;    // [BH, L, D]
     const float* lse;    // [BH, L]
-    float* lse2_pad;     // [BH, Lpad]: LSE * log2(e), zero past L
+    float* nlse2_pad;    // [BH, Lpad]: -LSE * log2(e), zero past L
     float* delta_pad;    // [BH, Lpad]: rowsum(dO * O), zero past L
     int L, Lpad, BH, D;
     int bf16;
@@ -61,7 +61,7 @@ struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // [BH, L, D] 16-bit, box {64, 128, 1}
     const void* q;                        // [BH, L, D] (rows staged into TMEM by the dQ pass)
     const void* dout;                     // [BH, L, D]
-    const float* lse2_pad;                // [BH, Lpad]
+    const float* nlse2_pad;               // [BH, Lpad]: -LSE * log2(e)
     const float* delta_pad;               // [BH, Lpad]
     void* dq;                             // [BH, L, D]
     void* dk;
