@@ -14,15 +14,16 @@
 // arrive.  The two tiles also give the tensor core independent work to interleave: while the
 // softmax of tile A runs, the MMA warp computes tile B's PV and S, and the other way round.
 //
-// CTA roles (kSplit = 1: 352 threads):
+// CTA roles (kSplit = 1: 352 threads at D = 128, 320 at D = 64):
 //   softmax warps, one group of 4*kSplit per query tile (tile A first).  In a group, warp w
 //                owns TMEM lanes 32*(w%4).. (query rows) and key columns
 //                [kCols*(w/4), +kCols) of the tile's S (kCols = 128/kSplit); with kSplit > 1
 //                the warps of a lane quadrant combine partial row maxima through shared memory
 //                at a named barrier, with kSplit = 1 every thread owns a whole row;
-//   next warp    TMA producer of Q_A, Q_B (once) and the K_j ring;
-//   next warp    MMA issuer (one thread) and TMEM owner;
-//   last warp    TMA producer of the V_j ring.
+//   next warp    TMA producer of Q_A, Q_B (once) and the K_j ring (at D = 64 K_j and V_j
+//                together in one slot);
+//   next warp    MMA issuer (one elected thread) and TMEM owner;
+//   last warp    TMA producer of the V_j ring (D = 128 only).
 // TMEM columns: S_A [0,128), S_B [128,256) (fp32; the 16-bit P of a tile overwrites the first
 // 64 columns of its S and feeds the PV MMA straight from TMEM), O_A [256, 256+D),
 // O_B [256+D, 256+2D).  MMA order: S_A0, S_B0, then for each key tile j: PV_Aj, S_A(j+1),
@@ -47,8 +48,12 @@ template <int D, bool BF16, bool CAUSAL>
 struct FwdCfg {
     static constexpr int kChunks = D / kChunkElems;            // swizzle boxes per tile row
     static constexpr int kTileBytes = kTileRows * D * 2;       // one 128 x D tile
-    static constexpr int kKStages = (D == 128) ? 2 : 4;        // K ring depth
-    static constexpr int kVStages = (D == 128) ? 2 : 4;        // V ring depth
+    // D = 64: K_j and V_j share one slot of the K ring (one full and one empty barrier per
+    // slot, one producer warp).  D = 128: separate K and V rings of two slots each, so that
+    // K_{j+1} can land while V_j is still being read (measured faster at that size).
+    static constexpr bool kMergedKV = (D == 64);
+    static constexpr int kKStages = (D == 128) ? 2 : 4;        // K (or K/V) ring depth
+    static constexpr int kVStages = (D == 128) ? 2 : 4;        // V ring depth (separate rings)
     static constexpr int kOffQ = 0;                            // Q_A, then Q_B
     static constexpr int kOffK = kOffQ + 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kKStages * kTileBytes;
@@ -60,7 +65,7 @@ struct FwdCfg {
     static constexpr int kProducerWarp = kSoftmaxWarps;
     static constexpr int kMmaWarp = kSoftmaxWarps + 1;
     static constexpr int kVProducerWarp = kSoftmaxWarps + 2;
-    static constexpr int kThreads = (kSoftmaxWarps + 3) * 32;
+    static constexpr int kThreads = (kSoftmaxWarps + (kMergedKV ? 2 : 3)) * 32;
     static constexpr int kCols = 128 / kSplit;                 // S columns per softmax warp
     static constexpr int kOCols = D / kSplit;                  // O columns per softmax warp
     static constexpr uint32_t kTmemCols = 512;
@@ -125,127 +130,245 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = tmem_base_sh;
 
-    if (warp == C::kProducerWarp || warp == C::kVProducerWarp) {
-        // ------------------------------ TMA producers ------------------------------
-        // One ring per warp: Q + K on kProducerWarp, V on kVProducerWarp.
-        if (lane == 0) {
-            const bool is_k = warp == C::kProducerWarp;
-            const CUtensorMap* map = is_k ? &p.tm_k : &p.tm_v;
-            const int stages = is_k ? C::kKStages : C::kVStages;
-            uint64_t* full = is_k ? bar_kf : bar_vf;
-            uint64_t* empty = is_k ? bar_ke : bar_ve;
-            uint8_t* ring = smem + (is_k ? C::kOffK : C::kOffV);
-            tma_prefetch_desc(map);
-            if (is_k) {
+    if (warp == C::kProducerWarp || (!C::kMergedKV && warp == C::kVProducerWarp)) {
+        if constexpr (C::kMergedKV) {
+            // ------------------------------ TMA producer ------------------------------
+            // Q_A, Q_B once, then K_j and V_j together into ring slot j % kKStages.
+            if (lane == 0) {
                 tma_prefetch_desc(&p.tm_q);
+                tma_prefetch_desc(&p.tm_k);
+                tma_prefetch_desc(&p.tm_v);
                 mbar_arrive_expect_tx(&bar_q, (has_b ? 2 : 1) * C::kTileBytes);
                 for (int t = 0; t < (has_b ? 2 : 1); ++t)
                     for (int c = 0; c < C::kChunks; ++c)
                         tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + c * kChunkBytes, &p.tm_q,
                                     &bar_q, c * kChunkElems, (t ? q_b : q_a) * kTileRows, bh);
-            }
-            bool ok = true;
-            int issued = 0;  // fills handed to the TMA unit
-            for (int j = 0; j < n_kv; ++j) {
-                const int st = j % stages;
-                const uint32_t ph = (uint32_t)(j / stages) & 1u;
-                if (j >= stages && !wait_bounded(&empty[st], ph ^ 1u, abort_v, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&full[st], C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(ring + st * C::kTileBytes + c * kChunkBytes, map, &full[st],
-                                c * kChunkElems, j * kTileRows, bh);
-                issued = j + 1;
-            }
-            if (!ok) record_timeout(p.status, abort_v);
-            // Drain: the newest fill of every stage must have landed before the CTA exits.
-            // (These waits return at once on the normal path.)
-            if (is_k) wait_bounded(&bar_q, 0, nullptr, p.timeout_ns);
-            for (int j = issued - 1; j >= 0 && j >= issued - stages; --j)
-                wait_bounded(&full[j % stages], (uint32_t)(j / stages) & 1u, nullptr, p.timeout_ns);
-        }
-    } else if (warp == C::kMmaWarp) {
-        // ------------------------------ MMA issuer ------------------------------
-        // The whole warp walks the loop (warp-uniform values); one elected lane issues.
-        bool ok = wait_warp(&bar_q, 0, abort_v, p.timeout_ns);
-        int k_ready = -1;  // newest K tile known to have landed
-        auto wait_k = [&](int j) -> bool {
-            if (k_ready >= j) return true;
-            const int st = j % C::kKStages;
-            if (!wait_warp(&bar_kf[st], (uint32_t)(j / C::kKStages) & 1u, abort_v,
-                              p.timeout_ns))
-                return false;
-            tc_fence_after_sync();
-            k_ready = j;
-            return true;
-        };
-        auto issue_s = [&](int t, int j) {
-            const uint64_t qd = sdesc_kmajor_sw128(smem_u32(smem + C::kOffQ + t * C::kTileBytes));
-            const uint64_t kd =
-                sdesc_kmajor_sw128(smem_u32(smem + C::kOffK + (j % C::kKStages) * C::kTileBytes));
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                mma_ss_w(tmem + C::kTmS + 128 * t, sdesc_advance(qd, off), sdesc_advance(kd, off),
-                       C::kIdescS, kk > 0 ? 1u : 0u);
-            }
-            mma_commit_w(&bar_sf[t]);
-        };
-        auto issue_pv = [&](int t, int j) -> bool {
-            const int st = j % C::kVStages;
-            if (!wait_warp(&bar_pf[t], (uint32_t)j & 1u, abort_v, p.timeout_ns))
-                return false;
-            if (!wait_warp(&bar_vf[st], (uint32_t)(j / C::kVStages) & 1u, abort_v,
-                              p.timeout_ns))
-                return false;
-            tc_fence_after_sync();
-            const uint64_t vd =
-                sdesc_mnmajor_sw128(smem_u32(smem + C::kOffV + st * C::kTileBytes), kChunkBytes);
-#pragma unroll
-            for (int kk = 0; kk < kTileRows / 16; ++kk) {
-                const uint64_t bd = sdesc_advance(vd, kk * 2048);
-                mma_ts_w(tmem + C::kTmO + D * t, tmem + C::kTmS + 128 * t + kk * 8, bd,
-                       C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
-            }
-            if (j + 1 == (t ? n_kv_b : n_kv_a)) mma_commit_w(&bar_oready[t]);  // O_t is final
-            return true;
-        };
-        if (ok && n_kv > 0) {
-            ok = wait_k(0);
-            if (ok) {
-                issue_s(0, 0);
-                if (n_kv_b > 0) issue_s(1, 0);
-                mma_commit_w(&bar_ke[0]);
-            }
-        }
-        for (int j = 0; ok && j < n_kv; ++j) {
-            const bool next = j + 1 < n_kv;
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const int n_t = t ? n_kv_b : n_kv_a;
-                if (!ok) break;
-                if (j < n_t && !issue_pv(t, j)) {
-                    ok = false;
-                    break;
-                }
-                if (next && j + 1 < n_t) {
-                    if (!wait_k(j + 1)) {
+                bool ok = true;
+                int issued = 0;  // fills handed to the TMA unit
+                for (int j = 0; j < n_kv; ++j) {
+                    const int st = j % C::kKStages;
+                    const uint32_t ph = (uint32_t)(j / C::kKStages) & 1u;
+                    if (j >= C::kKStages && !wait_bounded(&bar_ke[st], ph ^ 1u, abort_v, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
-                    issue_s(t, j + 1);
+                    mbar_arrive_expect_tx(&bar_kf[st], 2 * C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        tma_load_3d(smem + C::kOffK + st * C::kTileBytes + c * kChunkBytes, &p.tm_k,
+                                    &bar_kf[st], c * kChunkElems, j * kTileRows, bh);
+                        tma_load_3d(smem + C::kOffV + st * C::kTileBytes + c * kChunkBytes, &p.tm_v,
+                                    &bar_kf[st], c * kChunkElems, j * kTileRows, bh);
+                    }
+                    issued = j + 1;
+                }
+                if (!ok) record_timeout(p.status, abort_v);
+                // Drain: the newest fill of every slot must have landed before the CTA exits.
+                // (These waits return at once on the normal path.)
+                wait_bounded(&bar_q, 0, nullptr, p.timeout_ns);
+                for (int j = issued - 1; j >= 0 && j >= issued - C::kKStages; --j)
+                    wait_bounded(&bar_kf[j % C::kKStages], (uint32_t)(j / C::kKStages) & 1u, nullptr,
+                                 p.timeout_ns);
+            }
+        } else {
+            // ------------------------------ TMA producers ------------------------------
+            // One ring per warp: Q + K on kProducerWarp, V on kVProducerWarp.
+            if (lane == 0) {
+                const bool is_k = warp == C::kProducerWarp;
+                const CUtensorMap* map = is_k ? &p.tm_k : &p.tm_v;
+                const int stages = is_k ? C::kKStages : C::kVStages;
+                uint64_t* full = is_k ? bar_kf : bar_vf;
+                uint64_t* empty = is_k ? bar_ke : bar_ve;
+                uint8_t* ring = smem + (is_k ? C::kOffK : C::kOffV);
+                tma_prefetch_desc(map);
+                if (is_k) {
+                    tma_prefetch_desc(&p.tm_q);
+                    mbar_arrive_expect_tx(&bar_q, (has_b ? 2 : 1) * C::kTileBytes);
+                    for (int t = 0; t < (has_b ? 2 : 1); ++t)
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + c * kChunkBytes, &p.tm_q,
+                                        &bar_q, c * kChunkElems, (t ? q_b : q_a) * kTileRows, bh);
+                }
+                bool ok = true;
+                int issued = 0;  // fills handed to the TMA unit
+                for (int j = 0; j < n_kv; ++j) {
+                    const int st = j % stages;
+                    const uint32_t ph = (uint32_t)(j / stages) & 1u;
+                    if (j >= stages && !wait_bounded(&empty[st], ph ^ 1u, abort_v, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[st], C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(ring + st * C::kTileBytes + c * kChunkBytes, map, &full[st],
+                                    c * kChunkElems, j * kTileRows, bh);
+                    issued = j + 1;
+                }
+                if (!ok) record_timeout(p.status, abort_v);
+                // Drain: the newest fill of every stage must have landed before the CTA exits.
+                // (These waits return at once on the normal path.)
+                if (is_k) wait_bounded(&bar_q, 0, nullptr, p.timeout_ns);
+                for (int j = issued - 1; j >= 0 && j >= issued - stages; --j)
+                    wait_bounded(&full[j % stages], (uint32_t)(j / stages) & 1u, nullptr, p.timeout_ns);
+            }
+        }
+    } else if (warp == C::kMmaWarp) {
+        if constexpr (C::kMergedKV) {
+
+            // ------------------------------ MMA issuer ------------------------------
+            // The whole warp walks the loop (warp-uniform values); one elected lane issues.  Each
+            // wait between MMA groups can let the tensor pipe's short queue run dry, so there are
+            // three per key tile: P of tile A, the next K/V slot, P of tile B.
+            bool ok = wait_warp(&bar_q, 0, abort_v, p.timeout_ns);
+            auto wait_kv = [&](int j) -> bool {  // K_j and V_j landed
+                if (!wait_warp(&bar_kf[j % C::kKStages], (uint32_t)(j / C::kKStages) & 1u, abort_v,
+                               p.timeout_ns))
+                    return false;
+                tc_fence_after_sync();
+                return true;
+            };
+            auto issue_s = [&](int t, int j) {
+                const uint64_t qd = sdesc_kmajor_sw128(smem_u32(smem + C::kOffQ + t * C::kTileBytes));
+                const uint64_t kd =
+                    sdesc_kmajor_sw128(smem_u32(smem + C::kOffK + (j % C::kKStages) * C::kTileBytes));
+    #pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                    mma_ss_w(tmem + C::kTmS + 128 * t, sdesc_advance(qd, off), sdesc_advance(kd, off),
+                           C::kIdescS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit_w(&bar_sf[t]);
+            };
+            auto issue_pv = [&](int t, int j) -> bool {
+                if (!wait_warp(&bar_pf[t], (uint32_t)j & 1u, abort_v, p.timeout_ns))
+                    return false;
+                tc_fence_after_sync();
+                const uint64_t vd = sdesc_mnmajor_sw128(
+                    smem_u32(smem + C::kOffV + (j % C::kKStages) * C::kTileBytes), kChunkBytes);
+    #pragma unroll
+                for (int kk = 0; kk < kTileRows / 16; ++kk) {
+                    const uint64_t bd = sdesc_advance(vd, kk * 2048);
+                    mma_ts_w(tmem + C::kTmO + D * t, tmem + C::kTmS + 128 * t + kk * 8, bd,
+                           C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                if (j + 1 == (t ? n_kv_b : n_kv_a)) mma_commit_w(&bar_oready[t]);  // O_t is final
+                return true;
+            };
+            if (ok && n_kv > 0) {
+                ok = wait_kv(0);
+                if (ok) {
+                    issue_s(0, 0);
+                    if (n_kv_b > 0) issue_s(1, 0);
                 }
             }
-            if (!ok) break;
-            mma_commit_w(&bar_ve[j % C::kVStages]);                // V_j read by both PVs
-            if (next) mma_commit_w(&bar_ke[(j + 1) % C::kKStages]);  // K_{j+1} read by both S
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const bool next = j + 1 < n_kv;
+    #pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int n_t = t ? n_kv_b : n_kv_a;
+                    if (!ok) break;
+                    if (j < n_t && !issue_pv(t, j)) {
+                        ok = false;
+                        break;
+                    }
+                    if (next && j + 1 < n_t) {
+                        if (t == 0 || j + 1 >= n_kv_a) {  // slot j+1 not yet waited for
+                            if (!wait_kv(j + 1)) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        issue_s(t, j + 1);
+                    }
+                }
+                if (!ok) break;
+                mma_commit_w(&bar_ke[j % C::kKStages]);  // K_j (S_j) and V_j (both PV_j) consumed
+            }
+            if (!ok && lane == 0) record_timeout(p.status, abort_v);
+            // Every issued MMA must finish before TMEM is released.
+            mma_commit_w(&bar_fin);
+            wait_warp(&bar_fin, 0, nullptr, p.timeout_ns);
+        } else {
+
+            // ------------------------------ MMA issuer ------------------------------
+            // The whole warp walks the loop (warp-uniform values); one elected lane issues.
+            bool ok = wait_warp(&bar_q, 0, abort_v, p.timeout_ns);
+            int k_ready = -1;  // newest K tile known to have landed
+            auto wait_k = [&](int j) -> bool {
+                if (k_ready >= j) return true;
+                const int st = j % C::kKStages;
+                if (!wait_warp(&bar_kf[st], (uint32_t)(j / C::kKStages) & 1u, abort_v,
+                                  p.timeout_ns))
+                    return false;
+                tc_fence_after_sync();
+                k_ready = j;
+                return true;
+            };
+            auto issue_s = [&](int t, int j) {
+                const uint64_t qd = sdesc_kmajor_sw128(smem_u32(smem + C::kOffQ + t * C::kTileBytes));
+                const uint64_t kd =
+                    sdesc_kmajor_sw128(smem_u32(smem + C::kOffK + (j % C::kKStages) * C::kTileBytes));
+    #pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                    mma_ss_w(tmem + C::kTmS + 128 * t, sdesc_advance(qd, off), sdesc_advance(kd, off),
+                           C::kIdescS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit_w(&bar_sf[t]);
+            };
+            auto issue_pv = [&](int t, int j) -> bool {
+                const int st = j % C::kVStages;
+                if (!wait_warp(&bar_pf[t], (uint32_t)j & 1u, abort_v, p.timeout_ns))
+                    return false;
+                if (!wait_warp(&bar_vf[st], (uint32_t)(j / C::kVStages) & 1u, abort_v,
+                                  p.timeout_ns))
+                    return false;
+                tc_fence_after_sync();
+                const uint64_t vd =
+                    sdesc_mnmajor_sw128(smem_u32(smem + C::kOffV + st * C::kTileBytes), kChunkBytes);
+    #pragma unroll
+                for (int kk = 0; kk < kTileRows / 16; ++kk) {
+                    const uint64_t bd = sdesc_advance(vd, kk * 2048);
+                    mma_ts_w(tmem + C::kTmO + D * t, tmem + C::kTmS + 128 * t + kk * 8, bd,
+                           C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                if (j + 1 == (t ? n_kv_b : n_kv_a)) mma_commit_w(&bar_oready[t]);  // O_t is final
+                return true;
+            };
+            if (ok && n_kv > 0) {
+                ok = wait_k(0);
+                if (ok) {
+                    issue_s(0, 0);
+                    if (n_kv_b > 0) issue_s(1, 0);
+                    mma_commit_w(&bar_ke[0]);
+                }
+            }
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const bool next = j + 1 < n_kv;
+    #pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int n_t = t ? n_kv_b : n_kv_a;
+                    if (!ok) break;
+                    if (j < n_t && !issue_pv(t, j)) {
+                        ok = false;
+                        break;
+                    }
+                    if (next && j + 1 < n_t) {
+                        if (!wait_k(j + 1)) {
+                            ok = false;
+                            break;
+                        }
+                        issue_s(t, j + 1);
+                    }
+                }
+                if (!ok) break;
+                mma_commit_w(&bar_ve[j % C::kVStages]);                // V_j read by both PVs
+                if (next) mma_commit_w(&bar_ke[(j + 1) % C::kKStages]);  // K_{j+1} read by both S
+            }
+            if (!ok && lane == 0) record_timeout(p.status, abort_v);
+            // Every issued MMA must finish before TMEM is released.
+            mma_commit_w(&bar_fin);
+            wait_warp(&bar_fin, 0, nullptr, p.timeout_ns);
         }
-        if (!ok && lane == 0) record_timeout(p.status, abort_v);
-        // Every issued MMA must finish before TMEM is released.
-        mma_commit_w(&bar_fin);
-        wait_warp(&bar_fin, 0, nullptr, p.timeout_ns);
     } else {
         // ------------------------------ softmax warps ------------------------------
         constexpr int kC = C::kCols;
