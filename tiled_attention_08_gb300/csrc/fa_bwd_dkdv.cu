@@ -32,14 +32,20 @@ template <int D, bool BF16, bool CAUSAL>
 struct DkdvCfg {
     static constexpr int kChunks = D / kChunkElems;
     static constexpr int kTileBytes = kTileRows * D * 2;
-    static constexpr int kStages = (D == 128) ? 2 : 3;
-    static constexpr int kVecBytes = 2 * kTileRows * 4;  // LSE*log2e then Delta, fp32
+    // Q_i is needed early (by S^T) and late (by dK), dO_i only in between, so the Q ring is one
+    // slot deeper than the dO ring.  At D = 128 the tiles then fill 224 KB of the 227 KB a block
+    // may have, so everything else (the -LSE*log2e and Delta vectors, the barriers) lives in
+    // the same 1024-aligned dynamic allocation and no alignment slack is requested.
+    static constexpr int kQStages = (D == 128) ? 3 : 4;
+    static constexpr int kOStages = (D == 128) ? 2 : 3;
+    static constexpr int kVecBytes = kTileRows * 4;  // one fp32 vector of a 128-row tile
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kTileBytes;
     static constexpr int kOffQ = 2 * kTileBytes;
-    static constexpr int kOffDO = kOffQ + kStages * kTileBytes;
-    static constexpr int kOffVec = kOffDO + kStages * kTileBytes;
-    static constexpr int kSmemBytes = kOffVec + kStages * kVecBytes + 1024;
+    static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;
+    static constexpr int kOffNlse = kOffDO + kOStages * kTileBytes;  // per Q slot
+    static constexpr int kOffDelta = kOffNlse + kQStages * kVecBytes;  // per dO slot
+    static constexpr int kOffBar = kOffDelta + kOStages * kVecBytes;
     static constexpr int kSplit = 4;  // elementwise warps per TMEM lane quadrant
     static constexpr int kEwWarps = 4 * kSplit;
     static constexpr int kEwThreads = kEwWarps * 32;
@@ -54,19 +60,49 @@ struct DkdvCfg {
     static constexpr uint32_t kIdescG = idesc_f16(BF16, 128, D, false, true);
 };
 
+// Barriers and small shared state, placed after the tiles in dynamic shared memory.
+template <int QS, int OS>
+struct DkdvBars {
+    uint64_t kv, qf[QS], qe[QS], of[OS], oe[OS], sf, df, sr, ppd, done, fin;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int D, bool BF16, bool CAUSAL>
+constexpr int dkdv_smem_bytes() {
+    using C = DkdvCfg<D, BF16, CAUSAL>;
+    return C::kOffBar + (int)sizeof(DkdvBars<C::kQStages, C::kOStages>);
+}
+
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = DkdvCfg<D, BF16, CAUSAL>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
-    // Q_i (+ LSE_i) and dO_i (+ Delta_i) have their own full/empty barriers: Q_i is released
-    // by dK_i, issued first, so the load of a later Q tile (needed early, by S^T) starts sooner.
-    __shared__ uint64_t bar_kv, bar_qf[C::kStages], bar_qe[C::kStages], bar_of[C::kStages],
-        bar_oe[C::kStages], bar_sf, bar_df, bar_sr, bar_ppd, bar_done, bar_fin;
-    __shared__ uint32_t tmem_base_sh;
-    __shared__ int abort_flag;
+    // The kernel declares no static shared memory, so its dynamic shared memory starts at the
+    // block's shared window, which is 1024-byte aligned; checked here (the 128-byte swizzle
+    // needs it) before any barrier, TMEM or copy is touched.
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if ((smem_u32(smem) & 1023u) != 0u) {
+        if (threadIdx.x == 0) atomicCAS(p.status, 0, 3);  // reported as FA_ERR_CUDA
+        return;
+    }
+    // Q_i (+ LSE_i) and dO_i (+ Delta_i) have their own rings and full/empty barriers: Q_i is
+    // released by dK_i, issued first, so the load of a later Q tile (needed early, by S^T)
+    // starts sooner.
+    auto& bars = *reinterpret_cast<DkdvBars<C::kQStages, C::kOStages>*>(smem + C::kOffBar);
+    uint64_t& bar_kv = bars.kv;
+    uint64_t* bar_qf = bars.qf;
+    uint64_t* bar_qe = bars.qe;
+    uint64_t* bar_of = bars.of;
+    uint64_t* bar_oe = bars.oe;
+    uint64_t& bar_sf = bars.sf;
+    uint64_t& bar_df = bars.df;
+    uint64_t& bar_sr = bars.sr;
+    uint64_t& bar_ppd = bars.ppd;
+    uint64_t& bar_done = bars.done;
+    uint64_t& bar_fin = bars.fin;
+    uint32_t& tmem_base_sh = bars.tmem_base;
+    int& abort_flag = bars.abort;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -81,9 +117,11 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(&bar_kv, 1);
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < C::kQStages; ++s) {
             mbar_init(&bar_qf[s], 1);
             mbar_init(&bar_qe[s], 1);
+        }
+        for (int s = 0; s < C::kOStages; ++s) {
             mbar_init(&bar_of[s], 1);
             mbar_init(&bar_oe[s], 1);
         }
@@ -117,41 +155,54 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
             }
             bool ok = true;
             int issued_q = 0, issued_o = 0;
-            for (int t = 0; t < n_it; ++t) {
+            auto load_q = [&](int t) -> bool {  // Q_t and -LSE_t*log2e into Q slot t % kQStages
+                const int st = t % C::kQStages;
+                if (t >= C::kQStages &&
+                    !wait_bounded(&bar_qe[st], ((uint32_t)(t / C::kQStages) & 1u) ^ 1u, abort_v,
+                                  p.timeout_ns))
+                    return false;
                 const int it = it0 + t;
-                const int st = t % C::kStages;
-                const uint32_t ph = (uint32_t)(t / C::kStages) & 1u;
-                const size_t voff = (size_t)bh * p.Lpad + (size_t)it * kTileRows;
-                uint8_t* vec = smem + C::kOffVec + st * C::kVecBytes;
-                if (t >= C::kStages && !wait_bounded(&bar_qe[st], ph ^ 1u, abort_v, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&bar_qf[st], C::kTileBytes + kTileRows * 4);
+                mbar_arrive_expect_tx(&bar_qf[st], C::kTileBytes + C::kVecBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(smem + C::kOffQ + st * C::kTileBytes + c * kChunkBytes, &p.tm_q,
                                 &bar_qf[st], c * kChunkElems, it * kTileRows, bh);
-                bulk_load(vec, p.nlse2_pad + voff, kTileRows * 4, &bar_qf[st]);
+                bulk_load(smem + C::kOffNlse + st * C::kVecBytes,
+                          p.nlse2_pad + (size_t)bh * p.Lpad + (size_t)it * kTileRows, C::kVecBytes,
+                          &bar_qf[st]);
                 issued_q = t + 1;
-                if (t >= C::kStages && !wait_bounded(&bar_oe[st], ph ^ 1u, abort_v, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&bar_of[st], C::kTileBytes + kTileRows * 4);
+                return true;
+            };
+            auto load_do = [&](int t) -> bool {  // dO_t and Delta_t into dO slot t % kOStages
+                const int st = t % C::kOStages;
+                if (t >= C::kOStages &&
+                    !wait_bounded(&bar_oe[st], ((uint32_t)(t / C::kOStages) & 1u) ^ 1u, abort_v,
+                                  p.timeout_ns))
+                    return false;
+                const int it = it0 + t;
+                mbar_arrive_expect_tx(&bar_of[st], C::kTileBytes + C::kVecBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(smem + C::kOffDO + st * C::kTileBytes + c * kChunkBytes, &p.tm_do,
                                 &bar_of[st], c * kChunkElems, it * kTileRows, bh);
-                bulk_load(vec + kTileRows * 4, p.delta_pad + voff, kTileRows * 4, &bar_of[st]);
+                bulk_load(smem + C::kOffDelta + st * C::kVecBytes,
+                          p.delta_pad + (size_t)bh * p.Lpad + (size_t)it * kTileRows, C::kVecBytes,
+                          &bar_of[st]);
                 issued_o = t + 1;
+                return true;
+            };
+            // Q runs one tile ahead of dO: Q_{t+1} only waits for dK_{t+1-kQStages}.
+            if (n_it > 0) ok = load_q(0);
+            for (int t = 0; ok && t < n_it; ++t) {
+                if (t + 1 < n_it) ok = load_q(t + 1);
+                ok = ok && load_do(t);
             }
             if (!ok) record_timeout(p.status, abort_v);
             // Drain: no copy may still be landing when the CTA exits.
             wait_bounded(&bar_kv, 0, nullptr, p.timeout_ns);
-            for (int t = issued_q - 1; t >= 0 && t >= issued_q - C::kStages; --t)
-                wait_bounded(&bar_qf[t % C::kStages], (uint32_t)(t / C::kStages) & 1u, nullptr,
+            for (int t = issued_q - 1; t >= 0 && t >= issued_q - C::kQStages; --t)
+                wait_bounded(&bar_qf[t % C::kQStages], (uint32_t)(t / C::kQStages) & 1u, nullptr,
                              p.timeout_ns);
-            for (int t = issued_o - 1; t >= 0 && t >= issued_o - C::kStages; --t)
-                wait_bounded(&bar_of[t % C::kStages], (uint32_t)(t / C::kStages) & 1u, nullptr,
+            for (int t = issued_o - 1; t >= 0 && t >= issued_o - C::kOStages; --t)
+                wait_bounded(&bar_of[t % C::kOStages], (uint32_t)(t / C::kOStages) & 1u, nullptr,
                              p.timeout_ns);
         }
     } else if (warp == C::kMmaWarp) {
@@ -160,19 +211,19 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
         const uint32_t k_base = smem_u32(smem + C::kOffK);
         const uint32_t v_base = smem_u32(smem + C::kOffV);
         auto q_base = [&](int t) {
-            return smem_u32(smem + C::kOffQ + (t % C::kStages) * C::kTileBytes);
+            return smem_u32(smem + C::kOffQ + (t % C::kQStages) * C::kTileBytes);
         };
         auto do_base = [&](int t) {
-            return smem_u32(smem + C::kOffDO + (t % C::kStages) * C::kTileBytes);
+            return smem_u32(smem + C::kOffDO + (t % C::kOStages) * C::kTileBytes);
         };
         auto wait_q = [&](int t) {  // Q_t landed
-            const bool r = wait_warp(&bar_qf[t % C::kStages], (uint32_t)(t / C::kStages) & 1u,
+            const bool r = wait_warp(&bar_qf[t % C::kQStages], (uint32_t)(t / C::kQStages) & 1u,
                                      abort_v, p.timeout_ns);
             tc_fence_after_sync();
             return r;
         };
         auto wait_do = [&](int t) {  // dO_t landed
-            const bool r = wait_warp(&bar_of[t % C::kStages], (uint32_t)(t / C::kStages) & 1u,
+            const bool r = wait_warp(&bar_of[t % C::kOStages], (uint32_t)(t / C::kOStages) & 1u,
                                      abort_v, p.timeout_ns);
             tc_fence_after_sync();
             return r;
@@ -228,12 +279,12 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
             for (int kk = 0; kk < kTileRows / 16; ++kk)
                 mma_ts_w(tmem + C::kTmDK, tmem + C::kTmDPT + 64 + kk * 8,
                        sdesc_advance(qmd, kk * 2048), C::kIdescG, (acc0 || kk > 0) ? 1u : 0u);
-            mma_commit_w(&bar_qe[t % C::kStages]);  // Q_t fully read
+            mma_commit_w(&bar_qe[t % C::kQStages]);  // Q_t fully read
 #pragma unroll
             for (int kk = 0; kk < kTileRows / 16; ++kk)
                 mma_ts_w(tmem + C::kTmDV, tmem + C::kTmDPT + kk * 8,
                        sdesc_advance(dod, kk * 2048), C::kIdescG, (acc0 || kk > 0) ? 1u : 0u);
-            mma_commit_w(&bar_oe[t % C::kStages]);  // dO_t fully read
+            mma_commit_w(&bar_oe[t % C::kOStages]);  // dO_t fully read
             if (t + 1 < n_it) {                     // after dV_t, dK_t read the dP^T columns
                 if (!wait_do(t + 1)) {
                     ok = false;
@@ -260,17 +311,18 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
         bool ok = true;
         for (int t = 0; t < n_it; ++t) {
             const int it = it0 + t;
-            const int st = t % C::kStages;
-            const uint32_t ph = (uint32_t)(t / C::kStages) & 1u;
+            const int qs = t % C::kQStages, os = t % C::kOStages;  // ring slots of Q_t, dO_t
+            const uint32_t qph = (uint32_t)(t / C::kQStages) & 1u;
+            const uint32_t oph = (uint32_t)(t / C::kOStages) & 1u;
             // -LSE*log2e and Delta of this warp's query columns (broadcast shared reads).
-            const uint32_t nlse2_addr = smem_u32(smem + C::kOffVec + st * C::kVecBytes) + c0 * 4;
-            const uint32_t dlt_addr = nlse2_addr + kTileRows * 4;
+            const uint32_t nlse2_addr = smem_u32(smem + C::kOffNlse + qs * C::kVecBytes) + c0 * 4;
+            const uint32_t dlt_addr = smem_u32(smem + C::kOffDelta + os * C::kVecBytes) + c0 * 4;
             const int q0 = it * kTileRows + c0;
             const bool masked = (CAUSAL && it == kt) || (it * kTileRows + kTileRows > p.L);
             const int qlim = p.L - 1;  // last valid query
             // Phase 1: P^T = exp2(S^T * scale*log2e - LSE*log2e) on this warp's columns; kept
             // in registers, and the S^T columns are released at once.
-            ok = wait_bounded(&bar_qf[st], ph, abort_v, p.timeout_ns) &&
+            ok = wait_bounded(&bar_qf[qs], qph, abort_v, p.timeout_ns) &&
                  wait_bounded(&bar_sf, (uint32_t)t & 1u, abort_v, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
             float pv[kC];
@@ -307,7 +359,7 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < kC / 2; ++i) pk_p[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
                 // Phase 2: dS^T = P^T o (dP^T - Delta).
-                ok = wait_bounded(&bar_of[st], ph, abort_v, p.timeout_ns) &&
+                ok = wait_bounded(&bar_of[os], oph, abort_v, p.timeout_ns) &&
                      wait_bounded(&bar_df, (uint32_t)t & 1u, abort_v, p.timeout_ns);
                 ok = __all_sync(0xffffffffu, ok);
             }
@@ -381,10 +433,11 @@ template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_t(const BwdParams& p, cudaStream_t s) {
     using C = DkdvCfg<D, BF16, CAUSAL>;
     auto kern = fa_bwd_dkdv_kernel<D, BF16, CAUSAL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+    constexpr int kSmem = dkdv_smem_bytes<D, BF16, CAUSAL>();
+    static_assert(kSmem <= 232448, "dynamic shared memory over the 227 KB per-block limit");
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)p.n_tiles * (unsigned)p.BH, C::kThreads, C::kSmemBytes, s>>>(p);
+    kern<<<(unsigned)p.n_tiles * (unsigned)p.BH, C::kThreads, kSmem, s>>>(p);
     return cudaGetLastError();
 }
 
