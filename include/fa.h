@@ -108,7 +108,8 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
 /*
  * Synchronises `stream`, then reads and clears the current device's status word.  Returns
  * FA_OK, FA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last call, or
- * FA_ERR_CUDA if synchronisation itself failed.
+ * FA_ERR_CUDA if synchronisation itself failed or a kernel refused to run (its dynamic shared
+ * memory was not 1024-byte aligned; it then wrote nothing).
  */
 fa_status fa_get_device_status(void* stream);
 

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
     // needs it) before any barrier, TMEM or copy is touched.
     extern __shared__ __align__(1024) uint8_t smem[];
     if ((smem_u32(smem) & 1023u) != 0u) {
-        if (threadIdx.x == 0) atomicCAS(p.status, 0, 3);  // reported as FA_ERR_CUDA
+        if (threadIdx.x == 0) atomicCAS(p.status, 0, (int)kDevBadShared);  // -> FA_ERR_CUDA
         return;
     }
     // Q_i (+ LSE_i) and dO_i (+ Delta_i) have their own rings and full/empty barriers: Q_i is

@@ -10,7 +10,8 @@ namespace fa {
 // Status codes a kernel records in the device status word (first error wins).
 enum DeviceError : int {
     kDevOk = 0,
-    kDevTimeout = 4,  // a bounded wait ran out
+    kDevBadShared = 3,  // dynamic shared memory not 1024-byte aligned (kernel did nothing)
+    kDevTimeout = 4,    // a bounded wait ran out
 };
 
 // Tile geometry shared by every kernel: 128 query rows x 128 keys per tile; operands are
