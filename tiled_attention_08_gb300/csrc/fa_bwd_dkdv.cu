@@ -267,7 +267,12 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                 }
                 issue_st(t + 1);
             }
-            if (!wait_warp(&bar_ppd, par, abort_v, p.timeout_ns)) {
+            // With three or more dO slots, dO_{t+1} has normally landed by now: wait for it here
+            // so dK_t, dV_t and dP^T_{t+1} go out as one batch.  With two it may still be in
+            // flight, and waiting here would hold up dK_t and dV_t (measured slower).
+            constexpr bool kEarlyDo = C::kOStages >= 3;
+            if ((kEarlyDo && t + 1 < n_it && !wait_do(t + 1)) ||
+                !wait_warp(&bar_ppd, par, abort_v, p.timeout_ns)) {
                 ok = false;
                 break;
             }
@@ -286,7 +291,7 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                        sdesc_advance(dod, kk * 2048), C::kIdescG, (acc0 || kk > 0) ? 1u : 0u);
             mma_commit_w(&bar_oe[t % C::kOStages]);  // dO_t fully read
             if (t + 1 < n_it) {                     // after dV_t, dK_t read the dP^T columns
-                if (!wait_do(t + 1)) {
+                if (!kEarlyDo && !wait_do(t + 1)) {
                     ok = false;
                     break;
                 }

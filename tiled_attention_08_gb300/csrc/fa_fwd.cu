@@ -315,12 +315,9 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                 }
                 mma_commit_w(&bar_sf[t]);
             };
-            auto issue_pv = [&](int t, int j) -> bool {
+            auto issue_pv = [&](int t, int j) -> bool {  // V_j was waited for at the tile's start
                 const int st = j % C::kVStages;
                 if (!wait_warp(&bar_pf[t], (uint32_t)j & 1u, abort_v, p.timeout_ns))
-                    return false;
-                if (!wait_warp(&bar_vf[st], (uint32_t)(j / C::kVStages) & 1u, abort_v,
-                                  p.timeout_ns))
                     return false;
                 tc_fence_after_sync();
                 const uint64_t vd =
@@ -344,6 +341,15 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
             }
             for (int j = 0; ok && j < n_kv; ++j) {
                 const bool next = j + 1 < n_kv;
+                // Ring waits first, while this warp idles until P_A(j) anyway: then each P wait
+                // is followed by PV and the next S with no wait in between.
+                if (!wait_warp(&bar_vf[j % C::kVStages], (uint32_t)(j / C::kVStages) & 1u, abort_v,
+                               p.timeout_ns) ||
+                    (next && !wait_k(j + 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
     #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     const int n_t = t ? n_kv_b : n_kv_a;
