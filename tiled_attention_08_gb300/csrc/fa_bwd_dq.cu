@@ -22,9 +22,11 @@
 // TMEM: S [0,128), dP [128,256), dQ [256,256+D), Q [256+D, 256+3D/2), dO [256+3D/2, 256+2D).
 //
 // Pipeline.  The elementwise warps read S into registers and release its columns at once, so
-// the MMA warp issues S for the next key tile right away; once dP has been read, the 16-bit
-// dS is written over dP's first 64 columns and feeds the dQ MMA; the next dP is issued after
-// it.  The P phase of key tile j+1 therefore runs while the tensor core does dQ_j and dP_{j+1}.
+// the MMA warp issues S for the next key tile right away.  At D = 128 the 16-bit dS is then
+// written over dP's first 64 columns and feeds the dQ MMA; the next dP is issued after it.  At
+// D = 64 TMEM has room for dS in its own columns [256+2D, +64): dP_{j+1} is issued as soon as
+// dP_j has been read, and the elementwise warps write dS_{j+1} once dQ_j has completed.  The
+// P phase of key tile j+1 therefore runs while the tensor core does dQ_j and dP_{j+1}.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -51,7 +53,12 @@ struct DqCfg {
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmDQ = 256;
     static constexpr uint32_t kTmQ = 256 + D, kTmDO = 256 + D + D / 2;
-    static_assert(kTmDO + D / 2 <= kTmemCols, "TMEM budget");
+    // D = 64 leaves room for dS in its own 64 columns: dP_{j+1} then no longer waits for dQ_j
+    // to have read dS_j out of the dP columns.  At D = 128 dS is written over dP.
+    static constexpr bool kSepDS = (D == 64);
+    static constexpr uint32_t kTmDS = kSepDS ? 256 + 2 * D : kTmDP;
+    static_assert(kTmDO + D / 2 <= kTmemCols && (!kSepDS || kTmDS + 64 <= kTmemCols),
+                  "TMEM budget");
     static constexpr uint32_t kIdescS = idesc_f16(BF16, 128, 128, false, false);
     static constexpr uint32_t kIdescG = idesc_f16(BF16, 128, D, false, true);
 };
@@ -63,6 +70,7 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
+    __shared__ uint64_t bar_dpr, bar_dqd;  // dP read / dQ_j done (separate dS columns only)
     __shared__ uint64_t bar_qt, bar_kvf[C::kStages], bar_kve[C::kStages], bar_sf, bar_df, bar_sr,
         bar_pd, bar_done, bar_fin;
     __shared__ uint32_t tmem_base_sh;
@@ -88,7 +96,9 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
         mbar_init(&bar_sf, 1);
         mbar_init(&bar_df, 1);
         mbar_init(&bar_sr, C::kEwThreads);  // S read: its columns may be overwritten
-        mbar_init(&bar_pd, C::kEwThreads);  // dS written over dP
+        mbar_init(&bar_pd, C::kEwThreads);  // dS written
+        mbar_init(&bar_dpr, C::kEwThreads);  // dP read: its columns may be overwritten
+        mbar_init(&bar_dqd, 1);              // dQ_j done: the dS columns may be overwritten
         mbar_init(&bar_done, 1);
         mbar_init(&bar_fin, 1);
         mbar_fence_init();
@@ -180,6 +190,15 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
                     break;
                 }
                 issue_s(j + 1);
+                if constexpr (C::kSepDS) {
+                    // dP_{j+1} as soon as dP_j has been read (dS has its own columns).
+                    if (!wait_warp(&bar_dpr, par, abort_v, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    issue_dp(j + 1);
+                }
             }
             if (!wait_warp(&bar_pd, par, abort_v, p.timeout_ns)) {
                 ok = false;
@@ -189,10 +208,14 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
             const uint64_t kmd = sdesc_mnmajor_sw128(k_base(j), kChunkBytes);
 #pragma unroll
             for (int kk = 0; kk < kTileRows / 16; ++kk)
-                mma_ts_w(tmem + C::kTmDQ, tmem + C::kTmDP + kk * 8, sdesc_advance(kmd, kk * 2048),
+                mma_ts_w(tmem + C::kTmDQ, tmem + C::kTmDS + kk * 8, sdesc_advance(kmd, kk * 2048),
                        C::kIdescG, (j > 0 || kk > 0) ? 1u : 0u);
             mma_commit_w(&bar_kve[j % C::kStages]);  // K_j, V_j fully read
-            if (j + 1 < n_kv) issue_dp(j + 1);     // after dQ_j read the dS columns
+            if constexpr (C::kSepDS) {
+                mma_commit_w(&bar_dqd);  // dS_j consumed
+            } else {
+                if (j + 1 < n_kv) issue_dp(j + 1);  // after dQ_j read the dS columns
+            }
         }
         if (ok) mma_commit_w(&bar_done);
         if (!ok && lane == 0) record_timeout(p.status, abort_v);
@@ -290,16 +313,31 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
                                  q[0], q[1]);
                     }
                 }
+                if constexpr (C::kSepDS) {
+                    tc_fence_before_sync();
+                    mbar_arrive(&bar_dpr);  // this thread's dP columns are read
+                }
             }
-            // Every slice of the quadrant has read its dP columns before dS overwrites them.
-            // (All warps reach this barrier once per key tile on every path.)
-            ok = bar_and(grp_bar, kGrpThreads, ok);
-            if (!ok) break;
+            if constexpr (C::kSepDS) {
+                // dS has its own columns: wait only until dQ_{j-1} has read dS_{j-1}.
+                if (!ok) break;
+                if (j > 0) {
+                    ok = wait_bounded(&bar_dqd, par ^ 1u, abort_v, p.timeout_ns);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                }
+            } else {
+                // Every slice of the quadrant has read its dP columns before dS overwrites
+                // them.  (All warps reach this barrier once per key tile on every path.)
+                ok = bar_and(grp_bar, kGrpThreads, ok);
+                if (!ok) break;
+            }
             {
                 uint32_t pk[kC / 2];
 #pragma unroll
                 for (int i = 0; i < kC / 2; ++i) pk[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
-                tmem_st<kC / 2>(tmem + lane_off + C::kTmDP + part * (kC / 2), pk);
+                tmem_st<kC / 2>(tmem + lane_off + C::kTmDS + part * (kC / 2), pk);
             }
             tmem_st_wait();
             tc_fence_before_sync();
