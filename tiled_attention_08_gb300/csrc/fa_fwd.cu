@@ -262,6 +262,11 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
             }
             for (int j = 0; ok && j < n_kv; ++j) {
                 const bool next = j + 1 < n_kv;
+                // Slot j+1 first, while this warp idles until P_A(j) anyway.
+                if (next && !wait_kv(j + 1)) {
+                    ok = false;
+                    break;
+                }
     #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     const int n_t = t ? n_kv_b : n_kv_a;
@@ -270,15 +275,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (next && j + 1 < n_t) {
-                        if (t == 0 || j + 1 >= n_kv_a) {  // slot j+1 not yet waited for
-                            if (!wait_kv(j + 1)) {
-                                ok = false;
-                                break;
-                            }
-                        }
-                        issue_s(t, j + 1);
-                    }
+                    if (next && j + 1 < n_t) issue_s(t, j + 1);
                 }
                 if (!ok) break;
                 mma_commit_w(&bar_ke[j % C::kKStages]);  // K_j (S_j) and V_j (both PV_j) consumed
