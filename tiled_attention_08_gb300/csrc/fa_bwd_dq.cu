@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
             const uint32_t par = (uint32_t)j & 1u;
             if (j + 1 < n_kv) {
                 // S of the next key tile as soon as this one's S has been read.
-                if (!wait_warp(&bar_sr, par, abort_v, p.timeout_ns) || !wait_stage(j + 1)) {
+                if (!wait_stage(j + 1) || !wait_warp(&bar_sr, par, abort_v, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
