@@ -9,24 +9,24 @@
 //   dQ_i += dS K_j
 // dQ_i is scaled by the softmax scale and written once: no atomics, deterministic.
 //
-// GB300 layout.  Q_i and dO_i are the A operands of S and dP for every key tile, so they are
-// staged once into TMEM (16-bit, two values per column) and all three contractions here run
-// with A in TMEM; shared memory holds only the K_j / V_j ring.  With A in TMEM an M = N = 128
-// step reads 4 KB of shared memory instead of 8 KB (the latter is the SM's whole
-// shared-memory bandwidth over the 64 cycles a step takes), which leaves room for the TMA
-// copies that refill the ring.
+// GB300 layout.  dO_i is the A operand of dP for every key tile, so it is staged once into TMEM
+// (16-bit, two values per column) and dP runs with A in TMEM.  At D = 64, Q_i is staged the
+// same way for S = Q K_j^T; at D = 128 TMEM has no room for it beside a dedicated dS region,
+// so Q_i stays in shared memory (loaded once by TMA) and S reads both operands from there
+// (SS and TS contractions run at the same rate on this part).  Shared memory otherwise holds
+// the K_j / V_j ring.
 //
 // CTA roles: 4*kSplit elementwise warps (warp w: query rows 32*(w%4).. == TMEM lanes, key
-// columns [kCols*(w/4), +kCols)), then one TMA producer warp (the K_j / V_j ring) and one
-// MMA-issuer warp that also owns TMEM.
-// TMEM: S [0,128), dP [128,256), dQ [256,256+D), Q [256+D, 256+3D/2), dO [256+3D/2, 256+2D).
+// columns [kCols*(w/4), +kCols)), then one TMA producer warp (Q_i at D = 128, the K_j / V_j
+// ring) and one MMA-issuer warp that also owns TMEM.
+// TMEM: S [0,128), dP [128,256), dQ [256,256+D), then Q (D = 64 only, D/2 columns), dO (D/2)
+// and dS (64 columns).
 //
 // Pipeline.  The elementwise warps read S into registers and release its columns at once, so
-// the MMA warp issues S for the next key tile right away.  At D = 128 the 16-bit dS is then
-// written over dP's first 64 columns and feeds the dQ MMA; the next dP is issued after it.  At
-// D = 64 TMEM has room for dS in its own columns [256+2D, +64): dP_{j+1} is issued as soon as
-// dP_j has been read, and the elementwise warps write dS_{j+1} once dQ_j has completed.  The
-// P phase of key tile j+1 therefore runs while the tensor core does dQ_j and dP_{j+1}.
+// the MMA warp issues S for the next key tile right away.  dS has its own columns: dP_{j+1} is
+// issued as soon as dP_j has been read, and the elementwise warps write dS_{j+1} once dQ_j has
+// completed.  The P phase of key tile j+1 therefore runs while the tensor core does dQ_j and
+// dP_{j+1}.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -38,7 +38,11 @@ struct DqCfg {
     static constexpr int kChunks = D / kChunkElems;
     static constexpr int kTileBytes = kTileRows * D * 2;
     static constexpr int kStages = (D == 128) ? 3 : 6;  // K/V ring depth
-    static constexpr int kOffK = 0;
+    // D = 128: Q_i stays in shared memory (S = Q K_j^T reads both operands from there) so that
+    // TMEM has room for dS in its own columns; D = 64: Q_i is staged into TMEM as well.
+    static constexpr bool kQSmem = (D == 128);
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kQSmem ? kTileBytes : 0;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
     static constexpr int kSmemBytes = kOffV + kStages * kTileBytes + 1024;
     static constexpr int kSplit = 2;  // elementwise warps per TMEM lane quadrant
@@ -52,13 +56,12 @@ struct DqCfg {
     static constexpr int kStageCols = D / 2 / kSplit;  // packed Q / dO columns each warp stages
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmDQ = 256;
-    static constexpr uint32_t kTmQ = 256 + D, kTmDO = 256 + D + D / 2;
-    // D = 64 leaves room for dS in its own 64 columns: dP_{j+1} then no longer waits for dQ_j
-    // to have read dS_j out of the dP columns.  At D = 128 dS is written over dP.
-    static constexpr bool kSepDS = (D == 64);
-    static constexpr uint32_t kTmDS = kSepDS ? 256 + 2 * D : kTmDP;
-    static_assert(kTmDO + D / 2 <= kTmemCols && (!kSepDS || kTmDS + 64 <= kTmemCols),
-                  "TMEM budget");
+    // dS has its own 64 columns, so dP_{j+1} never waits for dQ_j to have read dS_j.
+    static constexpr uint32_t kTmQ = 256 + D;                   // D = 64 only
+    static constexpr uint32_t kTmDO = kQSmem ? 256 + D : 256 + D + D / 2;
+    static constexpr bool kSepDS = true;
+    static constexpr uint32_t kTmDS = kTmDO + D / 2;
+    static_assert(kTmDS + 64 <= kTmemCols, "TMEM budget");
     static constexpr uint32_t kIdescS = idesc_f16(BF16, 128, 128, false, false);
     static constexpr uint32_t kIdescG = idesc_f16(BF16, 128, D, false, true);
 };
@@ -70,7 +73,8 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    __shared__ uint64_t bar_dpr, bar_dqd;  // dP read / dQ_j done (separate dS columns only)
+    __shared__ uint64_t bar_dpr, bar_dqd;  // dP read / dQ_j done: the dS columns may be reused
+    __shared__ uint64_t bar_q;             // Q_i landed in shared memory (D = 128)
     __shared__ uint64_t bar_qt, bar_kvf[C::kStages], bar_kve[C::kStages], bar_sf, bar_df, bar_sr,
         bar_pd, bar_done, bar_fin;
     __shared__ uint32_t tmem_base_sh;
@@ -98,6 +102,7 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
         mbar_init(&bar_sr, C::kEwThreads);  // S read: its columns may be overwritten
         mbar_init(&bar_pd, C::kEwThreads);  // dS written
         mbar_init(&bar_dpr, C::kEwThreads);  // dP read: its columns may be overwritten
+        mbar_init(&bar_q, 1);
         mbar_init(&bar_dqd, 1);              // dQ_j done: the dS columns may be overwritten
         mbar_init(&bar_done, 1);
         mbar_init(&bar_fin, 1);
@@ -114,6 +119,13 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
         if (lane == 0) {
             tma_prefetch_desc(&p.tm_k);
             tma_prefetch_desc(&p.tm_v);
+            if constexpr (C::kQSmem) {
+                tma_prefetch_desc(&p.tm_q);
+                mbar_arrive_expect_tx(&bar_q, C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(smem + C::kOffQ + c * kChunkBytes, &p.tm_q, &bar_q, c * kChunkElems,
+                                qt * kTileRows, bh);
+            }
             bool ok = true;
             int issued = 0;
             for (int j = 0; j < n_kv; ++j) {
@@ -133,6 +145,8 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
                 issued = j + 1;
             }
             if (!ok) record_timeout(p.status, abort_v);
+            // Drain: no copy may still be landing when the CTA exits.
+            if (C::kQSmem) wait_bounded(&bar_q, 0, nullptr, p.timeout_ns);
             for (int j = issued - 1; j >= 0 && j >= issued - C::kStages; --j)
                 wait_bounded(&bar_kvf[j % C::kStages], (uint32_t)(j / C::kStages) & 1u, nullptr,
                              p.timeout_ns);
@@ -152,13 +166,18 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
             tc_fence_after_sync();
             return r;
         };
-        auto issue_s = [&](int j) {  // S = Q K_j^T, Q from TMEM
+        auto issue_s = [&](int j) {  // S = Q K_j^T, Q from shared memory (D=128) or TMEM
             const uint64_t kd = sdesc_kmajor_sw128(k_base(j));
+            const uint64_t qd = sdesc_kmajor_sw128(smem_u32(smem + C::kOffQ));
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                mma_ts_w(tmem + C::kTmS, tmem + C::kTmQ + kk * 8, sdesc_advance(kd, off),
-                       C::kIdescS, kk > 0 ? 1u : 0u);
+                if constexpr (C::kQSmem)
+                    mma_ss_w(tmem + C::kTmS, sdesc_advance(qd, off), sdesc_advance(kd, off),
+                             C::kIdescS, kk > 0 ? 1u : 0u);
+                else
+                    mma_ts_w(tmem + C::kTmS, tmem + C::kTmQ + kk * 8, sdesc_advance(kd, off),
+                             C::kIdescS, kk > 0 ? 1u : 0u);
             }
             mma_commit_w(&bar_sf);
         };
@@ -172,7 +191,8 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
             }
             mma_commit_w(&bar_df);
         };
-        bool ok = wait_warp(&bar_qt, 0, abort_v, p.timeout_ns);
+        bool ok = wait_warp(&bar_qt, 0, abort_v, p.timeout_ns) &&
+                  (!C::kQSmem || wait_warp(&bar_q, 0, abort_v, p.timeout_ns));
         tc_fence_after_sync();
         if (ok && n_kv > 0) {
             ok = wait_stage(0);
@@ -240,7 +260,7 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
             const bool valid = q_row < p.L;
             const size_t eoff = ((size_t)bh * p.L + q_row) * D + part * kE;
 #pragma unroll
-            for (int which = 0; which < 2; ++which) {
+            for (int which = C::kQSmem ? 1 : 0; which < 2; ++which) {
                 const uint4* src =
                     reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(
                                                        which ? p.dout : p.q) + eoff * 2);
