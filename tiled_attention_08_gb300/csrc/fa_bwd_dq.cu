@@ -59,7 +59,6 @@ struct DqCfg {
     // dS has its own 64 columns, so dP_{j+1} never waits for dQ_j to have read dS_j.
     static constexpr uint32_t kTmQ = 256 + D;                   // D = 64 only
     static constexpr uint32_t kTmDO = kQSmem ? 256 + D : 256 + D + D / 2;
-    static constexpr bool kSepDS = true;
     static constexpr uint32_t kTmDS = kTmDO + D / 2;
     static_assert(kTmDS + 64 <= kTmemCols, "TMEM budget");
     static constexpr uint32_t kIdescS = idesc_f16(BF16, 128, 128, false, false);
@@ -73,7 +72,7 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    __shared__ uint64_t bar_dpr, bar_dqd;  // dP read / dQ_j done: the dS columns may be reused
+    __shared__ uint64_t bar_dpr, bar_dqd;  // dP read / dQ_j done (dS columns reusable)
     __shared__ uint64_t bar_q;             // Q_i landed in shared memory (D = 128)
     __shared__ uint64_t bar_qt, bar_kvf[C::kStages], bar_kve[C::kStages], bar_sf, bar_df, bar_sr,
         bar_pd, bar_done, bar_fin;
@@ -210,15 +209,13 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
                     break;
                 }
                 issue_s(j + 1);
-                if constexpr (C::kSepDS) {
-                    // dP_{j+1} as soon as dP_j has been read (dS has its own columns).
-                    if (!wait_warp(&bar_dpr, par, abort_v, p.timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    issue_dp(j + 1);
+                // dP_{j+1} as soon as dP_j has been read (dS has its own columns).
+                if (!wait_warp(&bar_dpr, par, abort_v, p.timeout_ns)) {
+                    ok = false;
+                    break;
                 }
+                tc_fence_after_sync();
+                issue_dp(j + 1);
             }
             if (!wait_warp(&bar_pd, par, abort_v, p.timeout_ns)) {
                 ok = false;
@@ -231,11 +228,7 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
                 mma_ts_w(tmem + C::kTmDQ, tmem + C::kTmDS + kk * 8, sdesc_advance(kmd, kk * 2048),
                        C::kIdescG, (j > 0 || kk > 0) ? 1u : 0u);
             mma_commit_w(&bar_kve[j % C::kStages]);  // K_j, V_j fully read
-            if constexpr (C::kSepDS) {
-                mma_commit_w(&bar_dqd);  // dS_j consumed
-            } else {
-                if (j + 1 < n_kv) issue_dp(j + 1);  // after dQ_j read the dS columns
-            }
+            mma_commit_w(&bar_dqd);                  // dS_j consumed
         }
         if (ok) mma_commit_w(&bar_done);
         if (!ok && lane == 0) record_timeout(p.status, abort_v);
@@ -246,8 +239,6 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
         constexpr int kC = C::kCols;
         const int quad = warp & 3;              // TMEM lane quadrant (query rows)
         const int part = warp >> 2;             // which kC key columns
-        const uint32_t grp_bar = 1 + quad;      // named barrier of the quadrant
-        constexpr uint32_t kGrpThreads = 32 * C::kSplit;
         const int row = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const int q_row = qt * kTileRows + row;  // < Lpad always
@@ -333,25 +324,16 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
                                  q[0], q[1]);
                     }
                 }
-                if constexpr (C::kSepDS) {
-                    tc_fence_before_sync();
-                    mbar_arrive(&bar_dpr);  // this thread's dP columns are read
-                }
+                tc_fence_before_sync();
+                mbar_arrive(&bar_dpr);  // this thread's dP columns are read
             }
-            if constexpr (C::kSepDS) {
-                // dS has its own columns: wait only until dQ_{j-1} has read dS_{j-1}.
+            // dS has its own columns: wait only until dQ_{j-1} has read dS_{j-1}.
+            if (!ok) break;
+            if (j > 0) {
+                ok = wait_bounded(&bar_dqd, par ^ 1u, abort_v, p.timeout_ns);
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                if (j > 0) {
-                    ok = wait_bounded(&bar_dqd, par ^ 1u, abort_v, p.timeout_ns);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    tc_fence_after_sync();
-                }
-            } else {
-                // Every slice of the quadrant has read its dP columns before dS overwrites
-                // them.  (All warps reach this barrier once per key tile on every path.)
-                ok = bar_and(grp_bar, kGrpThreads, ok);
-                if (!ok) break;
+                tc_fence_after_sync();
             }
             {
                 uint32_t pk[kC / 2];
