@@ -38,6 +38,10 @@ struct DkdvCfg {
     // the same 1024-aligned dynamic allocation and no alignment slack is requested.
     static constexpr int kQStages = (D == 128) ? 3 : 4;
     static constexpr int kOStages = (D == 128) ? 2 : 3;
+    // With three or more dO slots the MMA warp waits for dO_{t+1} before issuing dK_t, and the
+    // producer issues dO_{t+1} only after Q_{t+2}, whose slot dK_{t+2-kQStages} frees: with two
+    // Q slots that is dK_t itself, a circular wait.
+    static_assert(kOStages < 3 || kQStages >= 3, "early dO wait needs three or more Q slots");
     static constexpr int kVecBytes = kTileRows * 4;  // one fp32 vector of a 128-row tile
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kTileBytes;
