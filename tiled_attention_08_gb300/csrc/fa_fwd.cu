@@ -87,8 +87,11 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
         bar_ve[C::kVStages], bar_sf[2], bar_pf[2], bar_oready[2], bar_fin;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
-    __shared__ float red_max[2][2][C::kSplit][128];  // [tile][parity][column slice][row]
-    __shared__ float red_sum[2][C::kSplit][128];     // [tile][column slice][row]
+    // Partial row maxima / sums exchanged between the column slices of a lane quadrant
+    // (kSplit > 1 only; one element otherwise).
+    constexpr int kRedRows = C::kSplit > 1 ? 128 : 1;
+    __shared__ float red_max[2][2][C::kSplit][kRedRows];  // [tile][parity][column slice][row]
+    __shared__ float red_sum[2][C::kSplit][kRedRows];     // [tile][column slice][row]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -213,11 +216,11 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
         }
     } else if (warp == C::kMmaWarp) {
         if constexpr (C::kMergedKV) {
-
             // ------------------------------ MMA issuer ------------------------------
-            // The whole warp walks the loop (warp-uniform values); one elected lane issues.  Each
-            // wait between MMA groups can let the tensor pipe's short queue run dry, so there are
-            // three per key tile: P of tile A, the next K/V slot, P of tile B.
+            // The whole warp walks the loop (warp-uniform values); one elected lane issues.  A
+            // wait between MMA groups can let the tensor pipe's short queue run dry, so each key
+            // tile starts with the wait for the next K/V slot (the warp would idle until P of
+            // tile A anyway); after that only P of tile A and P of tile B are waited for.
             bool ok = wait_warp(&bar_q, 0, abort_v, p.timeout_ns);
             auto wait_kv = [&](int j) -> bool {  // K_j and V_j landed
                 if (!wait_warp(&bar_kf[j % C::kKStages], (uint32_t)(j / C::kKStages) & 1u, abort_v,
@@ -230,7 +233,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                 const uint64_t qd = sdesc_kmajor_sw128(smem_u32(smem + C::kOffQ + t * C::kTileBytes));
                 const uint64_t kd =
                     sdesc_kmajor_sw128(smem_u32(smem + C::kOffK + (j % C::kKStages) * C::kTileBytes));
-    #pragma unroll
+#pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
                     mma_ss_w(tmem + C::kTmS + 128 * t, sdesc_advance(qd, off), sdesc_advance(kd, off),
@@ -244,7 +247,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                 tc_fence_after_sync();
                 const uint64_t vd = sdesc_mnmajor_sw128(
                     smem_u32(smem + C::kOffV + (j % C::kKStages) * C::kTileBytes), kChunkBytes);
-    #pragma unroll
+#pragma unroll
                 for (int kk = 0; kk < kTileRows / 16; ++kk) {
                     const uint64_t bd = sdesc_advance(vd, kk * 2048);
                     mma_ts_w(tmem + C::kTmO + D * t, tmem + C::kTmS + 128 * t + kk * 8, bd,
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                     ok = false;
                     break;
                 }
-    #pragma unroll
+#pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     const int n_t = t ? n_kv_b : n_kv_a;
                     if (!ok) break;
@@ -285,9 +288,10 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
             mma_commit_w(&bar_fin);
             wait_warp(&bar_fin, 0, nullptr, p.timeout_ns);
         } else {
-
             // ------------------------------ MMA issuer ------------------------------
-            // The whole warp walks the loop (warp-uniform values); one elected lane issues.
+            // The whole warp walks the loop (warp-uniform values); one elected lane issues.  Each
+            // key tile starts with the ring waits (V_j, K_{j+1}) while the warp would idle until
+            // P of tile A anyway; after that only the two P waits sit between MMA groups.
             bool ok = wait_warp(&bar_q, 0, abort_v, p.timeout_ns);
             int k_ready = -1;  // newest K tile known to have landed
             auto wait_k = [&](int j) -> bool {
@@ -304,7 +308,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                 const uint64_t qd = sdesc_kmajor_sw128(smem_u32(smem + C::kOffQ + t * C::kTileBytes));
                 const uint64_t kd =
                     sdesc_kmajor_sw128(smem_u32(smem + C::kOffK + (j % C::kKStages) * C::kTileBytes));
-    #pragma unroll
+#pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
                     mma_ss_w(tmem + C::kTmS + 128 * t, sdesc_advance(qd, off), sdesc_advance(kd, off),
@@ -319,7 +323,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                 tc_fence_after_sync();
                 const uint64_t vd =
                     sdesc_mnmajor_sw128(smem_u32(smem + C::kOffV + st * C::kTileBytes), kChunkBytes);
-    #pragma unroll
+#pragma unroll
                 for (int kk = 0; kk < kTileRows / 16; ++kk) {
                     const uint64_t bd = sdesc_advance(vd, kk * 2048);
                     mma_ts_w(tmem + C::kTmO + D * t, tmem + C::kTmS + 128 * t + kk * 8, bd,
@@ -347,7 +351,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-    #pragma unroll
+#pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     const int n_t = t ? n_kv_b : n_kv_a;
                     if (!ok) break;

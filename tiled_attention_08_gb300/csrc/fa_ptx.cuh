@@ -25,8 +25,6 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
-
 // Named barrier over `nthreads` threads (a multiple of 32) that also ANDs a predicate across
 // them: every participant gets true only if all passed true.  Used by warp pairs that share
 // TMEM lanes; both warps reach it the same number of times on every path, so a failure seen
@@ -138,44 +136,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 }
 
 // ---------------------------------------------------------------------------------------
-// Thread-block clusters (all data stays in this GPU's own memory)
-// ---------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Every thread of every CTA of the cluster arrives and waits (release/acquire).
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile(
-        "barrier.cluster.arrive.release.aligned;\n\t"
-        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// TMA tile load whose data (and complete_tx on the mbarrier at the same offset) lands in
-// every CTA of `cta_mask`, at the same shared-memory offsets as in the issuing CTA.
-__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                               int x, int y, int z, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
-// Untiled bulk copy multicast to the CTAs of `cta_mask` (same rules as bulk_load).
-__device__ __forceinline__ void bulk_load_mc(void* dst, const void* src, uint32_t bytes,
-                                             uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "h"(cta_mask)
-        : "memory");
-}
-
-// ---------------------------------------------------------------------------------------
 // Tensor memory
 // ---------------------------------------------------------------------------------------
 // Whole warp: allocates `ncols` TMEM columns (power of two, 32..512); base address -> *dst.
@@ -197,11 +157,6 @@ __device__ __forceinline__ void tc_fence_before_sync() {
 }
 __device__ __forceinline__ void tc_fence_after_sync() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// TMEM address of (lane, column).
-__device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
-    return base + (lane << 16) + col;
 }
 
 // Warp-wide: thread t reads lane (lane_base + t), 32 consecutive 32-bit columns, and waits.
@@ -335,32 +290,12 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool a
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T for one K=16 slice.  Issued by a single thread.
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem] for one K=16 slice; A occupies 8 TMEM columns (two 16-bit
-// values per 32-bit column, one row per lane).  Issued by a single thread.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Warp-converged forms: every lane of the warp executes the call with the same (warp-uniform)
-// arguments, and one lane chosen by elect.sync issues the instruction.  Keeping the issuing
-// warp converged lets the descriptors stay warp-uniform values.
+// D[tmem] (+)= A * B for one K=16 slice: mma_ss_w reads A and B from shared memory (via their
+// descriptors), mma_ts_w reads A from TMEM (8 columns: two 16-bit values per 32-bit column, one
+// row per lane).  Warp-converged: every lane of the warp executes the call with the same
+// (warp-uniform) arguments and one lane chosen by elect.sync issues the instruction; keeping
+// the issuing warp converged lets the descriptors stay warp-uniform values.  mma_commit_w
+// arrives once on `bar` when every tcgen05 operation issued so far by that lane is done.
 __device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -390,14 +325,6 @@ __device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
         : "memory");
 }
 
-// Arrives once on `bar` when every tcgen05 operation issued so far by this thread is done.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
 // Warp-wide load of N = 32, 64 or 128 consecutive columns (loads issued in pairs, one wait
 // per pair).
 template <int N>
@@ -414,19 +341,9 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
     }
 }
 
-// Like mma_commit, but arrives on the mbarrier at the same offset in every CTA of
-// `cta_mask` (used to release a multicast-filled shared-memory stage in all its readers).
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
-// Four consecutive fp32 values from shared memory (16-byte aligned shared address).  The
-// kernels align their dynamic shared memory through an integer round trip, which leaves the
-// compiler with generic pointers; an explicit ld.shared keeps these reads on the shared path.
+// Four consecutive fp32 values from shared memory (16-byte aligned shared address).  Shared
+// tiles are addressed through pointers the compiler may only know as generic (an integer
+// alignment round trip); an explicit ld.shared keeps these reads on the shared path.
 __device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
