@@ -12,16 +12,18 @@
 // and at the end dK_j is multiplied by the softmax scale.
 //
 // CTA roles: 4*kSplit elementwise warps (warp w: key rows 32*(w%4).. == TMEM lanes, query
-// columns [kCols*(w/4), +kCols)), then one TMA producer warp (K_j, V_j once; Q_i, dO_i,
-// LSE_i, Delta_i per stage) and one MMA-issuer warp that also owns TMEM.
+// columns [kCols*(w/4), +kCols)), then one TMA producer warp (K_j, V_j once; then Q_i with
+// -LSE_i*log2e into a Q ring and dO_i with Delta_i into a dO ring one slot shallower, Q one
+// tile ahead) and one MMA-issuer warp that also owns TMEM.
 // TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D).
 //
 // Pipeline.  The elementwise warps read S^T into registers (P^T stays there) and at once
 // release the S^T columns, so the MMA warp issues S^T of the NEXT query tile right away.
 // Once dP^T has been read too, the 16-bit P^T and dS^T are written side by side into the
-// dP^T columns (P^T at [128,192), dS^T at [192,256)), which feed the dV and dK MMAs; the next
-// dP^T is issued after those.  So the P phase of query tile i+1 runs while the tensor core
-// does dV_i, dK_i and dP^T_{i+1}, instead of waiting for them.
+// dP^T columns (P^T at [128,192), dS^T at [192,256)), which feed the dK and dV MMAs (dK first:
+// it releases Q_i, whose slot the next-but-one S^T needs); the next dP^T is issued after
+// those.  So the P phase of query tile i+1 runs while the tensor core does dK_i, dV_i and
+// dP^T_{i+1}, instead of waiting for them.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
