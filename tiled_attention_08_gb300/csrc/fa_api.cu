@@ -280,7 +280,6 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
         return FA_ERR_CUDA;
     float* nlse2_pad = static_cast<float*>(workspace);
     float* delta_pad = nlse2_pad + (size_t)sh.BH * sh.Lpad;
-    p.q = q;
     p.dout = dout;
     p.nlse2_pad = nlse2_pad;
     p.delta_pad = delta_pad;

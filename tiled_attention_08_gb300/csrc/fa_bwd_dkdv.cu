@@ -35,11 +35,12 @@ struct DkdvCfg {
     static constexpr int kChunks = D / kChunkElems;
     static constexpr int kTileBytes = kTileRows * D * 2;
     // Q_i is needed early (by S^T) and late (by dK), dO_i only in between, so the Q ring is one
-    // slot deeper than the dO ring.  At D = 128 the tiles then fill 224 KB of the 227 KB a block
-    // may have, so everything else (the -LSE*log2e and Delta vectors, the barriers) lives in
-    // the same 1024-aligned dynamic allocation and no alignment slack is requested.
-    static constexpr int kQStages = (D == 128) ? 3 : 4;
-    static constexpr int kOStages = (D == 128) ? 2 : 3;
+    // slot deeper than the dO ring (D = 64: five and four slots; six and five ran slower).  At
+    // D = 128 the tiles then fill 224 KB of the 227 KB a block may have, so everything else
+    // (the -LSE*log2e and Delta vectors, the barriers) lives in the same 1024-aligned dynamic
+    // allocation and no alignment slack is requested.
+    static constexpr int kQStages = (D == 128) ? 3 : 5;
+    static constexpr int kOStages = (D == 128) ? 2 : 4;
     // With three or more dO slots the MMA warp waits for dO_{t+1} before issuing dK_t, and the
     // producer issues dO_{t+1} only after Q_{t+2}, whose slot dK_{t+2-kQStages} frees: with two
     // Q slots that is dK_t itself, a circular wait.

@@ -10,17 +10,16 @@
 // dQ_i is scaled by the softmax scale and written once: no atomics, deterministic.
 //
 // GB300 layout.  dO_i is the A operand of dP for every key tile, so it is staged once into TMEM
-// (16-bit, two values per column) and dP runs with A in TMEM.  At D = 64, Q_i is staged the
-// same way for S = Q K_j^T; at D = 128 TMEM has no room for it beside a dedicated dS region,
-// so Q_i stays in shared memory (loaded once by TMA) and S reads both operands from there
-// (SS and TS contractions run at the same rate on this part).  Shared memory otherwise holds
-// the K_j / V_j ring.
+// (16-bit, two values per column) and dP runs with A in TMEM.  Q_i stays in shared memory
+// (loaded once by TMA) and S = Q K_j^T reads both operands from there: SS and TS contractions
+// run at the same rate on this part, and the TMEM columns Q would take go to a dedicated dS
+// region (staging Q into TMEM as well measured 1.3% slower at D = 64).  Shared memory
+// otherwise holds the K_j / V_j ring.
 //
 // CTA roles: 4*kSplit elementwise warps (warp w: query rows 32*(w%4).. == TMEM lanes, key
-// columns [kCols*(w/4), +kCols)), then one TMA producer warp (Q_i at D = 128, the K_j / V_j
-// ring) and one MMA-issuer warp that also owns TMEM.
-// TMEM: S [0,128), dP [128,256), dQ [256,256+D), then Q (D = 64 only, D/2 columns), dO (D/2)
-// and dS (64 columns).
+// columns [kCols*(w/4), +kCols)), then one TMA producer warp (Q_i, the K_j / V_j ring) and
+// one MMA-issuer warp that also owns TMEM.
+// TMEM: S [0,128), dP [128,256), dQ [256,256+D), dO [256+D, +D/2), dS (64 columns).
 //
 // Pipeline.  The elementwise warps read S into registers and release its columns at once, so
 // the MMA warp issues S for the next key tile right away.  dS has its own columns: dP_{j+1} is
@@ -38,14 +37,13 @@ struct DqCfg {
     static constexpr int kChunks = D / kChunkElems;
     static constexpr int kTileBytes = kTileRows * D * 2;
     static constexpr int kStages = (D == 128) ? 3 : 6;  // K/V ring depth
-    // D = 128: Q_i stays in shared memory (S = Q K_j^T reads both operands from there) so that
-    // TMEM has room for dS in its own columns; D = 64: Q_i is staged into TMEM as well.
-    static constexpr bool kQSmem = (D == 128);
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kQSmem ? kTileBytes : 0;
+    static constexpr int kOffK = kTileBytes;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
     static constexpr int kSmemBytes = kOffV + kStages * kTileBytes + 1024;
-    static constexpr int kSplit = 2;  // elementwise warps per TMEM lane quadrant
+    // Elementwise warps per TMEM lane quadrant: at D = 64 the tensor core spends half as long
+    // per key tile, so the elementwise phase is split over twice as many warps.
+    static constexpr int kSplit = (D == 64) ? 4 : 2;
     static constexpr int kEwWarps = 4 * kSplit;
     static constexpr int kEwThreads = kEwWarps * 32;
     static constexpr int kProducerWarp = kEwWarps;
@@ -53,12 +51,11 @@ struct DqCfg {
     static constexpr int kThreads = (kEwWarps + 2) * 32;
     static constexpr int kCols = 128 / kSplit;   // key columns per elementwise warp
     static constexpr int kOutCols = D / kSplit;  // dQ columns per elementwise warp
-    static constexpr int kStageCols = D / 2 / kSplit;  // packed Q / dO columns each warp stages
+    static constexpr int kStageCols = D / 2 / kSplit;  // packed dO columns each warp stages
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmDQ = 256;
     // dS has its own 64 columns, so dP_{j+1} never waits for dQ_j to have read dS_j.
-    static constexpr uint32_t kTmQ = 256 + D;                   // D = 64 only
-    static constexpr uint32_t kTmDO = kQSmem ? 256 + D : 256 + D + D / 2;
+    static constexpr uint32_t kTmDO = 256 + D;
     static constexpr uint32_t kTmDS = kTmDO + D / 2;
     static_assert(kTmDS + 64 <= kTmemCols, "TMEM budget");
     static constexpr uint32_t kIdescS = idesc_f16(BF16, 128, 128, false, false);
@@ -73,7 +70,7 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     __shared__ uint64_t bar_dpr, bar_dqd;  // dP read / dQ_j done (dS columns reusable)
-    __shared__ uint64_t bar_q;             // Q_i landed in shared memory (D = 128)
+    __shared__ uint64_t bar_q;             // Q_i landed in shared memory
     __shared__ uint64_t bar_qt, bar_kvf[C::kStages], bar_kve[C::kStages], bar_sf, bar_df, bar_sr,
         bar_pd, bar_done, bar_fin;
     __shared__ uint32_t tmem_base_sh;
@@ -91,7 +88,7 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(&bar_qt, C::kEwThreads);  // Q_i and dO_i staged into TMEM
+        mbar_init(&bar_qt, C::kEwThreads);  // dO_i staged into TMEM
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&bar_kvf[s], 1);
             mbar_init(&bar_kve[s], 1);
@@ -118,13 +115,11 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
         if (lane == 0) {
             tma_prefetch_desc(&p.tm_k);
             tma_prefetch_desc(&p.tm_v);
-            if constexpr (C::kQSmem) {
-                tma_prefetch_desc(&p.tm_q);
-                mbar_arrive_expect_tx(&bar_q, C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(smem + C::kOffQ + c * kChunkBytes, &p.tm_q, &bar_q, c * kChunkElems,
-                                qt * kTileRows, bh);
-            }
+            tma_prefetch_desc(&p.tm_q);
+            mbar_arrive_expect_tx(&bar_q, C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(smem + C::kOffQ + c * kChunkBytes, &p.tm_q, &bar_q, c * kChunkElems,
+                            qt * kTileRows, bh);
             bool ok = true;
             int issued = 0;
             for (int j = 0; j < n_kv; ++j) {
@@ -145,7 +140,7 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
             }
             if (!ok) record_timeout(p.status, abort_v);
             // Drain: no copy may still be landing when the CTA exits.
-            if (C::kQSmem) wait_bounded(&bar_q, 0, nullptr, p.timeout_ns);
+            wait_bounded(&bar_q, 0, nullptr, p.timeout_ns);
             for (int j = issued - 1; j >= 0 && j >= issued - C::kStages; --j)
                 wait_bounded(&bar_kvf[j % C::kStages], (uint32_t)(j / C::kStages) & 1u, nullptr,
                              p.timeout_ns);
@@ -165,18 +160,14 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
             tc_fence_after_sync();
             return r;
         };
-        auto issue_s = [&](int j) {  // S = Q K_j^T, Q from shared memory (D=128) or TMEM
+        auto issue_s = [&](int j) {  // S = Q K_j^T, both operands in shared memory
             const uint64_t kd = sdesc_kmajor_sw128(k_base(j));
             const uint64_t qd = sdesc_kmajor_sw128(smem_u32(smem + C::kOffQ));
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                if constexpr (C::kQSmem)
-                    mma_ss_w(tmem + C::kTmS, sdesc_advance(qd, off), sdesc_advance(kd, off),
-                             C::kIdescS, kk > 0 ? 1u : 0u);
-                else
-                    mma_ts_w(tmem + C::kTmS, tmem + C::kTmQ + kk * 8, sdesc_advance(kd, off),
-                             C::kIdescS, kk > 0 ? 1u : 0u);
+                mma_ss_w(tmem + C::kTmS, sdesc_advance(qd, off), sdesc_advance(kd, off),
+                         C::kIdescS, kk > 0 ? 1u : 0u);
             }
             mma_commit_w(&bar_sf);
         };
@@ -191,7 +182,7 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
             mma_commit_w(&bar_df);
         };
         bool ok = wait_warp(&bar_qt, 0, abort_v, p.timeout_ns) &&
-                  (!C::kQSmem || wait_warp(&bar_q, 0, abort_v, p.timeout_ns));
+                  wait_warp(&bar_q, 0, abort_v, p.timeout_ns);
         tc_fence_after_sync();
         if (ok && n_kv > 0) {
             ok = wait_stage(0);
@@ -243,29 +234,25 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const int q_row = qt * kTileRows + row;  // < Lpad always
         const int c0 = part * kC;
-        // Stage this warp's slice (D/kSplit elements) of the Q and dO rows into TMEM as
-        // packed 16-bit pairs; rows past L are zeros.
+        // Stage this warp's slice (D/kSplit elements) of the dO row into TMEM as packed 16-bit
+        // pairs; rows past L are zeros.
         {
             constexpr int kE = D / C::kSplit;       // elements per warp slice
             constexpr int kW = C::kStageCols;       // packed 32-bit columns per slice
             const bool valid = q_row < p.L;
             const size_t eoff = ((size_t)bh * p.L + q_row) * D + part * kE;
+            const uint4* src = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const uint8_t*>(p.dout) + eoff * 2);
+            uint32_t w[kW];
 #pragma unroll
-            for (int which = C::kQSmem ? 1 : 0; which < 2; ++which) {
-                const uint4* src =
-                    reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(
-                                                       which ? p.dout : p.q) + eoff * 2);
-                uint32_t w[kW];
-#pragma unroll
-                for (int v = 0; v < kW / 4; ++v) {
-                    const uint4 x = valid ? src[v] : make_uint4(0u, 0u, 0u, 0u);
-                    w[4 * v + 0] = x.x;
-                    w[4 * v + 1] = x.y;
-                    w[4 * v + 2] = x.z;
-                    w[4 * v + 3] = x.w;
-                }
-                tmem_st<kW>(tmem + lane_off + (which ? C::kTmDO : C::kTmQ) + part * kW, w);
+            for (int v = 0; v < kW / 4; ++v) {
+                const uint4 x = valid ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+                w[4 * v + 0] = x.x;
+                w[4 * v + 1] = x.y;
+                w[4 * v + 2] = x.z;
+                w[4 * v + 3] = x.w;
             }
+            tmem_st<kW>(tmem + lane_off + C::kTmDO + part * kW, w);
             tmem_st_wait();
             tc_fence_before_sync();
             mbar_arrive(&bar_qt);

@@ -60,8 +60,7 @@ struct BwdPreParams {
 
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // [BH, L, D] 16-bit, box {64, 128, 1}
-    const void* q;                        // [BH, L, D] (rows staged into TMEM by the dQ pass)
-    const void* dout;                     // [BH, L, D]
+    const void* dout;                     // [BH, L, D] (rows staged into TMEM by the dQ pass)
     const float* nlse2_pad;               // [BH, Lpad]: -LSE * log2(e)
     const float* delta_pad;               // [BH, Lpad]
     void* dq;                             // [BH, L, D]
