@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -167,11 +168,21 @@ def gpu_selector(dev) -> str:
 
 def kernel_sha(kernel: str) -> str:
     """Hash of everything that shapes a kernel's memory traffic: its source file, the shared
-    device headers and the host launcher (tile schedule, tensor maps)."""
+    device headers, the host launcher (tile schedule, tensor maps) and any other header of the
+    package that the kernel's source includes."""
     csrc = os.path.join(ROOT, "tiled_attention_08_gb300", "csrc")
+    shared = ("fa_internal.h", "fa_ptx.cuh", "fa_api.cu")
+    with open(os.path.join(csrc, KERNEL_SOURCES[kernel]), "rb") as f:
+        src = f.read()
+    extra = sorted(n for n in set(re.findall(rb'#include "([A-Za-z0-9_.]+)"', src))
+                   if n.decode() not in shared and os.path.exists(os.path.join(csrc, n.decode())))
     h = hashlib.sha256()
-    for name in (KERNEL_SOURCES[kernel], "fa_internal.h", "fa_ptx.cuh", "fa_api.cu"):
+    h.update(src)
+    for name in shared:
         with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    for name in extra:
+        with open(os.path.join(csrc, name.decode()), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 

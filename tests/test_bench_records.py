@@ -24,8 +24,10 @@ def bench_copy(tmp_path):
     bench = load_bench()
     csrc = tmp_path / "tiled_attention_08_gb300" / "csrc"
     csrc.mkdir(parents=True)
-    for name in set(bench.KERNEL_SOURCES.values()) | set(SHARED):
-        shutil.copy(os.path.join(ROOT, "tiled_attention_08_gb300", "csrc", name), csrc / name)
+    src_dir = os.path.join(ROOT, "tiled_attention_08_gb300", "csrc")
+    headers = {n for n in os.listdir(src_dir) if n.endswith((".h", ".cuh"))}
+    for name in set(bench.KERNEL_SOURCES.values()) | set(SHARED) | headers:
+        shutil.copy(os.path.join(src_dir, name), csrc / name)
     (tmp_path / "profiles").mkdir()
     bench.ROOT = str(tmp_path)
     return bench, tmp_path
@@ -54,6 +56,17 @@ def test_sha_covers_kernel_and_shared_files(bench_copy, edited):
     path = tmp / "tiled_attention_08_gb300" / "csrc" / name
     path.write_text(path.read_text() + "\n// edited\n")
     assert bench.kernel_sha(kernel) != before
+
+
+def test_sha_covers_headers_the_kernel_includes(bench_copy):
+    bench, tmp = bench_copy
+    # The dQ pass includes the persistent-schedule header; the other kernels do not.
+    before = {k: bench.kernel_sha(k) for k in bench.KERNEL_SOURCES}
+    path = tmp / "tiled_attention_08_gb300" / "csrc" / "fa_sched.h"
+    path.write_text(path.read_text() + "\n// edited\n")
+    after = {k: bench.kernel_sha(k) for k in bench.KERNEL_SOURCES}
+    assert after["bwd_dq"] != before["bwd_dq"]
+    assert after["bwd_dkdv"] == before["bwd_dkdv"] and after["fa_fwd"] == before["fa_fwd"]
 
 
 def test_record_used_only_while_sources_match(bench_copy):

@@ -1,6 +1,6 @@
-// fa_bwd_dq.cu -- attention backward, dQ: one CTA per (b*h, 128-query tile).
+// fa_bwd_dq.cu -- attention backward, dQ: per (b*h, 128-query tile), one CTA each or persistent.
 //
-// The separate-pass form of the dQ accumulation: for the CTA's query tile i and every key
+// The separate-pass form of the dQ accumulation: for each query tile i and every key
 // tile j it can see (j <= i under the causal mask), P and dS are recomputed from the saved
 // log-sum-exp ("FlashAttention data-flow optimisation: MI50 memory and bandwidth
 // bottlenecks", section 2.2, third layer) and
@@ -26,8 +26,27 @@
 // issued as soon as dP_j has been read, and the elementwise warps write dS_{j+1} once dQ_j has
 // completed.  The P phase of key tile j+1 therefore runs while the tensor core does dQ_j and
 // dP_{j+1}.
+//
+// Two schedules.  For rows of few key tiles (a mean of at most kPersistMaxKv per query tile)
+// fa_bwd_dq_kernel_persistent runs one CTA per SM (a CTA fills an SM: all 512 TMEM columns and
+// over 200 KB of shared memory), each taking its query tiles in the rounds of persistent_tile.
+// The fixed cost of a CTA (launch, barrier and TMEM set-up, the first copies' latency, the
+// pipeline fill and the dQ read-out) is then paid once per SM instead of once per tile, and
+// most of it overlaps the neighbouring tiles: the K_j / V_j ring runs on across tiles, Q of the
+// next tile is loaded as soon as the S contractions of this one have completed, the
+// elementwise warps stage the next dO right after reading this tile's last dP, and the next
+// tile's first S and dP run while they read out dQ.  Its barrier phases count key-tile
+// iterations (or tiles) over the CTA's lifetime.  For longer rows the fixed cost matters less
+// than the balance of the hardware's own block scheduling over heaviest-first tiles, and
+// fa_bwd_dq_kernel runs one CTA per query tile.  Measured: B8 H32 L4096 D128 causal (16.5
+// key tiles per query tile on average) 1.205 ms one CTA per tile, 1.109 persistent; B1 H16
+// L16384 D64 causal (64.5) 0.688 one CTA per tile, 0.715 persistent (0.722 with the
+// persistent kernel launched one CTA per tile).
+#include <atomic>
+
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
+#include "fa_sched.h"
 
 namespace fa {
 namespace {
@@ -62,6 +81,8 @@ struct DqCfg {
     static constexpr uint32_t kIdescG = idesc_f16(BF16, 128, D, false, true);
 };
 
+// One CTA per (b*h, query tile), in tile_coords order (the hardware's block scheduler balances
+// the causal tiles): for rows of many key tiles, where a CTA's fixed cost is a small share.
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
@@ -355,14 +376,411 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
     }
 }
 
+// Persistent CTAs (see the file header): for rows of few key tiles.
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
+    fa_bwd_dq_kernel_persistent(const __grid_constant__ BwdParams p) {
+    using C = DqCfg<D, BF16, CAUSAL>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    // Per key-tile iteration (phase = running iteration count over all tiles of this CTA):
+    __shared__ uint64_t bar_sf, bar_df;     // S / dP complete
+    __shared__ uint64_t bar_sr, bar_dpr;    // S / dP read: their columns may be overwritten
+    __shared__ uint64_t bar_pd;             // dS written
+    __shared__ uint64_t bar_dqd;            // dQ += dS K done: the dS columns may be overwritten
+    __shared__ uint64_t bar_kvf[C::kStages], bar_kve[C::kStages];  // K/V ring full / empty
+    // Per query tile (phase = tile count of this CTA):
+    __shared__ uint64_t bar_q;    // Q_i landed in shared memory
+    __shared__ uint64_t bar_qe;   // every S of the tile complete: the Q buffer may be refilled
+    __shared__ uint64_t bar_qt;   // dO_i staged into TMEM
+    __shared__ uint64_t bar_done; // every MMA of the tile complete: dQ_i final
+    __shared__ uint64_t bar_dqr;  // dQ_i read out: the accumulator may be overwritten
+    __shared__ uint64_t bar_fin;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    volatile int* abort_v = &abort_flag;
+    // Persistent CTAs: this CTA's query tiles in round order (persistent_tile); inside each
+    // round the ids follow tile_coords (heads in L2-sized groups, heaviest tiles first).
+    const int total = p.n_tiles * p.BH;
+    struct Tile {
+        int bh, qt, n_kv;
+    };
+    auto tile_of = [&](int round, Tile& t) -> bool {
+        const int id = persistent_tile(round, (int)blockIdx.x, (int)gridDim.x, total);
+        if (id < 0) return false;
+        int rank;
+        tile_coords(id, p.BH, p.n_tiles, p.group, t.bh, rank);
+        t.qt = p.n_tiles - 1 - rank;
+        t.n_kv = CAUSAL ? (t.qt + 1) : p.n_tiles;
+        return true;
+    };
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&bar_kvf[s], 1);
+            mbar_init(&bar_kve[s], 1);
+        }
+        mbar_init(&bar_sf, 1);
+        mbar_init(&bar_df, 1);
+        mbar_init(&bar_sr, C::kEwThreads);
+        mbar_init(&bar_dpr, C::kEwThreads);
+        mbar_init(&bar_pd, C::kEwThreads);
+        mbar_init(&bar_dqd, 1);
+        mbar_init(&bar_q, 1);
+        mbar_init(&bar_qe, 1);
+        mbar_init(&bar_qt, C::kEwThreads);
+        mbar_init(&bar_done, 1);
+        mbar_init(&bar_dqr, C::kEwThreads);
+        mbar_init(&bar_fin, 1);
+        mbar_fence_init();
+    }
+    if (warp == C::kMmaWarp) tmem_alloc(&tmem_base_sh, C::kTmemCols);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = tmem_base_sh;
+
+    if (warp == C::kProducerWarp) {
+        // ------------------------------ TMA producer ------------------------------
+        // Per tile: Q_i (once the previous tile's S contractions have completed), then its
+        // K_j / V_j into the ring, which runs on across tiles, so the next tile's first key
+        // tiles are already in flight while this one finishes.
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tm_k);
+            tma_prefetch_desc(&p.tm_v);
+            tma_prefetch_desc(&p.tm_q);
+            bool ok = true;
+            int gk = 0;       // K/V fills handed to the TMA unit
+            int q_loads = 0;  // Q fills handed to the TMA unit
+            Tile t;
+            for (int round = 0; ok && tile_of(round, t); ++round) {
+                if (q_loads > 0 &&
+                    !wait_bounded(&bar_qe, (uint32_t)(q_loads - 1) & 1u, abort_v, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&bar_q, C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(smem + C::kOffQ + c * kChunkBytes, &p.tm_q, &bar_q,
+                                c * kChunkElems, t.qt * kTileRows, t.bh);
+                ++q_loads;
+                for (int j = 0; j < t.n_kv; ++j) {
+                    const int st = gk % C::kStages;
+                    const uint32_t ph = (uint32_t)(gk / C::kStages) & 1u;
+                    if (gk >= C::kStages &&
+                        !wait_bounded(&bar_kve[st], ph ^ 1u, abort_v, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bar_kvf[st], 2 * C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        tma_load_3d(smem + C::kOffK + st * C::kTileBytes + c * kChunkBytes,
+                                    &p.tm_k, &bar_kvf[st], c * kChunkElems, j * kTileRows, t.bh);
+                        tma_load_3d(smem + C::kOffV + st * C::kTileBytes + c * kChunkBytes,
+                                    &p.tm_v, &bar_kvf[st], c * kChunkElems, j * kTileRows, t.bh);
+                    }
+                    ++gk;
+                }
+            }
+            if (!ok) record_timeout(p.status, abort_v);
+            // Drain: no copy may still be landing when the CTA exits.
+            if (q_loads > 0)
+                wait_bounded(&bar_q, (uint32_t)(q_loads - 1) & 1u, nullptr, p.timeout_ns);
+            for (int g = gk - 1; g >= 0 && g >= gk - C::kStages; --g)
+                wait_bounded(&bar_kvf[g % C::kStages], (uint32_t)(g / C::kStages) & 1u, nullptr,
+                             p.timeout_ns);
+        }
+    } else if (warp == C::kMmaWarp) {
+        // ------------------------------ MMA issuer ------------------------------
+        // The whole warp walks the loop (warp-uniform values); one elected lane issues.  g is
+        // the running key-tile iteration over all of this CTA's tiles (ring slot and phase).
+        auto k_base = [&](int g) {
+            return smem_u32(smem + C::kOffK + (g % C::kStages) * C::kTileBytes);
+        };
+        auto v_base = [&](int g) {
+            return smem_u32(smem + C::kOffV + (g % C::kStages) * C::kTileBytes);
+        };
+        auto wait_stage = [&](int g) {
+            const bool r = wait_warp(&bar_kvf[g % C::kStages], (uint32_t)(g / C::kStages) & 1u,
+                                     abort_v, p.timeout_ns);
+            tc_fence_after_sync();
+            return r;
+        };
+        auto issue_s = [&](int g) {  // S = Q K^T, both operands in shared memory
+            const uint64_t kd = sdesc_kmajor_sw128(k_base(g));
+            const uint64_t qd = sdesc_kmajor_sw128(smem_u32(smem + C::kOffQ));
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                mma_ss_w(tmem + C::kTmS, sdesc_advance(qd, off), sdesc_advance(kd, off),
+                         C::kIdescS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit_w(&bar_sf);
+        };
+        auto issue_dp = [&](int g) {  // dP = dO V^T, dO from TMEM
+            const uint64_t vd = sdesc_kmajor_sw128(v_base(g));
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                mma_ts_w(tmem + C::kTmDP, tmem + C::kTmDO + kk * 8, sdesc_advance(vd, off),
+                         C::kIdescS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit_w(&bar_df);
+        };
+        bool ok = true;
+        int g = 0;
+        int tc = 0;
+        Tile t;
+        for (int round = 0; ok && tile_of(round, t); ++round, ++tc) {
+            const int n = t.n_kv;
+            // Q_i landed and dO_i staged; the previous tile's last S and dP have been read (their
+            // columns are reused); K_0 / V_0 of this tile landed.
+            ok = wait_warp(&bar_q, (uint32_t)tc & 1u, abort_v, p.timeout_ns) &&
+                 wait_warp(&bar_qt, (uint32_t)tc & 1u, abort_v, p.timeout_ns);
+            if (ok && g > 0)
+                ok = wait_warp(&bar_sr, (uint32_t)(g - 1) & 1u, abort_v, p.timeout_ns) &&
+                     wait_warp(&bar_dpr, (uint32_t)(g - 1) & 1u, abort_v, p.timeout_ns);
+            if (ok) ok = wait_stage(g);
+            if (!ok) break;
+            issue_s(g);
+            if (n == 1) mma_commit_w(&bar_qe);  // the tile's only S: Q free once it completes
+            issue_dp(g);
+            for (int j = 0; j < n; ++j) {
+                const int gg = g + j;
+                const uint32_t par = (uint32_t)gg & 1u;
+                if (j + 1 < n) {
+                    // S of the next key tile as soon as this one's S has been read.
+                    if (!wait_stage(gg + 1) || !wait_warp(&bar_sr, par, abort_v, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    issue_s(gg + 1);
+                    if (j + 2 == n) mma_commit_w(&bar_qe);  // the tile's last S issued
+                    // dP_{j+1} as soon as dP_j has been read (dS has its own columns).
+                    if (!wait_warp(&bar_dpr, par, abort_v, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    issue_dp(gg + 1);
+                }
+                if (!wait_warp(&bar_pd, par, abort_v, p.timeout_ns) ||
+                    (j == 0 && tc > 0 &&
+                     !wait_warp(&bar_dqr, (uint32_t)(tc - 1) & 1u, abort_v, p.timeout_ns))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint64_t kmd = sdesc_mnmajor_sw128(k_base(gg), kChunkBytes);
+#pragma unroll
+                for (int kk = 0; kk < kTileRows / 16; ++kk)
+                    mma_ts_w(tmem + C::kTmDQ, tmem + C::kTmDS + kk * 8,
+                             sdesc_advance(kmd, kk * 2048), C::kIdescG,
+                             (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit_w(&bar_kve[gg % C::kStages]);  // K_j, V_j fully read
+                mma_commit_w(&bar_dqd);                   // dS_j consumed
+            }
+            if (!ok) break;
+            mma_commit_w(&bar_done);
+            g += n;
+        }
+        if (!ok && lane == 0) record_timeout(p.status, abort_v);
+        mma_commit_w(&bar_fin);
+        wait_warp(&bar_fin, 0, nullptr, p.timeout_ns);
+    } else {
+        // ------------------------------ elementwise warps ------------------------------
+        constexpr int kC = C::kCols;
+        const int quad = warp & 3;              // TMEM lane quadrant (query rows)
+        const int part = warp >> 2;             // which kC key columns
+        const int row = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const int c0 = part * kC;
+        // Stage this warp's slice (D/kSplit elements) of tile t's dO row into TMEM as packed
+        // 16-bit pairs (rows past L are zeros), and read the row's -LSE*log2(e) and Delta.
+        auto stage_do = [&](const Tile& t, float& nl, float& dl) {
+            constexpr int kE = D / C::kSplit;       // elements per warp slice
+            constexpr int kW = C::kStageCols;       // packed 32-bit columns per slice
+            const int q_row = t.qt * kTileRows + row;  // < Lpad always
+            const bool valid = q_row < p.L;
+            const size_t eoff = ((size_t)t.bh * p.L + q_row) * D + part * kE;
+            const uint4* src = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const uint8_t*>(p.dout) + eoff * 2);
+            uint32_t w[kW];
+#pragma unroll
+            for (int v = 0; v < kW / 4; ++v) {
+                const uint4 x = valid ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+                w[4 * v + 0] = x.x;
+                w[4 * v + 1] = x.y;
+                w[4 * v + 2] = x.z;
+                w[4 * v + 3] = x.w;
+            }
+            nl = p.nlse2_pad[(size_t)t.bh * p.Lpad + q_row];
+            dl = p.delta_pad[(size_t)t.bh * p.Lpad + q_row];
+            tmem_st<kW>(tmem + lane_off + C::kTmDO + part * kW, w);
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(&bar_qt);
+        };
+        Tile cur, nxt;
+        float nlse2 = 0.0f, dlt = 0.0f;  // -LSE * log2(e) and Delta of this thread's row
+        bool ok = tile_of(0, cur);       // every CTA has at least one tile
+        if (ok) stage_do(cur, nlse2, dlt);
+        int g = 0;
+        for (int round = 0, tc = 0; ok; ++round, ++tc) {
+            const bool has_next = tile_of(round + 1, nxt);
+            const int n = cur.n_kv;
+            const int q_row = cur.qt * kTileRows + row;
+            const int klim = CAUSAL ? min(p.L - 1, q_row) : (p.L - 1);
+            const uint64_t dlt2 = f2_make(dlt, dlt);
+            float nlse2_n = 0.0f, dlt_n = 0.0f;
+            for (int j = 0; j < n; ++j) {
+                const int gg = g + j;
+                const int key0 = j * kTileRows + c0;
+                const bool masked = (CAUSAL && j == n - 1) || (j * kTileRows + kTileRows > p.L);
+                const uint32_t par = (uint32_t)gg & 1u;
+                float pv[kC];
+                ok = wait_bounded(&bar_sf, par, abort_v, p.timeout_ns);
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok) {
+                    tc_fence_after_sync();
+                    uint32_t r[kC];
+                    tmem_ld_cols<kC>(tmem + lane_off + C::kTmS + c0, r);
+                    tc_fence_before_sync();
+                    mbar_arrive(&bar_sr);
+                    const uint64_t scale2 = f2_make(p.scale_log2, p.scale_log2);
+                    const uint64_t shift2 = f2_make(nlse2, nlse2);
+#pragma unroll
+                    for (int i = 0; i < kC; i += 2) {  // two columns per f32x2 instruction
+                        float y0, y1;
+                        f2_split(f2_fma(f2_make(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                        scale2, shift2),
+                                 y0, y1);
+                        pv[i] = ex2_approx(y0);
+                        pv[i + 1] = ex2_approx(y1);
+                    }
+                    if (masked) {
+#pragma unroll
+                        for (int i = 0; i < kC; ++i)
+                            if (key0 + i > klim) pv[i] = 0.0f;
+                    }
+                    ok = wait_bounded(&bar_df, par, abort_v, p.timeout_ns);
+                    ok = __all_sync(0xffffffffu, ok);
+                }
+                if (ok) {
+                    tc_fence_after_sync();
+                    constexpr int kLd = kC >= 64 ? 32 : 16;  // dP columns per load (registers)
+#pragma unroll
+                    for (int h = 0; h < kC / kLd; ++h) {
+                        uint32_t r[kLd];
+                        tmem_ld<kLd>(tmem + lane_off + C::kTmDP + c0 + h * kLd, r);
+#pragma unroll
+                        for (int i = 0; i < kLd; i += 2) {  // P o (dP - Delta), two at a time
+                            float* q = pv + h * kLd + i;
+                            f2_split(f2_mul(f2_make(q[0], q[1]),
+                                            f2_sub(f2_make(__uint_as_float(r[i]),
+                                                           __uint_as_float(r[i + 1])),
+                                                   dlt2)),
+                                     q[0], q[1]);
+                        }
+                    }
+                    tc_fence_before_sync();
+                    mbar_arrive(&bar_dpr);  // this thread's dP columns are read
+                }
+                if (!ok) break;
+                // dS has its own columns: wait until the previous dQ contraction (of this tile
+                // or the last one of the previous tile) has read them.
+                if (gg > 0) {
+                    ok = wait_bounded(&bar_dqd, par ^ 1u, abort_v, p.timeout_ns);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                }
+                {
+                    uint32_t pk[kC / 2];
+#pragma unroll
+                    for (int i = 0; i < kC / 2; ++i) pk[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
+                    tmem_st<kC / 2>(tmem + lane_off + C::kTmDS + part * (kC / 2), pk);
+                }
+                tmem_st_wait();
+                tc_fence_before_sync();
+                mbar_arrive(&bar_pd);
+                // The tile's last dP has completed (it was read above), so the next tile's dO
+                // may take the dO columns now: the MMA warp can start that tile's dP while
+                // this tile's dQ is read out.
+                if (j == n - 1 && has_next) stage_do(nxt, nlse2_n, dlt_n);
+            }
+            if (ok) {
+                ok = wait_bounded(&bar_done, (uint32_t)tc & 1u, abort_v, p.timeout_ns);
+                ok = __all_sync(0xffffffffu, ok);
+            }
+            if (!ok) break;
+            tc_fence_after_sync();
+            uint8_t* dst_row = reinterpret_cast<uint8_t*>(p.dq) +
+                               ((size_t)cur.bh * p.L + q_row) * D * 2 + part * C::kOutCols * 2;
+            tmem_row_to_global<BF16, C::kOutCols>(tmem + lane_off + C::kTmDQ + part * C::kOutCols,
+                                                  dst_row, p.scale, q_row < p.L);
+            tc_fence_before_sync();
+            mbar_arrive(&bar_dqr);  // the accumulator is read: the next tile may overwrite it
+            g += n;
+            if (!has_next) break;
+            cur = nxt;
+            nlse2 = nlse2_n;
+            dlt = dlt_n;
+        }
+        if (!ok && lane == 0) record_timeout(p.status, abort_v);
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == C::kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// Mean key tiles per query tile up to which the grid is persistent.
+constexpr int kPersistMaxKv = 32;
+
+// Number of SMs of the current device (looked up once per device); 0 if unknown.
+int sm_count() {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        cache[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_t(const BwdParams& p, cudaStream_t s) {
     using C = DqCfg<D, BF16, CAUSAL>;
+    const int total = p.n_tiles * p.BH;
+    const int mean_kv2 = CAUSAL ? p.n_tiles + 1 : 2 * p.n_tiles;  // twice the mean
+    const int n_sm = mean_kv2 <= 2 * kPersistMaxKv ? sm_count() : 0;
+    if (n_sm > 0 && n_sm < total) {
+        // Persistent: one CTA per SM (each fills an SM).
+        auto kern = fa_bwd_dq_kernel_persistent<D, BF16, CAUSAL>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        kern<<<(unsigned)n_sm, C::kThreads, C::kSmemBytes, s>>>(p);
+        return cudaGetLastError();
+    }
     auto kern = fa_bwd_dq_kernel<D, BF16, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)p.n_tiles * (unsigned)p.BH, C::kThreads, C::kSmemBytes, s>>>(p);
+    kern<<<(unsigned)total, C::kThreads, C::kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }
 
