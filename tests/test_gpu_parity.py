@@ -34,6 +34,23 @@ def test_small_shapes_full_tensors(oracle_mod, L, D, causal, dtype):
             gh.check_head(oracle_mod, w, inp, out, b, h, backward=True)
 
 
+@pytest.mark.parametrize("L,D,causal", [(L, D, c) for L in (377, 384) for D in (64, 128)
+                                         for c in (False, True)])
+def test_persistent_dq_rounds(oracle_mod, L, D, causal):
+    """More query tiles (2 x 40 heads x 3) than SMs, with few key tiles each: the dQ pass runs
+    its persistent form, each CTA taking tiles in two rounds; the tile order gives every head
+    tiles in both rounds, so each sampled head crosses the hand-offs between tiles."""
+    n_tiles = (L + 127) // 128
+    total = 2 * 40 * n_tiles
+    assert total > torch.cuda.get_device_properties(0).multi_processor_count
+    assert (n_tiles + 1 if causal else 2 * n_tiles) <= 64  # mean key tiles <= 32: persistent
+    w = workloads.custom(2, 40, L, D, causal, torch.bfloat16)
+    inp = workloads.make_inputs(w, seed=L + D + int(causal))
+    out = gh.run_gpu(w, inp, backward=True)
+    for b, h in gh.sample_heads(w.B, w.H):
+        gh.check_head(oracle_mod, w, inp, out, b, h, backward=True)
+
+
 @pytest.mark.parametrize("name", list(workloads.WORKLOADS))
 def test_workload_full_size(oracle_mod, name):
     """Each workload at its full size in the benchmark's launch configuration; heads are
