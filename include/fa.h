@@ -68,7 +68,9 @@ size_t fa_bwd_workspace_bytes(int B, int H, int L, int D);
  * dq, dk, dv [B,H,L,D] (dtype).  `workspace` is a device buffer of at least
  * fa_bwd_workspace_bytes(B,H,L,D) bytes, 16-byte aligned, owned by the caller; its contents
  * on entry do not matter.  Three kernels are enqueued on `stream`: the Delta/LSE preprocess,
- * the dK/dV pass (one CTA per key tile) and the dQ pass (one CTA per query tile).
+ * the dK/dV pass (one CTA per key tile) and the dQ pass (one CTA per query tile, or, when
+ * query tiles see at most 32 key tiles on average, one persistent CTA per SM taking query
+ * tiles in turn; the results are the same either way).
  * Data-flow page, section 2.2, third layer (recompute P from the saved statistics).
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
