@@ -85,6 +85,26 @@ int main() {
             ++failures;
         }
     }
+    // The dQ pass's grid: persistent (152 CTAs) for short rows with more tiles than SMs, one
+    // CTA per tile otherwise.  {n_tiles, BH, causal, n_sm, expected}
+    const int gcases[][5] = {{32, 256, 1, 152, 152},    // B8 H32 L4096 causal: mean 16.5
+                             {16, 32, 1, 152, 152},     // B1 H32 L2048 causal: mean 8.5
+                             {128, 16, 1, 152, 2048},   // B1 H16 L16384 causal: mean 64.5
+                             {4, 512, 0, 152, 152},     // B16 H32 L512: mean 4
+                             {32, 64, 0, 152, 152},     // non-causal L4096: mean 32 (limit)
+                             {33, 64, 0, 152, 2112},    // non-causal, mean 33
+                             {63, 64, 1, 152, 152},     // causal, mean 32
+                             {64, 64, 1, 152, 4096},    // causal, mean 32.5
+                             {1, 1, 0, 152, 1},         // fewer tiles than SMs
+                             {32, 256, 1, 0, 8192}};    // SM count unknown
+    for (const auto& c : gcases) {
+        const int got = fa::dq_grid(c[0], c[1], c[2] != 0, c[3]);
+        if (got != c[4]) {
+            std::printf("FAIL dq_grid(%d,%d,%d,%d) = %d, want %d\n", c[0], c[1], c[2], c[3], got,
+                        c[4]);
+            ++failures;
+        }
+    }
     std::printf(failures ? "FAILED %d\n" : "OK\n", failures);
     return failures ? 1 : 0;
 }

@@ -27,21 +27,21 @@
 // completed.  The P phase of key tile j+1 therefore runs while the tensor core does dQ_j and
 // dP_{j+1}.
 //
-// Two schedules.  For rows of few key tiles (a mean of at most kPersistMaxKv per query tile)
-// fa_bwd_dq_kernel_persistent runs one CTA per SM (a CTA fills an SM: all 512 TMEM columns and
-// over 200 KB of shared memory), each taking its query tiles in the rounds of persistent_tile.
-// The fixed cost of a CTA (launch, barrier and TMEM set-up, the first copies' latency, the
-// pipeline fill and the dQ read-out) is then paid once per SM instead of once per tile, and
-// most of it overlaps the neighbouring tiles: the K_j / V_j ring runs on across tiles, Q of the
-// next tile is loaded as soon as the S contractions of this one have completed, the
-// elementwise warps stage the next dO right after reading this tile's last dP, and the next
-// tile's first S and dP run while they read out dQ.  Its barrier phases count key-tile
-// iterations (or tiles) over the CTA's lifetime.  For longer rows the fixed cost matters less
-// than the balance of the hardware's own block scheduling over heaviest-first tiles, and
-// fa_bwd_dq_kernel runs one CTA per query tile.  Measured: B8 H32 L4096 D128 causal (16.5
-// key tiles per query tile on average) 1.205 ms one CTA per tile, 1.109 persistent; B1 H16
-// L16384 D64 causal (64.5) 0.688 one CTA per tile, 0.715 persistent (0.722 with the
-// persistent kernel launched one CTA per tile).
+// Two schedules (dq_grid).  For rows of few key tiles (a mean of at most kPersistMaxKv per
+// query tile) fa_bwd_dq_kernel_persistent runs one CTA per SM (a CTA fills an SM: all 512 TMEM
+// columns and over 200 KB of shared memory), each taking its query tiles in the rounds of
+// persistent_tile.  The fixed cost of a CTA (launch, barrier and TMEM set-up, the first copies'
+// latency, the pipeline fill and the dQ read-out) is then paid once per SM instead of once per
+// tile, and most of it overlaps the neighbouring tiles: the K_j / V_j ring runs on across
+// tiles, Q of the next tile is loaded as soon as the S contractions of this one have
+// completed, the elementwise warps stage the next dO right after reading this tile's last dP,
+// and the next tile's first S and dP run while they read out dQ.  Its barrier phases count
+// key-tile iterations (or tiles) over the CTA's lifetime.  For longer rows the fixed cost
+// matters less than the balance of the hardware's own block scheduling over heaviest-first
+// tiles, and fa_bwd_dq_kernel runs one CTA per query tile.  Measured: B8 H32 L4096 D128
+// causal (16.5 key tiles per query tile on average) 1.205 ms one CTA per tile, 1.109
+// persistent; B1 H16 L16384 D64 causal (64.5) 0.688 one CTA per tile, 0.715 persistent (0.722
+// with the persistent kernel launched one CTA per tile).
 #include <atomic>
 
 #include "fa_internal.h"
@@ -743,9 +743,6 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
     }
 }
 
-// Mean key tiles per query tile up to which the grid is persistent.
-constexpr int kPersistMaxKv = 32;
-
 // Number of SMs of the current device (looked up once per device); 0 if unknown.
 int sm_count() {
     constexpr int kMaxDevices = 64;
@@ -765,15 +762,14 @@ template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_t(const BwdParams& p, cudaStream_t s) {
     using C = DqCfg<D, BF16, CAUSAL>;
     const int total = p.n_tiles * p.BH;
-    const int mean_kv2 = CAUSAL ? p.n_tiles + 1 : 2 * p.n_tiles;  // twice the mean
-    const int n_sm = mean_kv2 <= 2 * kPersistMaxKv ? sm_count() : 0;
-    if (n_sm > 0 && n_sm < total) {
+    const int grid = dq_grid(p.n_tiles, p.BH, CAUSAL, sm_count());
+    if (grid < total) {
         // Persistent: one CTA per SM (each fills an SM).
         auto kern = fa_bwd_dq_kernel_persistent<D, BF16, CAUSAL>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
-        kern<<<(unsigned)n_sm, C::kThreads, C::kSmemBytes, s>>>(p);
+        kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, s>>>(p);
         return cudaGetLastError();
     }
     auto kern = fa_bwd_dq_kernel<D, BF16, CAUSAL>;

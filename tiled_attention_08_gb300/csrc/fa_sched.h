@@ -13,4 +13,15 @@ __host__ __device__ __forceinline__ int persistent_tile(int round, int cta, int 
     return id < (long long)total ? (int)id : -1;
 }
 
+// Grid of the dQ pass.  Persistent (one CTA per SM) when query tiles see at most kPersistMaxKv
+// key tiles on average and there are more tiles than SMs; otherwise one CTA per tile.  The
+// fixed cost of a CTA is worth hiding only for short rows; for long rows the hardware's own
+// block scheduling balances the causal tiles better than fixed rounds.
+constexpr int kPersistMaxKv = 32;
+__host__ __device__ __forceinline__ int dq_grid(int n_tiles, int BH, bool causal, int n_sm) {
+    const int total = n_tiles * BH;
+    const int mean_kv2 = causal ? n_tiles + 1 : 2 * n_tiles;  // twice the mean
+    return (n_sm > 0 && n_sm < total && mean_kv2 <= 2 * kPersistMaxKv) ? n_sm : total;
+}
+
 }  // namespace fa
