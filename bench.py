@@ -446,9 +446,179 @@ def run_ours(args, w):
     if not args.no_e2e:
         del q, k, v, do, o, lse, dq, dk, dv, ws  # the e2e pass allocates its own buffer sets
         result["e2e"] = run_e2e(w, inp, dev, K)
+    if world == 1 and not args.no_configs:
+        import gc
+        gc.collect()
+        torch.cuda.empty_cache()
+        result["configs"] = run_configs(dev, skip=w.name)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, inp)
     return result if rank == 0 else None
+
+
+L2_BYTES = 129 * 2**20  # GB300 L2
+
+
+def _time_config(w, dev, peaks):
+    """Times one workload's fa_fwd + fa_bwd through the C ABI with every kernel bracketed by
+    CUDA events, sampling clocks meanwhile.  Inputs that fit in L2 get an L2 flush (a write of
+    a 256 MiB buffer, outside the kernels' events) before every step, so each step starts cold.
+    The step count is chosen from the warm-up so the timed region lasts about half a second."""
+    import torch
+    import tiled_attention_08_gb300 as fa
+    import workloads
+    from tiled_attention_08_gb300 import perfmodel as pm
+    inp = workloads.make_inputs(w, seed=0)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    B, H, L, D = w.B, w.H, w.L, w.D
+    dt = fa.FA_BF16 if w.dtype == torch.bfloat16 else fa.FA_FP16
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, L), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws_bytes = fa.fa_bwd_workspace_bytes(B, H, L, D)
+    ws = torch.empty(max(ws_bytes, 16), device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    flush = None
+    if q.numel() * q.element_size() < L2_BYTES:
+        flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        if flush is not None:
+            flush.fill_(1)
+        if ev is not None:
+            fa.fa_trace_next_call([ev[0].cuda_event, ev[1].cuda_event], 1)
+        st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                       B, H, L, D, w.scale, int(w.causal), dt, sh)
+        if st != fa.FA_OK:
+            raise fa.FaError("fa_fwd", st)
+        if ev is not None:
+            fa.fa_trace_next_call([x.cuda_event for x in ev[2:8]], 3)
+        st = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
+                       ws_bytes, B, H, L, D, w.scale, int(w.causal), dt, sh)
+        if st != fa.FA_OK:
+            raise fa.FaError("fa_bwd", st)
+
+    def events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)
+        return evs
+
+    warm = [events(8) for _ in range(3)]
+    for ev in warm:
+        step(ev)
+    torch.cuda.synchronize(dev)
+    t_step = min(sum(ev[2 * j].elapsed_time(ev[2 * j + 1]) for j in range(4)) for ev in warm)
+    steps = int(max(10, min(400, math.ceil(500.0 / max(t_step, 1e-3)))))
+    kev = [events(8) for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(gpu_selector(dev))
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(steps):
+        step(kev[i])
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    st = fa.fa_get_device_status(sh)
+    if st != fa.FA_OK:
+        raise fa.FaError(w.name, st)
+    kern_ms = {name: statistics.mean(kev[i][2 * j].elapsed_time(kev[i][2 * j + 1])
+                                     for i in range(steps))
+               for j, name in enumerate(KERNELS)}
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    fwd_ms = kern_ms["fa_fwd"]
+    bwd_ms = kern_ms["bwd_pre"] + kern_ms["bwd_dkdv"] + kern_ms["bwd_dq"]
+    fwd_tf = pm.flops_fwd(B, H, L, D, w.causal) / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = pm.flops_bwd(B, H, L, D, w.causal) / (bwd_ms * 1e-3) / 1e12
+    dom = max(("fa_fwd", "bwd_dkdv", "bwd_dq"), key=lambda n: kern_ms[n])
+    dom_tf = pm.flops_kernel(dom, B, H, L, D, w.causal) / (kern_ms[dom] * 1e-3) / 1e12
+    tot_flops = pm.flops_fwd(B, H, L, D, w.causal) + pm.flops_bwd(B, H, L, D, w.causal)
+    return {
+        "B": B, "H": H, "L": L, "D": D, "causal": w.causal, "dtype": w.dtype_name,
+        "row_scaled": w.row_scaled, "steps": steps,
+        "l2": "flushed before every step" if flush is not None else "inputs larger than L2",
+        "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4),
+        "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2),
+        "fwd_bwd_tflops": round(tot_flops / ((fwd_ms + bwd_ms) * 1e-3) / 1e12, 2),
+        "fwd_frac_of_peak": round(fwd_tf / peak_tf, 4),
+        "bwd_frac_of_peak": round(bwd_tf / peak_tf, 4),
+        "fwd_hbm_gbs": round(pm.bytes_fwd(B, H, L, D) / (fwd_ms * 1e-3) / 1e9, 1),
+        "bwd_hbm_gbs": round(pm.bytes_bwd(B, H, L, D) / (bwd_ms * 1e-3) / 1e9, 1),
+        "kernels_ms": {n: round(kern_ms[n], 4) for n in KERNELS},
+        "dominant": {"kernel": dom, "tflops": round(dom_tf, 2),
+                     "frac": round(dom_tf / peak_tf, 4)},
+        "clocks": clocks,
+    }
+
+
+def _time_forward_latency(w, dev, launches=1000):
+    """Latency of single forward launches (a one-tile problem is launch-bound): each of
+    `launches` calls is bracketed by CUDA events on the launching stream, and the median and
+    the mean over them are reported, with the mean of the same calls back to back."""
+    import torch
+    import tiled_attention_08_gb300 as fa
+    import workloads
+    inp = workloads.make_inputs(w, seed=0, with_do=False)
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    B, H, L, D = w.B, w.H, w.L, w.D
+    dt = fa.FA_BF16 if w.dtype == torch.bfloat16 else fa.FA_FP16
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, L), device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def call():
+        st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                       B, H, L, D, w.scale, int(w.causal), dt, sh)
+        if st != fa.FA_OK:
+            raise fa.FaError("fa_fwd", st)
+
+    for _ in range(20):
+        call()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(launches)]
+    for a, b in evs:
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(gpu_selector(dev))
+    sampler.start()
+    time.sleep(0.3)
+    for a, b in evs:
+        fa.fa_trace_next_call([a.cuda_event, b.cuda_event], 1)
+        call()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(launches):
+        call()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    st = fa.fa_get_device_status(sh)
+    if st != fa.FA_OK:
+        raise fa.FaError(w.name, st)
+    us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+    return {"B": B, "H": H, "L": L, "D": D, "causal": w.causal, "dtype": w.dtype_name,
+            "forward_only": True, "launches": launches,
+            "fwd_latency_us_median": round(statistics.median(us), 3),
+            "fwd_latency_us_mean": round(statistics.mean(us), 3),
+            "fwd_latency_us_p90": round(us[int(0.9 * (len(us) - 1))], 3),
+            "fwd_back_to_back_us": round(t0.elapsed_time(t1) * 1e3 / launches, 3),
+            "l2": "warm (the 66 KB problem stays in L2)", "clocks": clocks}
+
+
+def run_configs(dev, skip):
+    """Every other workload of the path, each timed on its own (see _time_config)."""
+    import workloads
+    peaks, _ = load_peaks()
+    out = {}
+    for name, w in workloads.WORKLOADS.items():
+        if name == skip:
+            continue
+        out[name] = _time_config(w, dev, peaks) if w.backward else _time_forward_latency(w, dev)
+    return out
 
 
 def run_e2e(w, inp, dev, K):
@@ -551,6 +721,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer end-to-end pass (profiling runs)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config measurements of the other workloads")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

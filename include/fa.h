@@ -16,9 +16,12 @@
  *  - Tensors are DEVICE pointers to contiguous row-major [B, H, L, D] arrays (LSE: [B, H, L]
  *    fp32), each 16-byte aligned.  q, k, v, o, dO, dq, dk, dv all have the dtype `dtype`.
  *  - Supported: D in {64, 128}; B, H, L >= 0 (an empty problem returns FA_OK and launches
- *    nothing); causal in {0, 1} (query i sees key j iff j <= i); scale finite.
+ *    nothing); causal in {0, 1} (query i sees key j iff j <= i); scale finite, of either sign
+ *    or zero ("FlashAttention principles and engineering practice", section 2.1: the scale
+ *    multiplies q k^T before the softmax), with scale * (q . k) inside the fp32 range.
  *  - The caller allocates and owns every buffer, including the backward workspace; the
- *    library never allocates or frees device memory in these calls.
+ *    library never allocates or frees device memory in these calls.  The one exception is
+ *    fa_bwd_noalloc's fixed scratch array, which is compiled into the library.
  *  - Calls are asynchronous: they validate, enqueue on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream) and return without synchronising.  Argument errors are reported
  *    before anything is enqueued and leave every output untouched.  A non-OK status from a
@@ -26,8 +29,12 @@
  *    its time limit records FA_ERR_TIMEOUT in a device status word, read by
  *    fa_get_device_status().
  *  - Outputs must not overlap inputs.  fa_bwd overwrites dq, dk, dv (it does not accumulate).
- *  - The library keeps no per-call state; it caches only the driver entry point used to
- *    build TMA descriptors and, per device, the address of its status word.
+ *  - The library keeps no per-call state.  It caches the driver entry point used to build TMA
+ *    descriptors and, per device index, the address of its status word, the address of
+ *    fa_bwd_noalloc's scratch array and the SM count.  Those addresses belong to the device's
+ *    primary context: after cudaDeviceReset (or anything else that destroys that context) the
+ *    cached addresses are stale, so do not call into the library on that device again in the
+ *    same process.
  */
 #ifndef FA_H
 #define FA_H
@@ -60,6 +67,10 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
  * Bytes of device workspace fa_bwd needs for this shape: two fp32 vectors per head padded to
  * a whole number of 128-row tiles (-LSE * log2(e) and Delta = rowsum(dO * O)).
  * Returns 0 for an empty problem or invalid sizes.
+ * The pages have no such call: they keep "the max and the sum of exponentials" for the
+ * backward (data-flow page, section 2.2, third layer) without saying where the per-row
+ * vectors the backward derives from them live.  Here the caller owns that memory, so the
+ * library reports how much it needs.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int L, int D);
 
@@ -101,7 +112,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  * a device shares the one array, so calls whose kernels overlap on the GPU (on different
  * streams, or from different threads) race on it and give undefined results: serialise them.
  * Nothing in the array needs clearing between calls; each call's first kernel overwrites
- * everything its later kernels read.
+ * everything its later kernels read.  Checks run in fa_bwd's order (sizes and flags, then null
+ * pointers), then the scratch limit, then fa_bwd's remaining checks; every outcome consumes a
+ * trace arming made with fa_trace_next_call.
  */
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                          const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
@@ -112,6 +125,8 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
  * FA_OK, FA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last call, or
  * FA_ERR_CUDA if synchronisation itself failed or a kernel refused to run (its dynamic shared
  * memory was not 1024-byte aligned; it then wrote nothing).
+ * The pages are silent on failure detection; this call is the library's own way of making a
+ * stalled kernel visible without faulting the GPU (every device-side wait is bounded).
  */
 fa_status fa_get_device_status(void* stream);
 
@@ -140,7 +155,8 @@ fa_status fa_trace_next_call(void* const* events, int n_pairs);
 /* Number of kernels this library has enqueued in this process so far. */
 uint64_t fa_launch_count(void);
 
-/* Static, human-readable name of a status code. */
+/* Static, human-readable name of a status code.  The pages have no counterpart (they
+ * define no C interface); it names the fa_status values above. */
 const char* fa_status_string(int status);
 
 #ifdef __cplusplus

@@ -4,11 +4,13 @@ Tolerances are the ones the method's target states for 16-bit inputs with fp32 a
 O max-abs <= 1e-2 and mean-abs <= 1e-3 (N(0,1) inputs), LSE max-abs <= 1e-3, and dQ/dK/dV
 relative Frobenius error <= 2e-2.
 
-O is returned in the 16-bit input dtype, so even the exact result stored in that dtype is off
-by up to half an ulp of the format (0.0078 for |O| in [2,4) in bf16).  The O bounds therefore
-apply to the error beyond that unavoidable rounding: per element,
-    excess = max(0, |O_gpu - O_ref| - ulp16(O_ref) / 2),
-and max(excess) <= 1e-2, mean(excess) <= 1e-3.  The raw errors are reported alongside.
+For i.i.d. N(0,1) inputs at the usual 1/sqrt(D) scale (``Workload.plain_inputs``) the O bounds
+are asserted on the raw error |O_gpu - O_ref|, exactly as stated.  Other inputs (row-scaled
+queries, stretched keys, scales far from 1/sqrt(D)) make the softmax peaked, so |O| reaches
+about 4, where the exact result stored in 16 bits is already off by up to half an ulp (0.0078
+in bf16 for |O| in [2,4)).  There the bounds apply to the error beyond that unavoidable
+rounding: per element excess = max(0, |O_gpu - O_ref| - ulp16(O_ref) / 2), max(excess) <= 1e-2
+and mean(excess) <= 1e-3; the raw errors are reported alongside.
 """
 import numpy as np
 import pytest
@@ -78,16 +80,24 @@ def f64(t):
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def check_head(oracle, w, inp, out, b, h, backward=True):
-    """Compares one (b,h) head of the GPU result with the oracle; returns the error summary."""
+def check_head(oracle, w, inp, out, b, h, backward=True, raw_o=None):
+    """Compares one (b,h) head of the GPU result with the oracle; returns the error summary.
+
+    ``raw_o`` (default: ``w.plain_inputs``) selects the raw O bound; pass False when the test
+    has reshaped plain inputs so that the softmax is peaked."""
+    if raw_o is None:
+        raw_o = w.plain_inputs
     q, k, v = (f64(inp[n][b, h]) for n in ("q", "k", "v"))
     o_ref, lse_ref = oracle.forward(q, k, v, w.scale, w.causal)
     o = f64(out["o"][b, h])
     lse = f64(out["lse"][b, h])
     err = o_errors(o, o_ref, w.dtype)
     err["lse_max"] = float(np.max(np.abs(lse - lse_ref))) if lse.size else 0.0
-    assert err["o_max"] <= O_MAX_ABS, (b, h, err)
-    assert err["o_mean"] <= O_MEAN_ABS, (b, h, err)
+    err["o_bound"] = "raw" if raw_o else "beyond half ulp"
+    o_max, o_mean = (err["o_raw_max"], err["o_raw_mean"]) if raw_o else (err["o_max"],
+                                                                          err["o_mean"])
+    assert o_max <= O_MAX_ABS, (b, h, err)
+    assert o_mean <= O_MEAN_ABS, (b, h, err)
     assert err["lse_max"] <= LSE_MAX_ABS, (b, h, err)
     if backward:
         do = f64(inp["do"][b, h])

@@ -86,8 +86,9 @@ def test_deterministic(oracle_mod):
 
 
 def test_row_scaled_extremes(oracle_mod):
-    """Large logits (Q rows scaled up to x4, scale 1): the running max moves by far more
-    than the rescale threshold across tiles, exercising the O rescale path."""
+    """Large logits (Q rows scaled up to x4, keys stretched up to x3 along the sequence, scale
+    1/sqrt(64)): the running max moves by far more than the rescale threshold across tiles,
+    exercising the O rescale path."""
     w = workloads.Workload("row_scaled_unit_scale", 1, 2, 640, 64, False, torch.bfloat16,
                            row_scaled=True)
     inp = workloads.make_inputs(w, seed=9)
@@ -96,6 +97,22 @@ def test_row_scaled_extremes(oracle_mod):
     out = gh.run_gpu(w, inp)
     for b, h in [(0, 0), (0, 1)]:
         gh.check_head(oracle_mod, w, inp, out, b, h)
+
+
+@pytest.mark.parametrize("scale", (1.0, 0.3, -0.125, 0.0))
+@pytest.mark.parametrize("D,dtype", ((64, torch.float16), (128, torch.bfloat16)),
+                         ids=("D64-fp16", "D128-bf16"))
+@pytest.mark.parametrize("causal", (False, True))
+def test_scale_argument(oracle_mod, scale, D, dtype, causal):
+    """The scale multiplies Q K^T before the mask and the softmax for any finite value: larger
+    than 1/sqrt(D) (a peaked softmax), negative (the row maximum of the logits is then taken
+    where Q K^T is smallest) and zero (a uniform softmax).  Row-scaled queries widen the logit
+    range; three query tiles with a ragged tail."""
+    w = workloads.custom(1, 2, 300, D, causal, dtype, row_scaled=True, scale=scale)
+    inp = workloads.make_inputs(w, seed=31 + D)
+    out = gh.run_gpu(w, inp, backward=True)
+    for h in range(w.H):
+        gh.check_head(oracle_mod, w, inp, out, 0, h, backward=True)
 
 
 def test_timeout_reported_and_context_survives(oracle_mod):

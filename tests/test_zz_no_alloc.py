@@ -5,20 +5,11 @@ not call cudaMalloc) cannot hand fa_bwd a workspace; fa_bwd_noalloc takes its sc
 fixed 16 MiB array inside the library instead.  This file is collected last on purpose: a
 failure here must not stop a fail-fast run before every other test has run.
 """
-import numpy as np
 import pytest
 import torch
 
 import tiled_attention_08_gb300 as fa
 import workloads
-
-GRAD_REL_FRO = 2e-2  # the gradient tolerance of the parity tests
-
-
-def _rel(a, b):
-    a = a.double()
-    b = b.double()
-    return float((a - b).norm() / b.norm().clamp_min(1e-30))
 
 
 @pytest.mark.gpu
@@ -38,9 +29,16 @@ def test_noalloc_matches_workspace_backward_on_consecutive_calls():
                             A + (5 << 30), A + (6 << 30), A + (7 << 30), A + (8 << 30),
                             64, 64, 1024, 64, 0.125, 1, fa.FA_BF16, stream)
     assert big == fa.FA_ERR_UNSUPPORTED
+    # fa_bwd's own argument checks come first: null pointers are an argument error at any size.
+    assert fa.fa_bwd_noalloc(0, 0, 0, 0, 0, 0, 0, 0, 0, 64, 64, 1024, 64, 0.125, 1, fa.FA_BF16,
+                             stream) == fa.FA_ERR_INVALID_ARG
 
+    # The backward is deterministic (no atomics), so both entry points give the same bits.  The
+    # third shape has more query tiles (2 x 40 x 3) than SMs: its dQ pass runs persistent CTAs,
+    # which read their per-row vectors from the scratch array over several rounds.
     for (B, H, L, D, causal, dtype) in ((2, 4, 700, 128, True, torch.bfloat16),
-                                        (1, 3, 300, 64, False, torch.float16)):
+                                        (1, 3, 300, 64, False, torch.float16),
+                                        (2, 40, 384, 128, False, torch.bfloat16)):
         w = workloads.custom(B, H, L, D, causal, dtype)
         inp = workloads.make_inputs(w, seed=21)
         q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
@@ -55,6 +53,5 @@ def test_noalloc_matches_workspace_backward_on_consecutive_calls():
             assert st == fa.FA_OK, fa.fa_status_string(st)
             torch.cuda.synchronize(dev)
             assert fa.fa_get_device_status(stream) == fa.FA_OK
-            for got, want in zip((dq, dk, dv), ref):
-                assert torch.isfinite(got.float()).all()
-                assert _rel(got, want) <= GRAD_REL_FRO
+            for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+                assert torch.equal(got, want), (B, H, L, D, name)

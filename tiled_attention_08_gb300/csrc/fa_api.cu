@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cfloat>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -143,6 +144,21 @@ fa_status check_shape(int B, int H, int L, int D, float scale, int causal, int d
 
 }  // namespace
 
+void trace_disarm() { t_trace_pairs = 0; }
+
+int bwd_check_args(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, const void* dq, const void* dk, const void* dv, int B, int H,
+                   int L, int D, float scale, int causal, int dtype, size_t* ws_need) {
+    Shape sh;
+    *ws_need = 0;
+    fa_status st = check_shape(B, H, L, D, scale, causal, dtype, &sh);
+    if (st != FA_OK) return st;
+    if (sh.empty) return FA_OK;
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    *ws_need = 2u * (size_t)sh.BH * (size_t)sh.Lpad * 4u;
+    return FA_OK;
+}
+
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s);
 
 namespace {
@@ -230,7 +246,13 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     p.BH = sh.BH;
     p.n_tiles = sh.n_tiles;
     p.group = schedule_group(sh.BH, L, D);
-    p.scale_log2 = scale * 1.4426950408889634f;
+    // The softmax takes the row maximum of the stored S, so it must work with a non-negative
+    // multiplier: a negative scale is moved into the S contraction as an exact sign flip.  The
+    // multiplier is at least the smallest normal float, so that a masked logit (-inf) stays
+    // -inf; for scale = 0 every visible logit times it is below 2^-100 in magnitude and exp2
+    // returns exactly 1, the uniform softmax that scale 0 defines.
+    p.scale_log2 = std::fmax(std::fabs(scale) * 1.4426950408889634f, FLT_MIN);
+    p.s_negate = scale < 0.0f ? kIdescNegateA : 0u;
     p.status = status_ptr();
     p.timeout_ns = g_timeout_ns.load();
     if (!p.status) return FA_ERR_CUDA;

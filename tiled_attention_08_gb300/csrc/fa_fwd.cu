@@ -31,7 +31,10 @@
 // issue order) it never overwrites a P still being read, and once the softmax sees S_t(j+1)
 // every PV before it has finished: O_t may be rescaled in place with no further wait.
 //
-// Online softmax in the log2 domain: y = s * scale * log2(e).  The running reference max m
+// Online softmax in the log2 domain: y = s * |scale| * log2(e), where s is the stored S.  For a
+// negative scale the S contraction runs with its A operand negated (an exact sign flip set in
+// the instruction descriptor), so s * |scale| = (Q K^T) * scale for either sign and the row
+// maximum of the stored S is always the row maximum of the logits.  The running reference max m
 // is only raised when a tile's max exceeds it by more than kRescaleThreshold (2^8 headroom
 // for P), so O is rescaled rarely; the result is unchanged because O and the running sum
 // always share the same reference.  LSE = (m + log2(l)) * ln(2).
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
                     mma_ss_w(tmem + C::kTmS + 128 * t, sdesc_advance(qd, off), sdesc_advance(kd, off),
-                           C::kIdescS, kk > 0 ? 1u : 0u);
+                           C::kIdescS | p.s_negate, kk > 0 ? 1u : 0u);
                 }
                 mma_commit_w(&bar_sf[t]);
             };
@@ -312,7 +315,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
                     mma_ss_w(tmem + C::kTmS + 128 * t, sdesc_advance(qd, off), sdesc_advance(kd, off),
-                           C::kIdescS, kk > 0 ? 1u : 0u);
+                           C::kIdescS | p.s_negate, kk > 0 ? 1u : 0u);
                 }
                 mma_commit_w(&bar_sf[t]);
             };

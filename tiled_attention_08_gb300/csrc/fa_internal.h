@@ -43,7 +43,8 @@ struct FwdParams {
     int BH;
     int n_tiles;        // ceil(L / 128)
     int group;          // heads per schedule group (tile_coords)
-    float scale_log2;   // scale * log2(e)
+    float scale_log2;   // |scale| * log2(e)
+    uint32_t s_negate;  // kIdescNegateA when scale < 0 (S is computed as -Q K^T), else 0
     int* status;        // device status word
     uint64_t timeout_ns;
 };
@@ -73,6 +74,15 @@ struct BwdParams {
     int* status;
     uint64_t timeout_ns;
 };
+
+// Host-side helpers of the C-ABI layer shared with the other entry-point units.
+// Consumes the fa_trace_next_call arming of the calling thread (every public call ends so).
+void trace_disarm();
+// fa_bwd's checks of sizes, flags and null pointers (the workspace excepted), in fa_bwd's
+// order; on FA_OK (an int fa_status) *ws_need is the workspace the shape needs (0: empty).
+int bwd_check_args(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, const void* dq, const void* dk, const void* dv, int B, int H,
+                   int L, int D, float scale, int causal, int dtype, size_t* ws_need);
 
 // Launchers (one per kernel unit).  Return the launch error, if any.
 cudaError_t launch_fwd(const FwdParams& p, int D, bool bf16, bool causal, cudaStream_t s);

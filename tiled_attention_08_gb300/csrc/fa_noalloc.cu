@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "../../include/fa.h"
+#include "fa_internal.h"
 
 namespace {
 
@@ -47,18 +48,26 @@ fa_status scratch_address(void** out) {
     return FA_OK;
 }
 
+// Consumes a fa_trace_next_call arming on every way out, as fa_bwd itself does.
+struct DisarmOnExit {
+    ~DisarmOnExit() { fa::trace_disarm(); }
+};
+
 }  // namespace
 
 extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                                     const void* dout, const float* lse, void* dq, void* dk,
                                     void* dv, int B, int H, int L, int D, float scale, int causal,
                                     int dtype, void* stream) {
-    const size_t need = fa_bwd_workspace_bytes(B, H, L, D);
-    if (need == 0)  // empty problem or invalid sizes: fa_bwd reports which, touching nothing
-        return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, nullptr, 0, B, H, L, D, scale, causal,
-                      dtype, stream);
+    DisarmOnExit disarm;
+    // fa_bwd's own checks first (sizes, flags, null pointers), so a call that fa_bwd would
+    // refuse gets fa_bwd's status whatever its size.
+    size_t need = 0;
+    const int chk = fa::bwd_check_args(q, k, v, o, dout, lse, dq, dk, dv, B, H, L, D, scale,
+                                       causal, dtype, &need);
+    if (chk != FA_OK) return static_cast<fa_status>(chk);
+    if (need == 0) return FA_OK;                          // empty problem: nothing to do
     if (need > kScratchBytes) return FA_ERR_UNSUPPORTED;  // larger than the fixed scratch
-    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
     void* scratch = nullptr;
     const fa_status st = scratch_address(&scratch);
     if (st != FA_OK) return st;

@@ -290,6 +290,10 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool a
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction-descriptor bit that negates the A operand (D = -A*B (+ D)); negation of a
+// 16-bit value is exact, so the product is the exact negative of the plain one.
+constexpr uint32_t kIdescNegateA = 1u << 13;
+
 // D[tmem] (+)= A * B for one K=16 slice: mma_ss_w reads A and B from shared memory (via their
 // descriptors), mma_ts_w reads A from TMEM (8 columns: two 16-bit values per 32-bit column, one
 // row per lane).  Warp-converged: every lane of the warp executes the call with the same

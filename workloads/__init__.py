@@ -31,10 +31,17 @@ class Workload:
     dtype: torch.dtype
     backward: bool = True
     row_scaled: bool = False
+    scale_value: float | None = None  # None: the usual 1/sqrt(D)
 
     @property
     def scale(self) -> float:
-        return 1.0 / math.sqrt(self.D)
+        return 1.0 / math.sqrt(self.D) if self.scale_value is None else float(self.scale_value)
+
+    @property
+    def plain_inputs(self) -> bool:
+        """True for i.i.d. N(0,1) inputs at the usual 1/sqrt(D) scale: the setting the stated
+        O error bounds are quoted for."""
+        return not self.row_scaled and self.scale_value is None
 
     @property
     def dtype_name(self) -> str:
@@ -62,9 +69,9 @@ WORKLOADS = {
 
 
 def custom(B: int, H: int, L: int, D: int, causal: bool, dtype: torch.dtype,
-           row_scaled: bool = False) -> Workload:
+           row_scaled: bool = False, scale: float | None = None) -> Workload:
     return Workload(f"custom_B{B}_H{H}_L{L}_D{D}", B, H, L, D, causal, dtype,
-                    row_scaled=row_scaled)
+                    row_scaled=row_scaled, scale_value=scale)
 
 
 def shrink(w: Workload, B: int | None = None, H: int | None = None,
