@@ -4,13 +4,15 @@ Tolerances are the ones the method's target states for 16-bit inputs with fp32 a
 O max-abs <= 1e-2 and mean-abs <= 1e-3 (N(0,1) inputs), LSE max-abs <= 1e-3, and dQ/dK/dV
 relative Frobenius error <= 2e-2.
 
-For i.i.d. N(0,1) inputs at the usual 1/sqrt(D) scale (``Workload.plain_inputs``) the O bounds
-are asserted on the raw error |O_gpu - O_ref|, exactly as stated.  Other inputs (row-scaled
-queries, stretched keys, scales far from 1/sqrt(D)) make the softmax peaked, so |O| reaches
-about 4, where the exact result stored in 16 bits is already off by up to half an ulp (0.0078
-in bf16 for |O| in [2,4)).  There the bounds apply to the error beyond that unavoidable
-rounding: per element excess = max(0, |O_gpu - O_ref| - ulp16(O_ref) / 2), max(excess) <= 1e-2
-and mean(excess) <= 1e-3; the raw errors are reported alongside.
+For i.i.d. N(0,1) inputs at the usual 1/sqrt(D) scale (``Workload.plain_inputs``) and at least
+128 keys -- every configured workload -- the O bounds are asserted on the raw error
+|O_gpu - O_ref|, exactly as stated.  Elsewhere |O| is of order 1 or more: with a handful of keys
+O averages only a few rows of V, and row-scaled queries, stretched keys or scales far above
+1/sqrt(D) make the softmax peaked, so |O| reaches about 4.  There the exact result stored in 16
+bits is already off by up to half an ulp (0.0078 in bf16 for |O| in [2,4); about 1e-3 on
+average at |O| ~ 1), so the bounds apply to the error beyond that unavoidable rounding: per
+element excess = max(0, |O_gpu - O_ref| - ulp16(O_ref) / 2), max(excess) <= 1e-2 and
+mean(excess) <= 1e-3; the raw errors are reported alongside.
 """
 import numpy as np
 import pytest
@@ -83,10 +85,10 @@ def f64(t):
 def check_head(oracle, w, inp, out, b, h, backward=True, raw_o=None):
     """Compares one (b,h) head of the GPU result with the oracle; returns the error summary.
 
-    ``raw_o`` (default: ``w.plain_inputs``) selects the raw O bound; pass False when the test
-    has reshaped plain inputs so that the softmax is peaked."""
+    ``raw_o`` (default: plain inputs with L >= 128) selects the raw O bound; pass False when
+    the test has reshaped plain inputs so that the softmax is peaked."""
     if raw_o is None:
-        raw_o = w.plain_inputs
+        raw_o = w.plain_inputs and w.L >= 128
     q, k, v = (f64(inp[n][b, h]) for n in ("q", "k", "v"))
     o_ref, lse_ref = oracle.forward(q, k, v, w.scale, w.causal)
     o = f64(out["o"][b, h])
