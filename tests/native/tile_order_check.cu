@@ -1,6 +1,7 @@
 // Host-side check of the kernels' tile schedule (tile_coords): every (head, tile) is visited
-// exactly once, and inside each head group the tiles come heaviest first; and of the persistent
-// round order (persistent_tile): every tile id taken exactly once.
+// exactly once, and inside each head group the tiles come heaviest first; of the persistent
+// round order (persistent_tile): every tile id taken exactly once; and of the grid rules of the
+// dQ pass and the forward (dq_grid, fwd_grid).
 #include <cstdio>
 #include <vector>
 
@@ -102,6 +103,25 @@ int main() {
         if (got != c[4]) {
             std::printf("FAIL dq_grid(%d,%d,%d,%d) = %d, want %d\n", c[0], c[1], c[2], c[3], got,
                         c[4]);
+            ++failures;
+        }
+    }
+    // The forward's grid over query-tile pairs: {n_pairs, n_tiles, BH, causal, n_sm, expected}.
+    const int fcases[][6] = {{16, 32, 256, 1, 152, 152},    // B8 H32 L4096 causal: mean 17
+                             {8, 16, 32, 1, 152, 152},      // B1 H32 L2048 causal: mean 9
+                             {64, 128, 16, 1, 152, 1024},   // B1 H16 L16384 causal: mean 65
+                             {2, 4, 512, 0, 152, 152},      // B16 H32 L512: mean 4
+                             {16, 32, 64, 0, 152, 152},     // non-causal L4096: mean 32 (limit)
+                             {17, 33, 64, 0, 152, 1088},    // non-causal, mean 33
+                             {31, 62, 64, 1, 152, 152},     // causal, mean 32
+                             {32, 63, 64, 1, 152, 2048},    // causal, mean 32.5
+                             {1, 1, 1, 0, 152, 1},          // fewer pairs than SMs
+                             {16, 32, 256, 1, 0, 4096}};    // SM count unknown
+    for (const auto& c : fcases) {
+        const int got = fa::fwd_grid(c[0], c[1], c[2], c[3] != 0, c[4]);
+        if (got != c[5]) {
+            std::printf("FAIL fwd_grid(%d,%d,%d,%d,%d) = %d, want %d\n", c[0], c[1], c[2], c[3],
+                        c[4], got, c[5]);
             ++failures;
         }
     }

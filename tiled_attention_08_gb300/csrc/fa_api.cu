@@ -146,6 +146,19 @@ fa_status check_shape(int B, int H, int L, int D, float scale, int causal, int d
 
 void trace_disarm() { t_trace_pairs = 0; }
 
+int sm_count() {
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        cache[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 int bwd_check_args(const void* q, const void* k, const void* v, const void* o, const void* dout,
                    const float* lse, const void* dq, const void* dk, const void* dv, int B, int H,
                    int L, int D, float scale, int causal, int dtype, size_t* ws_need) {

@@ -42,8 +42,6 @@
 // causal (16.5 key tiles per query tile on average) 1.205 ms one CTA per tile, 1.109
 // persistent; B1 H16 L16384 D64 causal (64.5) 0.688 one CTA per tile, 0.715 persistent (0.722
 // with the persistent kernel launched one CTA per tile).
-#include <atomic>
-
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 #include "fa_sched.h"
@@ -741,21 +739,6 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
         tc_fence_after_sync();
         tmem_dealloc(tmem, C::kTmemCols);
     }
-}
-
-// Number of SMs of the current device (looked up once per device); 0 if unknown.
-int sm_count() {
-    constexpr int kMaxDevices = 64;
-    static std::atomic<int> cache[kMaxDevices];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-    int n = cache[dev].load(std::memory_order_relaxed);
-    if (n == 0) {
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return 0;
-        cache[dev].store(n, std::memory_order_relaxed);
-    }
-    return n;
 }
 
 template <int D, bool BF16, bool CAUSAL>

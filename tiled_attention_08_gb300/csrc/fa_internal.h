@@ -78,6 +78,8 @@ struct BwdParams {
 // Host-side helpers of the C-ABI layer shared with the other entry-point units.
 // Consumes the fa_trace_next_call arming of the calling thread (every public call ends so).
 void trace_disarm();
+// Number of SMs of the current device (looked up once per device index); 0 if unknown.
+int sm_count();
 // fa_bwd's checks of sizes, flags and null pointers (the workspace excepted), in fa_bwd's
 // order; on FA_OK (an int fa_status) *ws_need is the workspace the shape needs (0: empty).
 int bwd_check_args(const void* q, const void* k, const void* v, const void* o, const void* dout,

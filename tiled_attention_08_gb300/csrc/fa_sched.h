@@ -13,15 +13,28 @@ __host__ __device__ __forceinline__ int persistent_tile(int round, int cta, int 
     return id < (long long)total ? (int)id : -1;
 }
 
-// Grid of the dQ pass.  Persistent (one CTA per SM) when query tiles see at most kPersistMaxKv
-// key tiles on average and there are more tiles than SMs; otherwise one CTA per tile.  The
-// fixed cost of a CTA is worth hiding only for short rows; for long rows the hardware's own
-// block scheduling balances the causal tiles better than fixed rounds.
+// Grid of a pass over `items` work items that see `mean_kv2` / 2 key tiles on average.
+// Persistent (one CTA per SM) when the items see at most kPersistMaxKv key tiles on average and
+// there are more items than SMs; otherwise one CTA per item.  The fixed cost of a CTA is worth
+// hiding only for short rows; for long rows the hardware's own block scheduling balances the
+// causal items better than fixed rounds.
 constexpr int kPersistMaxKv = 32;
+__host__ __device__ __forceinline__ int persistent_grid(int items, int mean_kv2, int n_sm) {
+    return (n_sm > 0 && n_sm < items && mean_kv2 <= 2 * kPersistMaxKv) ? n_sm : items;
+}
+
+// Grid of the dQ pass: one item per query tile, which sees tile+1 key tiles under the causal
+// mask (mean (n_tiles+1)/2) and every key tile otherwise.
 __host__ __device__ __forceinline__ int dq_grid(int n_tiles, int BH, bool causal, int n_sm) {
-    const int total = n_tiles * BH;
-    const int mean_kv2 = causal ? n_tiles + 1 : 2 * n_tiles;  // twice the mean
-    return (n_sm > 0 && n_sm < total && mean_kv2 <= 2 * kPersistMaxKv) ? n_sm : total;
+    return persistent_grid(n_tiles * BH, causal ? n_tiles + 1 : 2 * n_tiles, n_sm);
+}
+
+// Grid of the forward: one item per pair of query tiles (2p, 2p+1), which sees
+// min(2p+2, n_tiles) key tiles under the causal mask (mean about n_tiles/2 + 1) and every key
+// tile otherwise.
+__host__ __device__ __forceinline__ int fwd_grid(int n_pairs, int n_tiles, int BH, bool causal,
+                                                 int n_sm) {
+    return persistent_grid(n_pairs * BH, causal ? n_tiles + 2 : 2 * n_tiles, n_sm);
 }
 
 }  // namespace fa
