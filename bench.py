@@ -461,9 +461,11 @@ L2_BYTES = 129 * 2**20  # GB300 L2
 
 def _time_config(w, dev, peaks):
     """Times one workload's fa_fwd + fa_bwd through the C ABI with every kernel bracketed by
-    CUDA events, sampling clocks meanwhile.  Inputs that fit in L2 get an L2 flush (a write of
-    a 256 MiB buffer, outside the kernels' events) before every step, so each step starts cold.
-    The step count is chosen from the warm-up so the timed region lasts about half a second."""
+    CUDA events, sampling clocks meanwhile.  Inputs that fit in L2 get an L2 flush before every
+    step, outside the kernels' events: a write of a 256 MiB buffer, then a read of another one,
+    so each step starts with none of its data in L2 and with no dirty lines left for its own
+    kernels to write back.  The step count is chosen from the warm-up so the timed region lasts
+    about half a second."""
     import torch
     import tiled_attention_08_gb300 as fa
     import workloads
@@ -481,11 +483,13 @@ def _time_config(w, dev, peaks):
     sh = stream.cuda_stream
     flush = None
     if q.numel() * q.element_size() < L2_BYTES:
-        flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+        flush = (torch.empty(256 * 2**20, dtype=torch.uint8, device=dev),
+                 torch.ones(64 * 2**20, dtype=torch.float32, device=dev))
 
     def step(ev=None):
         if flush is not None:
-            flush.fill_(1)
+            flush[0].fill_(1)
+            flush[1].sum()
         if ev is not None:
             fa.fa_trace_next_call([ev[0].cuda_event, ev[1].cuda_event], 1)
         st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
@@ -538,7 +542,8 @@ def _time_config(w, dev, peaks):
     return {
         "B": B, "H": H, "L": L, "D": D, "causal": w.causal, "dtype": w.dtype_name,
         "row_scaled": w.row_scaled, "steps": steps,
-        "l2": "flushed before every step" if flush is not None else "inputs larger than L2",
+        "l2": ("flushed before every step (256 MiB written, then 256 MiB read)"
+               if flush is not None else "inputs larger than L2"),
         "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4),
         "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2),
         "fwd_bwd_tflops": round(tot_flops / ((fwd_ms + bwd_ms) * 1e-3) / 1e12, 2),
