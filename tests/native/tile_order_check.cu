@@ -1,7 +1,7 @@
 // Host-side check of the kernels' tile schedule (tile_coords): every (head, tile) is visited
 // exactly once, and inside each head group the tiles come heaviest first; of the persistent
 // round order (persistent_tile): every tile id taken exactly once; and of the grid rules of the
-// dQ pass and the forward (dq_grid, fwd_grid).
+// dQ pass, the dK/dV pass and the forward (dq_grid, dkdv_grid, fwd_grid).
 #include <cstdio>
 #include <vector>
 
@@ -102,6 +102,26 @@ int main() {
         const int got = fa::dq_grid(c[0], c[1], c[2] != 0, c[3]);
         if (got != c[4]) {
             std::printf("FAIL dq_grid(%d,%d,%d,%d) = %d, want %d\n", c[0], c[1], c[2], c[3], got,
+                        c[4]);
+            ++failures;
+        }
+    }
+    // The dK/dV pass: persistent only up to a mean of 12 query tiles per key tile.
+    const int kcases[][5] = {{32, 256, 1, 152, 8192},   // B8 H32 L4096 causal: mean 16.5
+                             {16, 32, 1, 152, 152},     // B1 H32 L2048 causal: mean 8.5
+                             {128, 16, 1, 152, 2048},   // B1 H16 L16384 causal: mean 64.5
+                             {4, 512, 0, 152, 152},     // B16 H32 L512: mean 4
+                             {8, 512, 0, 152, 152},     // B16 H32 L1024: mean 8
+                             {12, 64, 0, 152, 152},     // non-causal, mean 12 (limit)
+                             {13, 64, 0, 152, 832},     // non-causal, mean 13
+                             {23, 64, 1, 152, 152},     // causal, mean 12
+                             {24, 64, 1, 152, 1536},    // causal, mean 12.5
+                             {1, 1, 0, 152, 1},         // fewer tiles than SMs
+                             {4, 512, 0, 0, 2048}};     // SM count unknown
+    for (const auto& c : kcases) {
+        const int got = fa::dkdv_grid(c[0], c[1], c[2] != 0, c[3]);
+        if (got != c[4]) {
+            std::printf("FAIL dkdv_grid(%d,%d,%d,%d) = %d, want %d\n", c[0], c[1], c[2], c[3], got,
                         c[4]);
             ++failures;
         }

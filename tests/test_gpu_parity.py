@@ -36,10 +36,11 @@ def test_small_shapes_full_tensors(oracle_mod, L, D, causal, dtype):
 
 @pytest.mark.parametrize("L,D,causal", [(L, D, c) for L in (377, 384) for D in (64, 128)
                                          for c in (False, True)])
-def test_persistent_dq_rounds(oracle_mod, L, D, causal):
-    """More query tiles (2 x 40 heads x 3) than SMs, with few key tiles each: the dQ pass runs
-    its persistent form, each CTA taking tiles in two rounds; the tile order gives every head
-    tiles in both rounds, so each sampled head crosses the hand-offs between tiles."""
+def test_persistent_rounds(oracle_mod, L, D, causal):
+    """More work items than SMs (2 x 40 heads x 3 query or key tiles, 2 x 40 x 2 query-tile
+    pairs) with short rows: the forward, the dK/dV pass and the dQ pass all run their persistent
+    forms, each CTA taking items in more than one round; the item order gives every head items
+    in several rounds, so each sampled head crosses the hand-offs between items."""
     n_tiles = (L + 127) // 128
     total = 2 * 40 * n_tiles
     assert total > torch.cuda.get_device_properties(0).multi_processor_count
