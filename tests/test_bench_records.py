@@ -60,13 +60,15 @@ def test_sha_covers_kernel_and_shared_files(bench_copy, edited):
 
 def test_sha_covers_headers_the_kernel_includes(bench_copy):
     bench, tmp = bench_copy
-    # The dQ pass includes the persistent-schedule header; the other kernels do not.
+    # The three attention passes include the persistent-schedule header; the preprocess
+    # kernel does not.
     before = {k: bench.kernel_sha(k) for k in bench.KERNEL_SOURCES}
     path = tmp / "tiled_attention_08_gb300" / "csrc" / "fa_sched.h"
     path.write_text(path.read_text() + "\n// edited\n")
     after = {k: bench.kernel_sha(k) for k in bench.KERNEL_SOURCES}
-    assert after["bwd_dq"] != before["bwd_dq"]
-    assert after["bwd_dkdv"] == before["bwd_dkdv"] and after["fa_fwd"] == before["fa_fwd"]
+    for k in ("fa_fwd", "bwd_dkdv", "bwd_dq"):
+        assert after[k] != before[k], k
+    assert after["bwd_pre"] == before["bwd_pre"]
 
 
 def test_record_used_only_while_sources_match(bench_copy):
