@@ -55,13 +55,14 @@ def _load():
             lib = ctypes.CDLL(_SO)
             dp = ctypes.POINTER(ctypes.c_double)
             L = ctypes.c_long
-            lib.oracle_fwd_f64.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, ctypes.c_double,
+            lib.oracle_fwd_f64.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, ctypes.c_double,
                                            ctypes.c_int, L]
             lib.oracle_fwd_f64.restype = ctypes.c_int
-            lib.oracle_bwd_f64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, L, L, L, L,
+            lib.oracle_bwd_f64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, L, L, L, L, L,
                                            ctypes.c_double, ctypes.c_int, L]
             lib.oracle_bwd_f64.restype = ctypes.c_int
-            lib.oracle_probs_f64.argtypes = [dp, dp, dp, L, L, ctypes.c_double, ctypes.c_int]
+            lib.oracle_probs_f64.argtypes = [dp, dp, dp, L, L, L, ctypes.c_double,
+                                             ctypes.c_int]
             lib.oracle_probs_f64.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
@@ -91,17 +92,27 @@ def _as4d(a: np.ndarray) -> tuple[np.ndarray, bool]:
     return a, False
 
 
+def _check_qkv(q, k, v, extra=()):
+    if k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q [B,H,Lq,D] and k, v [B,H,Lk,D] must agree in B, H and D")
+    for a in extra:
+        if a.shape != q.shape:
+            raise ValueError("dO must have the shape of q")
+
+
 def forward(q, k, v, scale: float, causal: bool, block_doubles: int = 0):
-    """O [B,H,L,D] and LSE [B,H,L] (natural log) in fp64.  Also accepts [L,D] inputs."""
+    """O [B,H,Lq,D] and LSE [B,H,Lq] (natural log) in fp64 for q [B,H,Lq,D] and k, v
+    [B,H,Lk,D] (Lq may differ from Lk; causal rows are aligned to the end of the keys).  Also
+    accepts [L,D] inputs."""
     q, sq = _as4d(_f64(q))
     k, _ = _as4d(_f64(k))
     v, _ = _as4d(_f64(v))
-    if not (q.shape == k.shape == v.shape):
-        raise ValueError("q, k, v must have the same shape")
-    B, H, L, D = q.shape
+    _check_qkv(q, k, v)
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
     o = np.empty_like(q)
-    lse = np.empty((B, H, L), dtype=np.float64)
-    rc = _load().oracle_fwd_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, L, D,
+    lse = np.empty((B, H, Lq), dtype=np.float64)
+    rc = _load().oracle_fwd_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Lq, Lk, D,
                                 float(scale), int(bool(causal)), int(block_doubles))
     if rc != 0:
         raise RuntimeError(f"oracle_fwd_f64 failed with code {rc}")
@@ -111,20 +122,21 @@ def forward(q, k, v, scale: float, causal: bool, block_doubles: int = 0):
 
 
 def backward(q, k, v, do, scale: float, causal: bool, block_doubles: int = 0):
-    """dQ, dK, dV [B,H,L,D] and Delta [B,H,L] in fp64.  Also accepts [L,D] inputs."""
+    """dQ [B,H,Lq,D], dK, dV [B,H,Lk,D] and Delta [B,H,Lq] in fp64.  Also accepts [L,D]
+    inputs."""
     q, sq = _as4d(_f64(q))
     k, _ = _as4d(_f64(k))
     v, _ = _as4d(_f64(v))
     do, _ = _as4d(_f64(do))
-    if not (q.shape == k.shape == v.shape == do.shape):
-        raise ValueError("q, k, v, do must have the same shape")
-    B, H, L, D = q.shape
+    _check_qkv(q, k, v, (do,))
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
     dq = np.empty_like(q)
-    dk = np.empty_like(q)
-    dv = np.empty_like(q)
-    delta = np.empty((B, H, L), dtype=np.float64)
+    dk = np.empty_like(k)
+    dv = np.empty_like(k)
+    delta = np.empty((B, H, Lq), dtype=np.float64)
     rc = _load().oracle_bwd_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
-                                _ptr(delta), B, H, L, D, float(scale), int(bool(causal)),
+                                _ptr(delta), B, H, Lq, Lk, D, float(scale), int(bool(causal)),
                                 int(block_doubles))
     if rc != 0:
         raise RuntimeError(f"oracle_bwd_f64 failed with code {rc}")
@@ -134,12 +146,13 @@ def backward(q, k, v, do, scale: float, causal: bool, block_doubles: int = 0):
 
 
 def probs(q, k, scale: float, causal: bool) -> np.ndarray:
-    """The probability matrix P [L,L] of one head (q, k: [L,D])."""
+    """The probability matrix P [Lq,Lk] of one head (q: [Lq,D], k: [Lk,D])."""
     q = _f64(q)
     k = _f64(k)
-    L, D = q.shape
-    p = np.empty((L, L), dtype=np.float64)
-    rc = _load().oracle_probs_f64(_ptr(q), _ptr(k), _ptr(p), L, D, float(scale),
+    Lq, D = q.shape
+    Lk = k.shape[0]
+    p = np.empty((Lq, Lk), dtype=np.float64)
+    rc = _load().oracle_probs_f64(_ptr(q), _ptr(k), _ptr(p), Lq, Lk, D, float(scale),
                                   int(bool(causal)))
     if rc != 0:
         raise RuntimeError(f"oracle_probs_f64 failed with code {rc}")

@@ -10,9 +10,10 @@
  *
  *   "FlashAttention principles and engineering practice", section 2.1 (memory access):
  *   the standard implementation forms attn = (q k^T) * scale, applies softmax over the
- *   last dimension and multiplies by v.  Per (b,h) head, with Q,K,V of shape [L,D]:
+ *   last dimension and multiplies by v.  Per (b,h) head, with Q of shape [Lq,D] and K, V of
+ *   shape [Lk,D]:
  *
- *     S   = scale * Q K^T                      (S_ij = -inf for j > i when causal)
+ *     S   = scale * Q K^T                      (S_ij = -inf for j > i + Lk - Lq when causal)
  *     m_i = max_j S_ij
  *     P   = exp(S - m) / rowsum(exp(S - m))    (materialised, fp64)
  *     O   = P V
@@ -30,13 +31,24 @@
  *     dQ = scale * dS K
  *     dK = scale * dS^T Q
  *
- * Masked entries (causal, j > i) have P_ij = exp(-inf) = 0 exactly, so they are simply
- * not visited: every sum below runs over the visible keys j < n_i, n_i = i+1 (causal)
- * or L.  Rows of S and P are materialised one row block at a time; a block holds every
- * row of the head whenever R*L doubles fit the block budget, so for test sizes the whole
- * L x L matrix is materialised at once.
+ * Queries and keys may differ in length (Lq != Lk: a block of queries attending to a longer
+ * or shorter key sequence, as the flash_attn_func interface allows, "FlashAttention data-flow
+ * optimisation", section 4.1, step 3).  The pages do not say how the causal mask lines up
+ * then; the reading taken here is that the queries are the LAST Lq positions of the sequence
+ * whose keys are given (a block of new tokens after a cache of earlier ones), so query i sits
+ * at position i + Lk - Lq and sees key j iff j <= i + Lk - Lq.  For Lq = Lk this is the usual
+ * j <= i.  When Lq > Lk the first Lq - Lk query rows see no key at all: their softmax is over
+ * an empty set, and the oracle gives them O = 0, LSE = -inf (the log of an empty sum) and
+ * dQ = 0; they contribute nothing to dK and dV.
  *
- * Layout: every tensor is contiguous [B,H,L,D] (LSE, Delta: [B,H,L]) in fp64.
+ * Masked entries have P_ij = exp(-inf) = 0 exactly, so they are simply not visited: every
+ * sum below runs over the visible keys j < n_i, n_i = clamp(i + 1 + Lk - Lq, 0, Lk) (causal)
+ * or Lk.  Rows of S and P are materialised one row block at a time; a block holds every row
+ * of the head whenever R*Lk doubles fit the block budget, so for test sizes the whole
+ * Lq x Lk matrix is materialised at once.
+ *
+ * Layout: every tensor is contiguous [B,H,L,D] (L = Lq for Q, O, dO, dQ and Lk for K, V,
+ * dK, dV; LSE, Delta: [B,H,Lq]) in fp64.
  * Parallelism: OpenMP over rows (and over key columns for dK/dV) inside one head.
  */
 #include <math.h>
@@ -61,12 +73,19 @@ int oracle_num_threads(void) {
 #endif
 }
 
-static long visible_keys(long i, long L, int causal) { return causal ? i + 1 : L; }
+/* Keys visible to query row i: all Lk, or (causal) those at positions <= i + Lk - Lq. */
+static long visible_keys(long i, long Lq, long Lk, int causal) {
+    if (!causal) return Lk;
+    long n = i + 1 + (Lk - Lq);
+    if (n < 0) n = 0;
+    if (n > Lk) n = Lk;
+    return n;
+}
 
 /* Row i of S (scaled logits), written into s[0..n), and returns n. */
-static long logits_row(const double* Q, const double* K, long i, long L, long D, double scale,
-                       int causal, double* s) {
-    long n = visible_keys(i, L, causal);
+static long logits_row(const double* Q, const double* K, long i, long Lq, long Lk, long D,
+                       double scale, int causal, double* s) {
+    long n = visible_keys(i, Lq, Lk, causal);
     const double* q = Q + i * D;
     for (long j = 0; j < n; ++j) {
         const double* k = K + j * D;
@@ -77,8 +96,10 @@ static long logits_row(const double* Q, const double* K, long i, long L, long D,
     return n;
 }
 
-/* Turns s[0..n) into the softmax row P in place; returns LSE = m + ln(sum exp(s - m)). */
+/* Turns s[0..n) into the softmax row P in place; returns LSE = m + ln(sum exp(s - m)), or
+ * -inf for an empty row (n = 0). */
 static double softmax_row(double* s, long n) {
+    if (n == 0) return -INFINITY;
     double m = -INFINITY;
     for (long j = 0; j < n; ++j)
         if (s[j] > m) m = s[j];
@@ -99,18 +120,18 @@ static long block_rows(long L, long block_doubles) {
     return r;
 }
 
-/* Forward pass for one head. */
+/* Forward pass for one head: Q, O [Lq,D], K, V [Lk,D], lse [Lq]. */
 static int fwd_head(const double* Q, const double* K, const double* V, double* O, double* lse,
-                    long L, long D, double scale, int causal, long block_doubles) {
-    long R = block_rows(L, block_doubles);
-    double* P = (double*)malloc(sizeof(double) * (size_t)R * (size_t)L);
+                    long Lq, long Lk, long D, double scale, int causal, long block_doubles) {
+    long R = block_rows(Lk, block_doubles);
+    double* P = (double*)malloc(sizeof(double) * (size_t)R * (size_t)(Lk > 0 ? Lk : 1));
     if (!P) return ORACLE_NO_MEMORY;
-    for (long i0 = 0; i0 < L; i0 += R) {
-        long i1 = i0 + R < L ? i0 + R : L;
+    for (long i0 = 0; i0 < Lq; i0 += R) {
+        long i1 = i0 + R < Lq ? i0 + R : Lq;
 #pragma omp parallel for schedule(dynamic, 4)
         for (long i = i0; i < i1; ++i) {
-            double* p = P + (i - i0) * L;
-            long n = logits_row(Q, K, i, L, D, scale, causal, p);
+            double* p = P + (i - i0) * Lk;
+            long n = logits_row(Q, K, i, Lq, Lk, D, scale, causal, p);
             lse[i] = softmax_row(p, n);
             double* o = O + i * D;
             for (long d = 0; d < D; ++d) o[d] = 0.0;
@@ -124,28 +145,30 @@ static int fwd_head(const double* Q, const double* K, const double* V, double* O
     return ORACLE_OK;
 }
 
-/* Backward pass for one head (P recomputed from the definition, nothing cached). */
+/* Backward pass for one head (P recomputed from the definition, nothing cached):
+ * Q, dO, dQ [Lq,D], K, V, dK, dV [Lk,D], delta [Lq]. */
 static int bwd_head(const double* Q, const double* K, const double* V, const double* dO,
-                    double* dQ, double* dK, double* dV, double* delta, long L, long D,
+                    double* dQ, double* dK, double* dV, double* delta, long Lq, long Lk, long D,
                     double scale, int causal, long block_doubles) {
-    long R = block_rows(L, block_doubles / 2);
-    double* P = (double*)malloc(sizeof(double) * (size_t)R * (size_t)L);
-    double* dS = (double*)malloc(sizeof(double) * (size_t)R * (size_t)L);
+    long R = block_rows(Lk, block_doubles / 2);
+    size_t row = (size_t)(Lk > 0 ? Lk : 1);
+    double* P = (double*)malloc(sizeof(double) * (size_t)R * row);
+    double* dS = (double*)malloc(sizeof(double) * (size_t)R * row);
     if (!P || !dS) {
         free(P);
         free(dS);
         return ORACLE_NO_MEMORY;
     }
-    memset(dK, 0, sizeof(double) * (size_t)L * (size_t)D);
-    memset(dV, 0, sizeof(double) * (size_t)L * (size_t)D);
-    for (long i0 = 0; i0 < L; i0 += R) {
-        long i1 = i0 + R < L ? i0 + R : L;
+    memset(dK, 0, sizeof(double) * (size_t)Lk * (size_t)D);
+    memset(dV, 0, sizeof(double) * (size_t)Lk * (size_t)D);
+    for (long i0 = 0; i0 < Lq; i0 += R) {
+        long i1 = i0 + R < Lq ? i0 + R : Lq;
         /* Rows: P, dP, Delta, dS and dQ. */
 #pragma omp parallel for schedule(dynamic, 4)
         for (long i = i0; i < i1; ++i) {
-            double* p = P + (i - i0) * L;
-            double* ds = dS + (i - i0) * L;
-            long n = logits_row(Q, K, i, L, D, scale, causal, p);
+            double* p = P + (i - i0) * Lk;
+            double* ds = dS + (i - i0) * Lk;
+            long n = logits_row(Q, K, i, Lq, Lk, D, scale, causal, p);
             (void)softmax_row(p, n);
             const double* g = dO + i * D;
             double dlt = 0.0;
@@ -168,13 +191,13 @@ static int bwd_head(const double* Q, const double* K, const double* V, const dou
         }
         /* Columns: dV_j += sum_i P_ij dO_i and dK_j += scale * sum_i dS_ij Q_i over this block. */
 #pragma omp parallel for schedule(dynamic, 4)
-        for (long j = 0; j < L; ++j) {
+        for (long j = 0; j < Lk; ++j) {
             double* dv = dV + j * D;
             double* dk = dK + j * D;
             for (long i = i0; i < i1; ++i) {
-                if (causal && j > i) continue; /* P_ij = 0 and dS_ij = 0 */
-                double pij = P[(i - i0) * L + j];
-                double dsij = dS[(i - i0) * L + j];
+                if (j >= visible_keys(i, Lq, Lk, causal)) continue; /* P_ij = 0 and dS_ij = 0 */
+                double pij = P[(i - i0) * Lk + j];
+                double dsij = dS[(i - i0) * Lk + j];
                 const double* g = dO + i * D;
                 const double* q = Q + i * D;
                 for (long d = 0; d < D; ++d) {
@@ -189,18 +212,22 @@ static int bwd_head(const double* Q, const double* K, const double* V, const dou
     return ORACLE_OK;
 }
 
-static int bad_shape(long B, long H, long L, long D) { return B < 0 || H < 0 || L < 0 || D < 1; }
+static int bad_shape(long B, long H, long Lq, long Lk, long D) {
+    return B < 0 || H < 0 || Lq < 0 || Lk < 0 || D < 1;
+}
 
 /*
- * Forward over all heads.  q,k,v: [B,H,L,D]; o: [B,H,L,D]; lse: [B,H,L].
+ * Forward over all heads.  q: [B,H,Lq,D]; k, v: [B,H,Lk,D]; o: [B,H,Lq,D]; lse: [B,H,Lq].
  * block_doubles caps the doubles of one materialised S/P block (<= 0: default).
  */
 int oracle_fwd_f64(const double* q, const double* k, const double* v, double* o, double* lse,
-                   long B, long H, long L, long D, double scale, int causal, long block_doubles) {
-    if (bad_shape(B, H, L, D)) return ORACLE_BAD_ARG;
+                   long B, long H, long Lq, long Lk, long D, double scale, int causal,
+                   long block_doubles) {
+    if (bad_shape(B, H, Lq, Lk, D)) return ORACLE_BAD_ARG;
     for (long bh = 0; bh < B * H; ++bh) {
-        size_t off = (size_t)bh * (size_t)L * (size_t)D;
-        int rc = fwd_head(q + off, k + off, v + off, o + off, lse + (size_t)bh * (size_t)L, L, D,
+        size_t oq = (size_t)bh * (size_t)Lq * (size_t)D;
+        size_t ok = (size_t)bh * (size_t)Lk * (size_t)D;
+        int rc = fwd_head(q + oq, k + ok, v + ok, o + oq, lse + (size_t)bh * (size_t)Lq, Lq, Lk, D,
                           scale, causal, block_doubles);
         if (rc) return rc;
     }
@@ -208,31 +235,34 @@ int oracle_fwd_f64(const double* q, const double* k, const double* v, double* o,
 }
 
 /*
- * Backward over all heads.  Inputs q,k,v,dO: [B,H,L,D]; outputs dq,dk,dv: [B,H,L,D] and
- * delta: [B,H,L] (Delta_i = sum_j P_ij dP_ij).
+ * Backward over all heads.  Inputs q, dO: [B,H,Lq,D], k, v: [B,H,Lk,D]; outputs dq: [B,H,Lq,D],
+ * dk, dv: [B,H,Lk,D] and delta: [B,H,Lq] (Delta_i = sum_j P_ij dP_ij).
  */
 int oracle_bwd_f64(const double* q, const double* k, const double* v, const double* dO,
-                   double* dq, double* dk, double* dv, double* delta, long B, long H, long L,
-                   long D, double scale, int causal, long block_doubles) {
-    if (bad_shape(B, H, L, D)) return ORACLE_BAD_ARG;
+                   double* dq, double* dk, double* dv, double* delta, long B, long H, long Lq,
+                   long Lk, long D, double scale, int causal, long block_doubles) {
+    if (bad_shape(B, H, Lq, Lk, D)) return ORACLE_BAD_ARG;
     for (long bh = 0; bh < B * H; ++bh) {
-        size_t off = (size_t)bh * (size_t)L * (size_t)D;
-        int rc = bwd_head(q + off, k + off, v + off, dO + off, dq + off, dk + off, dv + off,
-                          delta + (size_t)bh * (size_t)L, L, D, scale, causal, block_doubles);
+        size_t oq = (size_t)bh * (size_t)Lq * (size_t)D;
+        size_t ok = (size_t)bh * (size_t)Lk * (size_t)D;
+        int rc = bwd_head(q + oq, k + ok, v + ok, dO + oq, dq + oq, dk + ok, dv + ok,
+                          delta + (size_t)bh * (size_t)Lq, Lq, Lk, D, scale, causal,
+                          block_doubles);
         if (rc) return rc;
     }
     return ORACLE_OK;
 }
 
-/* The full probability matrix P [L,L] of one head (masked entries are 0). */
-int oracle_probs_f64(const double* q, const double* k, double* p, long L, long D, double scale,
-                     int causal) {
-    if (bad_shape(1, 1, L, D)) return ORACLE_BAD_ARG;
-    for (long i = 0; i < L; ++i) {
-        double* row = p + i * L;
-        long n = logits_row(q, k, i, L, D, scale, causal, row);
+/* The full probability matrix P [Lq,Lk] of one head (masked entries are 0; a row that sees
+ * no key is all zeros). */
+int oracle_probs_f64(const double* q, const double* k, double* p, long Lq, long Lk, long D,
+                     double scale, int causal) {
+    if (bad_shape(1, 1, Lq, Lk, D)) return ORACLE_BAD_ARG;
+    for (long i = 0; i < Lq; ++i) {
+        double* row = p + i * Lk;
+        long n = logits_row(q, k, i, Lq, Lk, D, scale, causal, row);
         (void)softmax_row(row, n);
-        for (long j = n; j < L; ++j) row[j] = 0.0;
+        for (long j = n; j < Lk; ++j) row[j] = 0.0;
     }
     return ORACLE_OK;
 }

@@ -19,7 +19,12 @@ What the facts rest on:
   invariants sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i that follow from shift invariance and
   from rows of P summing to one;
 * an independent library implementation of the same operation (torch's CPU
-  scaled_dot_product_attention in fp64, with autograd), for random heads.
+  scaled_dot_product_attention in fp64, with autograd), for random heads;
+* queries and keys of different lengths (Lq != Lk, the flash_attn_func interface of "FlashAttention
+  data-flow optimisation", section 4.1, step 3): with the causal mask the queries are read as the
+  last Lq positions of the key sequence, so a suffix of the queries of a square causal problem
+  must reproduce that problem's rows and gradients exactly; rows that see no key (Lq > Lk) give
+  O = 0, LSE = -inf and dQ = 0.
 """
 from __future__ import annotations
 
@@ -209,6 +214,113 @@ def pin_library_sdpa(impl):
         _close(dv, tv.grad.numpy(), 1e-12, "dV vs torch sdpa autograd")
 
 
+def _zero_early_rows(a, n):
+    b = a.copy()
+    b[:n] = 0.0
+    return b
+
+
+def pin_suffix_queries(impl):
+    """Bottom-right causal alignment: the last Lq queries against all Lk keys are rows
+    [Lk-Lq, Lk) of the square causal problem, and so are their gradients (the early rows of the
+    square problem then carry dO = 0)."""
+    r = _rng(14)
+    Lk, D, scale = 13, 5, 0.55
+    q, k, v, do = (r.standard_normal((Lk, D)) for _ in range(4))
+    for Lq in (1, 4, Lk - 1, Lk):
+        n0 = Lk - Lq
+        for causal in (True, False):
+            o, lse = impl.forward(q[n0:], k, v, scale, causal)
+            o_sq, lse_sq = impl.forward(q, k, v, scale, causal)
+            _close(o, o_sq[n0:], 1e-12, f"O of the last {Lq} queries (causal={causal})")
+            _close(lse, lse_sq[n0:], 1e-12, f"LSE of the last {Lq} queries (causal={causal})")
+            dq, dk, dv, _ = impl.backward(q[n0:], k, v, do[n0:], scale, causal)
+            dq_sq, dk_sq, dv_sq, _ = impl.backward(q, k, v, _zero_early_rows(do, n0), scale, causal)
+            _close(dq, dq_sq[n0:], 1e-12, f"dQ of the last {Lq} queries (causal={causal})")
+            _close(dk, dk_sq, 1e-12, f"dK with only the last {Lq} queries (causal={causal})")
+            _close(dv, dv_sq, 1e-12, f"dV with only the last {Lq} queries (causal={causal})")
+
+
+def pin_more_queries_than_keys(impl):
+    """Lq > Lk, causal: the first Lq - Lk queries see no key (O = 0, LSE = -inf, dQ = 0, no
+    contribution to dK, dV); the last Lk are the square causal problem."""
+    r = _rng(15)
+    Lq, Lk, D, scale = 11, 4, 3, 0.7
+    q, do = r.standard_normal((Lq, D)), r.standard_normal((Lq, D))
+    k, v = r.standard_normal((Lk, D)), r.standard_normal((Lk, D))
+    n0 = Lq - Lk
+    o, lse = impl.forward(q, k, v, scale, True)
+    assert np.all(o[:n0] == 0.0), "O of a row that sees no key"
+    assert np.all(np.isneginf(lse[:n0])), "LSE of a row that sees no key"
+    o_sq, lse_sq = impl.forward(q[n0:], k, v, scale, True)
+    _close(o[n0:], o_sq, 1e-12, "O of the rows that see keys")
+    _close(lse[n0:], lse_sq, 1e-12, "LSE of the rows that see keys")
+    dq, dk, dv, _ = impl.backward(q, k, v, do, scale, True)
+    assert np.all(dq[:n0] == 0.0), "dQ of a row that sees no key"
+    dq_sq, dk_sq, dv_sq, _ = impl.backward(q[n0:], k, v, do[n0:], scale, True)
+    _close(dq[n0:], dq_sq, 1e-12, "dQ of the rows that see keys")
+    _close(dk, dk_sq, 1e-12, "dK with rows that see no key")
+    _close(dv, dv_sq, 1e-12, "dV with rows that see no key")
+    # Non-causal: every row sees every key, whatever the lengths; rows are independent.
+    o, lse = impl.forward(q, k, v, scale, False)
+    for i in (0, n0, Lq - 1):
+        o1, lse1 = impl.forward(q[i:i + 1], k, v, scale, False)
+        _close(o[i:i + 1], o1, 1e-12, "non-causal O row vs a one-row problem")
+        _close(lse[i:i + 1], lse1, 1e-12, "non-causal LSE row vs a one-row problem")
+
+
+def pin_library_sdpa_rect(impl):
+    """Lq != Lk against torch's fp64 CPU scaled_dot_product_attention and its autograd, with the
+    causal mask built explicitly (query i sees key j iff j <= i + Lk - Lq)."""
+    import torch
+    import torch.nn.functional as F
+
+    r = _rng(16)
+    for (Lq, Lk, D, causal, scale) in ((9, 23, 8, True, 0.3), (23, 9, 8, False, 0.3),
+                                       (5, 40, 16, True, 0.2), (17, 17, 4, True, 0.5)):
+        q, do = r.standard_normal((Lq, D)), r.standard_normal((Lq, D))
+        k, v = r.standard_normal((Lk, D)), r.standard_normal((Lk, D))
+        tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+        mask = None
+        if causal:
+            mask = torch.tensor(np.arange(Lk)[None, :] <= np.arange(Lq)[:, None] + (Lk - Lq))
+        to = F.scaled_dot_product_attention(tq[None, None], tk[None, None], tv[None, None],
+                                            attn_mask=mask, scale=scale)[0, 0]
+        to.backward(torch.tensor(do, dtype=torch.float64))
+        o, _ = impl.forward(q, k, v, scale, causal)
+        _close(o, to.detach().numpy(), 1e-12, f"O vs torch sdpa (Lq={Lq}, Lk={Lk})")
+        dq, dk, dv, _ = impl.backward(q, k, v, do, scale, causal)
+        _close(dq, tq.grad.numpy(), 1e-12, f"dQ vs torch sdpa (Lq={Lq}, Lk={Lk})")
+        _close(dk, tk.grad.numpy(), 1e-12, f"dK vs torch sdpa (Lq={Lq}, Lk={Lk})")
+        _close(dv, tv.grad.numpy(), 1e-12, f"dV vs torch sdpa (Lq={Lq}, Lk={Lk})")
+
+
+def pin_finite_differences_rect(impl):
+    """Central differences of sum(O * dO) with Lq != Lk, including rows that see no key."""
+    r = _rng(17)
+    h = 1e-6
+    for (Lq, Lk, D, causal) in ((3, 6, 2, True), (6, 3, 2, True), (4, 7, 3, False)):
+        q, do = r.standard_normal((Lq, D)), r.standard_normal((Lq, D))
+        k, v = r.standard_normal((Lk, D)), r.standard_normal((Lk, D))
+        scale = 0.9
+        dq, dk, dv, _ = impl.backward(q, k, v, do, scale, causal)
+        for name, g in (("q", dq), ("k", dk), ("v", dv)):
+            x = {"q": q, "k": k, "v": v}[name]
+            num = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                args = [{"q": q, "k": k, "v": v}, {"q": q, "k": k, "v": v}]
+                for sgn, a in zip((1.0, -1.0), args):
+                    xs = x.copy()
+                    xs[idx] += sgn * h
+                    a[name] = xs
+                fp = _loss(impl, args[0]["q"], args[0]["k"], args[0]["v"], do, scale, causal)
+                fm = _loss(impl, args[1]["q"], args[1]["k"], args[1]["v"], do, scale, causal)
+                num[idx] = (fp - fm) / (2 * h)
+            err = np.linalg.norm(g - num)
+            assert err <= 1e-6 * max(np.linalg.norm(num), 1.0), \
+                f"d{name} vs finite differences (Lq={Lq}, Lk={Lk}, causal={causal}): {err:.2e}"
+
+
 ALL_PINS = [
     pin_probs_are_distributions,
     pin_single_key,
@@ -221,4 +333,8 @@ ALL_PINS = [
     pin_gradient_invariants,
     pin_zero_queries_backward,
     pin_library_sdpa,
+    pin_suffix_queries,
+    pin_more_queries_than_keys,
+    pin_library_sdpa_rect,
+    pin_finite_differences_rect,
 ]
