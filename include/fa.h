@@ -13,8 +13,9 @@
  * LSE instead of storing the L x L matrix (data-flow page, section 2.2, third layer).
  *
  * Conventions shared by every entry point:
- *  - Tensors are DEVICE pointers to contiguous row-major [B, H, L, D] arrays (LSE: [B, H, L]
- *    fp32), each 16-byte aligned.  q, k, v, o, dO, dq, dk, dv all have the dtype `dtype`.
+ *  - Tensors are DEVICE pointers to row-major [B, H, L, D] arrays (LSE: [B, H, L] fp32), each
+ *    16-byte aligned: contiguous for fa_fwd / fa_bwd, strided (fa_strides) for fa_fwd_ex /
+ *    fa_bwd_ex.  q, k, v, o, dO, dq, dk, dv all have the dtype `dtype`.
  *  - Supported: D in {64, 128}; B, H, L >= 0 (an empty problem returns FA_OK and launches
  *    nothing); causal in {0, 1} (query i sees key j iff j <= i); scale finite, of either sign
  *    or zero ("FlashAttention principles and engineering practice", section 2.1: the scale
@@ -57,11 +58,41 @@ typedef enum {
 typedef enum { FA_BF16 = 0, FA_FP16 = 1 } fa_dtype;
 
 /*
+ * Element strides of one [B, H, L, D] operand whose D elements are contiguous.  The layouts of
+ * the flash_attn_func interface ("FlashAttention data-flow optimisation", section 4.1, step 3:
+ * [B, L, H, D]) and of flash_attn_qkvpacked_func ("AIInfra notes 01: from TFLOPS to
+ * FlashAttention", sections 4.2-4.3: [B, L, 3, H, D]) are both of this form:
+ *     contiguous [B,H,L,D]:   {H*L*D, L*D,  D}
+ *     [B,L,H,D]:              {L*H*D, D,    H*D}
+ *     q/k/v of [B,L,3,H,D]:   {3*L*H*D, D,  3*H*D}, bases at +0, +H*D, +2*H*D elements.
+ * Every stride is a positive multiple of 8 elements (16 bytes: the tensor-copy unit's rule) and
+ * below 2^39; a stride of 0 is accepted for a dimension of size 1.
+ */
+typedef struct {
+    int64_t batch, head, row;
+} fa_strides;
+
+/*
  * Forward.  Writes o [B,H,L,D] (dtype) and lse [B,H,L] (fp32, natural log).
  * Data-flow page, section 2.2 (tiling, streaming softmax, statistics kept for backward).
  */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int L, int D, float scale, int causal, int dtype, void* stream);
+
+/*
+ * Forward with general layouts and lengths: q [B,H,Lq,D], k and v [B,H,Lk,D], o [B,H,Lq,D], each
+ * addressed through its own strides (strides[0..3] = q, k, v, o); lse is contiguous [B,H,Lq].
+ * Lq may differ from Lk.  Under the causal mask the queries are the last Lq positions of the
+ * key sequence (a block of new tokens after Lk - Lq earlier ones): query i sees key j iff
+ * j <= i + Lk - Lq.  A query row that sees no key (only when Lq > Lk) gets O = 0 and
+ * LSE = -inf.  Lq = 0 returns FA_OK with nothing to do; Lk = 0 with Lq > 0 returns
+ * FA_ERR_UNSUPPORTED.  Extents (first to last element) of the outputs must not overlap those of
+ * the inputs or each other.  fa_fwd(..., L, ...) is fa_fwd_ex with Lq = Lk = L and contiguous
+ * strides.
+ */
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const fa_strides* strides, int B, int H, int Lq, int Lk, int D, float scale,
+                    int causal, int dtype, void* stream);
 
 /*
  * Bytes of device workspace fa_bwd needs for this shape: two fp32 vectors per head padded to
@@ -88,6 +119,21 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const float* lse, void* dq, void* dk, void* dv, void* workspace,
                  size_t workspace_bytes, int B, int H, int L, int D, float scale, int causal,
                  int dtype, void* stream);
+
+/*
+ * Backward with general layouts and lengths (see fa_fwd_ex): strides[0..7] = q, k, v, o, dout,
+ * dq, dk, dv; dq has the shape of q, dk and dv that of k.  The workspace is
+ * fa_bwd_workspace_bytes(B, H, Lq, D).  Rows that see no key get dQ = 0.  Lq = Lk = 0 returns
+ * FA_OK; only one of them 0 returns FA_ERR_UNSUPPORTED.  dq, dk and dv may be the three
+ * interleaved parts of one packed [B,L,3,H,D] gradient (Lq = Lk, equal strides, the heads of a
+ * row together, each part's heads ending before the next part's begin); otherwise no two
+ * outputs' extents may overlap, and no output may overlap an input.  fa_bwd is fa_bwd_ex with
+ * Lq = Lk = L and contiguous strides.
+ */
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                    const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                    size_t workspace_bytes, const fa_strides* strides, int B, int H, int Lq,
+                    int Lk, int D, float scale, int causal, int dtype, void* stream);
 
 /* Size of the fixed device scratch array behind fa_bwd_noalloc: 16 MiB. */
 #define FA_BWD_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
@@ -144,11 +190,12 @@ fa_status fa_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
 
 /*
  * Kernel timing trace (the CUDA-event measurement the TFLOP/s figures rest on, per kernel).
- * Arms the next fa_fwd / fa_bwd call made by this host thread: the i-th kernel that call
+ * Arms the next forward or backward call made by this host thread: the i-th kernel that call
  * enqueues is bracketed by cudaEventRecord(events[2*i], stream) and
  * cudaEventRecord(events[2*i+1], stream).  `events` holds n_pairs pairs of cudaEvent_t created
  * by the caller (with timing enabled); kernels beyond n_pairs are not traced.  The next call
- * consumes the arming.  fa_fwd enqueues 1 kernel, fa_bwd 3 (preprocess, dK/dV, dQ).
+ * consumes the arming.  A forward enqueues 1 kernel (2 under the causal mask with Lq > Lk: the
+ * second writes the rows that see no key), a backward 3 (preprocess, dK/dV, dQ).
  */
 fa_status fa_trace_next_call(void* const* events, int n_pairs);
 

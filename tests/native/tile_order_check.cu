@@ -1,7 +1,8 @@
 // Host-side check of the kernels' tile schedule (tile_coords): every (head, tile) is visited
 // exactly once, and inside each head group the tiles come heaviest first; of the persistent
-// round order (persistent_tile): every tile id taken exactly once; and of the grid rules of the
-// dQ pass, the dK/dV pass and the forward (dq_grid, dkdv_grid, fwd_grid).
+// round order (persistent_tile): every tile id taken exactly once; of the tile bounds under the
+// causal mask with Lq != Lk (q_tile_kv, k_tile_q0, tile_masked) against the per-element
+// definition; and of the grid rules of the dQ pass, the dK/dV pass and the forward.
 #include <cstdio>
 #include <vector>
 
@@ -86,57 +87,99 @@ int main() {
             ++failures;
         }
     }
+    // Tile bounds under the causal mask against the per-element definition (query row i sees key
+    // j iff j <= i + Lk - Lq), on square and rectangular shapes with ragged tails.
+    const int shapes[][2] = {{1, 1},     {128, 128}, {129, 129}, {300, 300}, {384, 1000},
+                             {1000, 384}, {5, 700},   {700, 5},   {256, 128}, {128, 256},
+                             {200, 77},  {77, 200},  {513, 129}, {129, 513}};
+    for (const auto& sh : shapes) {
+        const int Lq = sh[0], Lk = sh[1];
+        const int n_q = (Lq + 127) / 128, n_k = (Lk + 127) / 128;
+        for (int causal = 0; causal < 2; ++causal) {
+            for (int qt = 0; qt < n_q; ++qt) {
+                int want_kv = 0;  // key tiles holding a key some row of the tile sees
+                for (int kt = 0; kt < n_k; ++kt) {
+                    bool seen = false, all = true;
+                    for (int i = qt * 128; i < qt * 128 + 128; ++i)
+                        for (int j = kt * 128; j < kt * 128 + 128; ++j) {
+                            const bool vis = i < Lq && j < Lk && (!causal || j <= i + Lk - Lq);
+                            seen = seen || vis;
+                            all = all && vis;
+                        }
+                    if (seen) want_kv = kt + 1;
+                    if (seen && fa::tile_masked(qt, kt, Lq, Lk, causal != 0) == all) {
+                        std::printf("FAIL tile_masked(%d,%d,%d,%d,%d)\n", qt, kt, Lq, Lk, causal);
+                        ++failures;
+                    }
+                    const bool q0_says = qt >= fa::k_tile_q0(kt, Lq, Lk, causal != 0);
+                    if (kt * 128 < Lk && seen != q0_says) {
+                        std::printf("FAIL k_tile_q0(%d,%d,%d,%d) vs qt=%d\n", kt, Lq, Lk, causal,
+                                    qt);
+                        ++failures;
+                    }
+                }
+                if (fa::q_tile_kv(qt, Lq, Lk, causal != 0) != want_kv) {
+                    std::printf("FAIL q_tile_kv(%d,%d,%d,%d) = %d, want %d\n", qt, Lq, Lk, causal,
+                                fa::q_tile_kv(qt, Lq, Lk, causal != 0), want_kv);
+                    ++failures;
+                }
+            }
+        }
+    }
     // The dQ pass's grid: persistent (152 CTAs) for short rows with more tiles than SMs, one
-    // CTA per tile otherwise.  {n_tiles, BH, causal, n_sm, expected}
-    const int gcases[][5] = {{32, 256, 1, 152, 152},    // B8 H32 L4096 causal: mean 16.5
-                             {16, 32, 1, 152, 152},     // B1 H32 L2048 causal: mean 8.5
-                             {128, 16, 1, 152, 2048},   // B1 H16 L16384 causal: mean 64.5
-                             {4, 512, 0, 152, 152},     // B16 H32 L512: mean 4
-                             {32, 64, 0, 152, 152},     // non-causal L4096: mean 32 (limit)
-                             {33, 64, 0, 152, 2112},    // non-causal, mean 33
-                             {63, 64, 1, 152, 152},     // causal, mean 32
-                             {64, 64, 1, 152, 4096},    // causal, mean 32.5
-                             {1, 1, 0, 152, 1},         // fewer tiles than SMs
-                             {32, 256, 1, 0, 8192}};    // SM count unknown
-    for (const auto& c : gcases) {
-        const int got = fa::dq_grid(c[0], c[1], c[2] != 0, c[3]);
-        if (got != c[4]) {
-            std::printf("FAIL dq_grid(%d,%d,%d,%d) = %d, want %d\n", c[0], c[1], c[2], c[3], got,
-                        c[4]);
+    // CTA per tile otherwise.  {Lq, Lk, BH, causal, n_sm, expected}
+    const int gcases[][6] = {{4096, 4096, 256, 1, 152, 152},    // B8 H32 L4096 causal: mean 16.5
+                             {2048, 2048, 32, 1, 152, 152},     // B1 H32 L2048 causal: mean 8.5
+                             {16384, 16384, 16, 1, 152, 2048},  // B1 H16 L16384 causal: mean 64.5
+                             {512, 512, 512, 0, 152, 152},      // B16 H32 L512: mean 4
+                             {4096, 4096, 64, 0, 152, 152},     // non-causal L4096: mean 32 (limit)
+                             {4224, 4224, 64, 0, 152, 2112},    // non-causal, mean 33
+                             {8064, 8064, 64, 1, 152, 152},     // causal, mean 32
+                             {8192, 8192, 64, 1, 152, 4096},    // causal, mean 32.5
+                             {128, 128, 1, 0, 152, 1},          // fewer tiles than SMs
+                             {4096, 4096, 256, 1, 0, 8192},     // SM count unknown
+                             {512, 8192, 64, 1, 152, 256},      // 512 queries after 7680 keys: 62.5
+                             {1024, 640, 256, 1, 152, 152}};    // Lq > Lk: 3 tiles see no key
+    for (int i = 0; i < (int)(sizeof(gcases) / sizeof(gcases[0])); ++i) {
+        const auto& c = gcases[i];
+        const int got = fa::dq_grid(c[0], c[1], c[2], c[3] != 0, c[4]);
+        if (got != c[5]) {
+            std::printf("FAIL dq_grid(%d,%d,%d,%d,%d) = %d, want %d\n", c[0], c[1], c[2], c[3],
+                        c[4], got, c[5]);
             ++failures;
         }
     }
     // The dK/dV pass: persistent only up to a mean of 12 query tiles per key tile.
-    const int kcases[][5] = {{32, 256, 1, 152, 8192},   // B8 H32 L4096 causal: mean 16.5
-                             {16, 32, 1, 152, 152},     // B1 H32 L2048 causal: mean 8.5
-                             {128, 16, 1, 152, 2048},   // B1 H16 L16384 causal: mean 64.5
-                             {4, 512, 0, 152, 152},     // B16 H32 L512: mean 4
-                             {8, 512, 0, 152, 152},     // B16 H32 L1024: mean 8
-                             {12, 64, 0, 152, 152},     // non-causal, mean 12 (limit)
-                             {13, 64, 0, 152, 832},     // non-causal, mean 13
-                             {23, 64, 1, 152, 152},     // causal, mean 12
-                             {24, 64, 1, 152, 1536},    // causal, mean 12.5
-                             {1, 1, 0, 152, 1},         // fewer tiles than SMs
-                             {4, 512, 0, 0, 2048}};     // SM count unknown
+    const int kcases[][6] = {{4096, 4096, 256, 1, 152, 8192},   // B8 H32 L4096 causal: mean 16.5
+                             {2048, 2048, 32, 1, 152, 152},     // B1 H32 L2048 causal: mean 8.5
+                             {16384, 16384, 16, 1, 152, 2048},  // B1 H16 L16384 causal: mean 64.5
+                             {512, 512, 512, 0, 152, 152},      // B16 H32 L512: mean 4
+                             {1024, 1024, 512, 0, 152, 152},    // B16 H32 L1024: mean 8
+                             {1536, 1536, 64, 0, 152, 152},     // non-causal, mean 12 (limit)
+                             {1664, 1664, 64, 0, 152, 832},     // non-causal, mean 13
+                             {2944, 2944, 64, 1, 152, 152},     // causal, mean 12
+                             {3072, 3072, 64, 1, 152, 1536},    // causal, mean 12.5
+                             {128, 128, 1, 0, 152, 1},          // fewer tiles than SMs
+                             {512, 512, 512, 0, 0, 2048}};      // SM count unknown
     for (const auto& c : kcases) {
-        const int got = fa::dkdv_grid(c[0], c[1], c[2] != 0, c[3]);
-        if (got != c[4]) {
-            std::printf("FAIL dkdv_grid(%d,%d,%d,%d) = %d, want %d\n", c[0], c[1], c[2], c[3], got,
-                        c[4]);
+        const int got = fa::dkdv_grid(c[0], c[1], c[2], c[3] != 0, c[4]);
+        if (got != c[5]) {
+            std::printf("FAIL dkdv_grid(%d,%d,%d,%d,%d) = %d, want %d\n", c[0], c[1], c[2], c[3],
+                        c[4], got, c[5]);
             ++failures;
         }
     }
-    // The forward's grid over query-tile pairs: {n_pairs, n_tiles, BH, causal, n_sm, expected}.
-    const int fcases[][6] = {{16, 32, 256, 1, 152, 152},    // B8 H32 L4096 causal: mean 17
-                             {8, 16, 32, 1, 152, 152},      // B1 H32 L2048 causal: mean 9
-                             {64, 128, 16, 1, 152, 1024},   // B1 H16 L16384 causal: mean 65
-                             {2, 4, 512, 0, 152, 152},      // B16 H32 L512: mean 4
-                             {16, 32, 64, 0, 152, 152},     // non-causal L4096: mean 32 (limit)
-                             {17, 33, 64, 0, 152, 1088},    // non-causal, mean 33
-                             {31, 62, 64, 1, 152, 152},     // causal, mean 32
-                             {32, 63, 64, 1, 152, 2048},    // causal, mean 32.5
-                             {1, 1, 1, 0, 152, 1},          // fewer pairs than SMs
-                             {16, 32, 256, 1, 0, 4096}};    // SM count unknown
+    // The forward's grid over query-tile pairs.
+    const int fcases[][6] = {{4096, 4096, 256, 1, 152, 152},    // B8 H32 L4096 causal: mean 17
+                             {2048, 2048, 32, 1, 152, 152},     // B1 H32 L2048 causal: mean 9
+                             {16384, 16384, 16, 1, 152, 1024},  // B1 H16 L16384 causal: mean 65
+                             {512, 512, 512, 0, 152, 152},      // B16 H32 L512: mean 4
+                             {4096, 4096, 64, 0, 152, 152},     // non-causal L4096: mean 32 (limit)
+                             {4224, 4224, 64, 0, 152, 1088},    // non-causal, mean 33
+                             {7936, 7936, 64, 1, 152, 152},     // causal, 62 tiles: mean 32
+                             {8064, 8064, 64, 1, 152, 2048},    // causal, 63 tiles: mean 33
+                             {128, 128, 1, 0, 152, 1},          // fewer pairs than SMs
+                             {4096, 4096, 256, 1, 0, 4096}};    // SM count unknown
     for (const auto& c : fcases) {
         const int got = fa::fwd_grid(c[0], c[1], c[2], c[3] != 0, c[4]);
         if (got != c[5]) {

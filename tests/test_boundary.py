@@ -32,8 +32,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_device_status",
-              "fa_status_string"):
+    for n in ("fa_fwd", "fa_bwd", "fa_fwd_ex", "fa_bwd_ex", "fa_bwd_workspace_bytes",
+              "fa_get_device_status", "fa_status_string"):
         assert n in names
 
 
@@ -114,6 +114,53 @@ def _bwd(B=1, H=2, L=256, D=64, causal=1, dtype=0, ws_bytes=None, **ptrs):
 ], ids=lambda x: str(x))
 def test_backward_argument_checks(lib, kw, status):
     assert _bwd(**kw) == status
+
+
+def _fwd_ex(strides=None, B=1, H=2, Lq=256, Lk=256, D=64, **ptrs):
+    p = dict(q=A, k=A + MB, v=A + 2 * MB, o=A + 3 * MB, lse=A + 4 * MB)
+    p.update(ptrs)
+    c = (H * Lq * D, Lq * D, D)
+    ck = (H * Lk * D, Lk * D, D)
+    st = strides or [c, ck, ck, c]
+    return fa.fa_fwd_ex(p["q"], p["k"], p["v"], p["o"], p["lse"], st, B, H, Lq, Lk, D, 0.125, 1,
+                        0, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(strides=[(512 * 64, 256 * 64, 60)] + [(512 * 64, 256 * 64, 64)] * 3),
+     fa.FA_ERR_INVALID_ARG),                                           # row stride not 8k
+    (dict(strides=[(512 * 64, 0, 64)] * 4), fa.FA_ERR_INVALID_ARG),    # zero head stride, H = 2
+    (dict(strides=[(-8, 256 * 64, 64)] * 4), fa.FA_ERR_INVALID_ARG),   # negative stride
+    (dict(Lk=0), fa.FA_ERR_UNSUPPORTED),                               # queries, no key
+    (dict(Lq=0), fa.FA_OK),                                            # no query: nothing to do
+    (dict(o=A + 2 * MB + 4096), fa.FA_ERR_INVALID_ARG),               # o inside v's extent
+    # [B,L,H,D] views whose extents overlap: o would be read as k
+    (dict(strides=[(256 * 2 * 64, 64, 2 * 64)] * 4, o=A + MB), fa.FA_ERR_INVALID_ARG),
+], ids=lambda x: str(x)[:60])
+def test_forward_ex_argument_checks(lib, kw, status):
+    assert _fwd_ex(**kw) == status
+
+
+def test_backward_ex_refuses_one_sided_empty_and_overlapping_outputs(lib):
+    B, H, L, D = 1, 2, 256, 64
+    c = (H * L * D, L * D, D)
+    p = [A + i * MB for i in range(10)]
+    ws = fa.fa_bwd_workspace_bytes(B, H, L, D)
+
+    def call(strides, Lq=L, Lk=L, **kw):
+        q = dict(zip(("q", "k", "v", "o", "do", "lse", "dq", "dk", "dv", "ws"), p))
+        q.update(kw)
+        return fa.fa_bwd_ex(q["q"], q["k"], q["v"], q["o"], q["do"], q["lse"], q["dq"], q["dk"],
+                            q["dv"], q["ws"], ws, strides, B, H, Lq, Lk, D, 0.125, 1, 0, None)
+
+    assert call([c] * 8, Lq=0, Lk=0) == fa.FA_OK
+    assert call([c] * 8, Lq=0) == fa.FA_ERR_UNSUPPORTED
+    assert call([c] * 8, Lk=0) == fa.FA_ERR_UNSUPPORTED
+    # dk inside dq's extent with contiguous strides: not the interleaved parts of a packed tensor
+    assert call([c] * 8, dk=p[6] + 4096) == fa.FA_ERR_INVALID_ARG
+    # packed [B,L,3,H,D] strides but dk placed on top of dq's heads: overlapping elements
+    pk = (L * 3 * H * D, D, 3 * H * D)
+    assert call([c] * 5 + [pk] * 3, dk=p[6] + 64 * 2) == fa.FA_ERR_INVALID_ARG
 
 
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -1,13 +1,19 @@
 """GB300 (sm_103a) exact attention, FlashAttention-style: Python binding of ``libfa.so``.
 
-The functions ``fa_fwd``, ``fa_bwd``, ``fa_bwd_workspace_bytes``, ``fa_get_device_status``,
-``fa_set_wait_timeout_ns``, ``fa_selftest_wait_timeout`` and ``fa_status_string`` mirror the C
-ABI in ``include/fa.h`` one to one: they only marshal arguments (device pointers, sizes,
-stream handle).  Every step of the computation runs in the library's CUDA kernels; there is
-no CPU or PyTorch fallback, and loading fails loudly when the library has not been built.
+The functions ``fa_fwd``, ``fa_fwd_ex``, ``fa_bwd``, ``fa_bwd_ex``, ``fa_bwd_workspace_bytes``,
+``fa_get_device_status``, ``fa_set_wait_timeout_ns``, ``fa_selftest_wait_timeout`` and
+``fa_status_string`` mirror the C ABI in ``include/fa.h`` one to one: they only marshal
+arguments (device pointers, strides, sizes, stream handle).  Every step of the computation runs
+in the library's CUDA kernels; there is no CPU or PyTorch fallback, and loading fails loudly
+when the library has not been built.
 
 ``forward`` / ``backward`` / ``attention`` are conveniences over the same calls for torch
-tensors of shape [B, H, L, D] (memory allocation and the current CUDA stream come from torch).
+tensors viewed as [B, H, L, D] with a contiguous last dimension and any other strides (memory
+allocation and the current CUDA stream come from torch); queries and keys may differ in length.
+``attention_blhd`` takes [B, L, H, D] tensors and ``attention_qkvpacked`` one [B, L, 3, H, D]
+tensor, the layouts of the flash_attn_func and flash_attn_qkvpacked_func interfaces the pages
+use ("FlashAttention data-flow optimisation", section 4.1, step 3; "AIInfra notes 01: from
+TFLOPS to FlashAttention", sections 4.2-4.3).
 """
 from __future__ import annotations
 
@@ -16,10 +22,11 @@ import math
 import os
 import threading
 
-__all__ = ["FaError", "load_library", "library_path", "fa_fwd", "fa_bwd",
+__all__ = ["FaError", "load_library", "library_path", "fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_ex",
            "fa_bwd_workspace_bytes", "fa_get_device_status", "fa_set_wait_timeout_ns",
            "fa_selftest_wait_timeout", "fa_trace_next_call", "fa_launch_count", "fa_status_string",
-           "fa_bwd_noalloc", "forward", "backward", "attention",
+           "fa_bwd_noalloc", "forward", "backward", "attention", "attention_blhd",
+           "attention_qkvpacked", "FaStrides",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
            "FA_BF16", "FA_FP16"]
 
@@ -31,9 +38,15 @@ _LIB_PATH = os.path.join(_PKG, "_build", "libfa.so")
 _lib = None
 _lock = threading.Lock()
 
-EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_get_device_status",
+EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_ex", "fa_bwd_workspace_bytes",
+            "fa_get_device_status",
             "fa_set_wait_timeout_ns", "fa_selftest_wait_timeout", "fa_trace_next_call",
             "fa_launch_count", "fa_status_string", "fa_bwd_noalloc")
+
+
+class FaStrides(ctypes.Structure):
+    """fa_strides: element strides (batch, head, row) of a [B, H, L, D] operand."""
+    _fields_ = [("batch", ctypes.c_int64), ("head", ctypes.c_int64), ("row", ctypes.c_int64)]
 
 
 class FaError(RuntimeError):
@@ -63,6 +76,12 @@ def load_library():
         lib.fa_bwd_workspace_bytes.restype = sz
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, i, vp]
         lib.fa_bwd.restype = i
+        sp = ctypes.POINTER(FaStrides)
+        lib.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, sp, i, i, i, i, i, f, i, i, vp]
+        lib.fa_fwd_ex.restype = i
+        lib.fa_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, sp, i, i, i, i, i, f,
+                                  i, i, vp]
+        lib.fa_bwd_ex.restype = i
         lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i,
                                        vp]
         lib.fa_bwd_noalloc.restype = i
@@ -87,6 +106,25 @@ def load_library():
 # ---------------------------------------------------------------------------------------
 def fa_fwd(q, k, v, o, lse, B, H, L, D, scale, causal, dtype, stream) -> int:
     return load_library().fa_fwd(q, k, v, o, lse, B, H, L, D, scale, int(causal), dtype, stream)
+
+
+def _strides_array(strides):
+    """Sequence of (batch, head, row) element strides -> ctypes array of fa_strides."""
+    return (FaStrides * len(strides))(*[FaStrides(*map(int, t)) for t in strides])
+
+
+def fa_fwd_ex(q, k, v, o, lse, strides, B, H, Lq, Lk, D, scale, causal, dtype, stream) -> int:
+    """``strides``: four (batch, head, row) tuples for q, k, v, o."""
+    return load_library().fa_fwd_ex(q, k, v, o, lse, _strides_array(strides), B, H, Lq, Lk, D,
+                                    scale, int(causal), dtype, stream)
+
+
+def fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, strides, B, H, Lq,
+              Lk, D, scale, causal, dtype, stream) -> int:
+    """``strides``: eight (batch, head, row) tuples for q, k, v, o, dout, dq, dk, dv."""
+    return load_library().fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace,
+                                    workspace_bytes, _strides_array(strides), B, H, Lq, Lk, D,
+                                    scale, int(causal), dtype, stream)
 
 
 def fa_bwd_workspace_bytes(B, H, L, D) -> int:
@@ -145,13 +183,17 @@ def _dtype_code(t) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}; expected bfloat16 or float16")
 
 
-def _check(t, name, shape=None):
+def _view_strides(t, name, shape=None):
+    """(batch, head, row) element strides of a CUDA tensor viewed as [B, H, L, D]."""
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous [B,H,L,D]")
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be a [B, H, L, D] view")
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.stride(3) != 1:
+        raise ValueError(f"{name}: the last (D) dimension must be contiguous")
+    return (t.stride(0), t.stride(1), t.stride(2))
 
 
 def _stream_handle(device) -> int:
@@ -160,54 +202,67 @@ def _stream_handle(device) -> int:
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
-    """O, LSE = attention(q, k, v) for contiguous CUDA tensors [B,H,L,D] (bf16 or fp16)."""
+    """O, LSE = attention(q, k, v) for CUDA tensors viewed as [B, H, Lq, D] (q) and
+    [B, H, Lk, D] (k, v), bf16 or fp16, with a contiguous last dimension.  O has q's shape (and,
+    where torch can keep them, q's strides); LSE is contiguous [B, H, Lq] fp32."""
     import torch
-    _check(q, "q")
-    _check(k, "k", q.shape)
-    _check(v, "v", q.shape)
-    B, H, L, D = q.shape
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    st = [_view_strides(q, "q"), _view_strides(k, "k", (B, H, Lk, D)),
+          _view_strides(v, "v", (B, H, Lk, D))]
     dt = _dtype_code(q)
     if k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must share a dtype")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     o = out if out is not None else torch.empty_like(q)
-    l = lse if lse is not None else torch.empty((B, H, L), device=q.device, dtype=torch.float32)
-    st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, H, L, D,
-                float(scale), causal, dt, _stream_handle(q.device))
-    if st != FA_OK:
-        raise FaError("fa_fwd", st)
+    st.append(_view_strides(o, "out", q.shape))
+    l = lse if lse is not None else torch.empty((B, H, Lq), device=q.device, dtype=torch.float32)
+    if not l.is_contiguous() or tuple(l.shape) != (B, H, Lq):
+        raise ValueError("lse must be a contiguous [B, H, Lq] tensor")
+    status = fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), st,
+                       B, H, Lq, Lk, D, float(scale), causal, dt, _stream_handle(q.device))
+    if status != FA_OK:
+        raise FaError("fa_fwd_ex", status)
     return o, l
 
 
 def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
-             workspace=None):
-    """dQ, dK, dV for the forward above (same shapes and dtype as q)."""
+             workspace=None, grads=None):
+    """dQ, dK, dV for the forward above.  ``grads`` optionally gives the three output views
+    (for example the parts of one packed gradient tensor); by default they are allocated like
+    q, k, v."""
     import torch
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
-        _check(t, name, q.shape)
-    B, H, L, D = q.shape
-    _check(lse, "lse", (B, H, L))
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    st = [_view_strides(q, "q"), _view_strides(k, "k", (B, H, Lk, D)),
+          _view_strides(v, "v", (B, H, Lk, D)), _view_strides(o, "o", q.shape),
+          _view_strides(dout, "dout", q.shape)]
+    if tuple(lse.shape) != (B, H, Lq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous [B, H, Lq] tensor")
     dt = _dtype_code(q)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    ws_bytes = fa_bwd_workspace_bytes(B, H, L, D)
+    ws_bytes = fa_bwd_workspace_bytes(B, H, Lq, D)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), device=q.device, dtype=torch.uint8)
-    dq = torch.empty_like(q)
-    dk = torch.empty_like(q)
-    dv = torch.empty_like(q)
-    st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
-                lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
-                workspace.numel() * workspace.element_size(), B, H, L, D, float(scale), causal, dt,
-                _stream_handle(q.device))
-    if st != FA_OK:
-        raise FaError("fa_bwd", st)
+    if grads is None:
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    dq, dk, dv = grads
+    st += [_view_strides(dq, "dq", q.shape), _view_strides(dk, "dk", k.shape),
+           _view_strides(dv, "dv", k.shape)]
+    status = fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                       workspace.data_ptr(), workspace.numel() * workspace.element_size(), st,
+                       B, H, Lq, Lk, D, float(scale), causal, dt, _stream_handle(q.device))
+    if status != FA_OK:
+        raise FaError("fa_bwd_ex", status)
     return dq, dk, dv
 
 
 def attention(q, k, v, causal: bool = False, scale: float | None = None):
-    """Differentiable attention for torch autograd (forward and backward run in libfa)."""
+    """Differentiable attention for torch autograd (forward and backward run in libfa) over
+    [B, H, L, D] views (Lq may differ from Lk)."""
     import torch
 
     class _Attention(torch.autograd.Function):
@@ -220,6 +275,45 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None):
         @staticmethod
         def backward(ctx, do_):
             q_, k_, v_, o_, lse_ = ctx.saved_tensors
-            return backward(q_, k_, v_, o_, lse_, do_.contiguous(), causal, scale)
+            if do_.stride(-1) != 1:
+                do_ = do_.contiguous()
+            return backward(q_, k_, v_, o_, lse_, do_, causal, scale)
 
     return _Attention.apply(q, k, v)
+
+
+def attention_blhd(q, k, v, causal: bool = False, scale: float | None = None):
+    """attention() for [B, L, H, D] tensors (the flash_attn_func layout); returns O as
+    [B, Lq, H, D].  No copy: the kernels read and write the [B, L, H, D] memory directly."""
+    return attention(q.transpose(1, 2), k.transpose(1, 2), v.transpose(1, 2), causal,
+                     scale).transpose(1, 2)
+
+
+def attention_qkvpacked(qkv, causal: bool = False, scale: float | None = None):
+    """attention() for one packed [B, L, 3, H, D] tensor (the flash_attn_qkvpacked_func layout);
+    returns O as [B, L, H, D].  Q, K and V are read in place, and the backward writes dQ, dK, dV
+    into the three interleaved parts of one packed [B, L, 3, H, D] gradient."""
+    import torch
+
+    class _Packed(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, qkv_):
+            q_, k_, v_ = (qkv_[:, :, i].transpose(1, 2) for i in range(3))
+            B, H, L, D = q_.shape
+            o_ = torch.empty((B, L, H, D), device=qkv_.device, dtype=qkv_.dtype).transpose(1, 2)
+            o_, lse_ = forward(q_, k_, v_, causal, scale, out=o_)
+            ctx.save_for_backward(qkv_, o_, lse_)
+            return o_.transpose(1, 2)
+
+        @staticmethod
+        def backward(ctx, do_):
+            qkv_, o_, lse_ = ctx.saved_tensors
+            q_, k_, v_ = (qkv_[:, :, i].transpose(1, 2) for i in range(3))
+            if do_.stride(-1) != 1:
+                do_ = do_.contiguous()
+            dqkv = torch.empty_like(qkv_)
+            parts = tuple(dqkv[:, :, i].transpose(1, 2) for i in range(3))
+            backward(q_, k_, v_, o_, lse_, do_.transpose(1, 2), causal, scale, grads=parts)
+            return dqkv
+
+    return _Packed.apply(qkv)

@@ -11,6 +11,7 @@
 #include "../../include/fa.h"
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
+#include "fa_sched.h"
 
 namespace fa {
 namespace {
@@ -51,17 +52,30 @@ int* status_ptr() {
     return g_status_ptr[dev];
 }
 
-// [BH, L, D] 16-bit tensor viewed as 3-D {D, L, BH}; box = 64 elements x 128 rows x 1, with
-// the 128-byte swizzle the tcgen05 descriptors expect.  Rows past L read as zeros.
-bool make_map(CUtensorMap* m, const void* ptr, int BH, int L, int D, bool bf16) {
+// Makes the current device's primary context current on the calling thread.  The driver's
+// tensor-map encoder needs a current context, and a thread may have none yet: a framework's
+// worker thread (torch's autograd engine, for one) that has made no runtime call that creates
+// or binds a context.  cudaSetDevice on the device the thread already uses does exactly that
+// and allocates nothing.
+bool bind_context() {
+    int dev = 0;
+    return cudaGetDevice(&dev) == cudaSuccess && cudaSetDevice(dev) == cudaSuccess;
+}
+
+// [B, H, L, D] 16-bit tensor with element strides `st` (D contiguous) viewed as 4-D
+// {D, L, H, B}; box = 64 elements x 128 rows x 1 x 1, with the 128-byte swizzle the tcgen05
+// descriptors expect.  Rows past L read as zeros.  The strides are positive multiples of 8
+// elements (16 bytes), checked by the caller.
+bool make_map(CUtensorMap* m, const void* ptr, int B, int H, int L, int D, const Strides& st,
+              bool bf16) {
     auto enc = encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)L * D * 2};
-    cuuint32_t box[3] = {(cuuint32_t)kChunkElems, (cuuint32_t)kTileRows, 1};
-    cuuint32_t elem[3] = {1, 1, 1};
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)st.l * 2, (cuuint64_t)st.h * 2, (cuuint64_t)st.b * 2};
+    cuuint32_t box[4] = {(cuuint32_t)kChunkElems, (cuuint32_t)kTileRows, 1, 1};
+    cuuint32_t elem[4] = {1, 1, 1, 1};
     CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                     3, const_cast<void*>(ptr), dims, strides, box, elem,
+                     4, const_cast<void*>(ptr), dims, strides, box, elem,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -116,30 +130,70 @@ Range range(const void* p, size_t bytes) {
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
 struct Shape {
-    int BH = 0, L = 0, D = 0, n_tiles = 0, Lpad = 0;
-    size_t tensor_bytes = 0, row_bytes = 0;
+    int BH = 0, H = 0, Lq = 0, Lk = 0, D = 0, n_qtiles = 0, n_ktiles = 0, Lqpad = 0;
+    size_t lse_bytes = 0;
     bool empty = true;
 };
 
 // Checks sizes and flags shared by both passes.  Does not touch the GPU.
-fa_status check_shape(int B, int H, int L, int D, float scale, int causal, int dtype, Shape* sh) {
+fa_status check_shape(int B, int H, int Lq, int Lk, int D, float scale, int causal, int dtype,
+                      Shape* sh) {
     if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-    if (B < 0 || H < 0 || L < 0 || D <= 0) return FA_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || D <= 0) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
     const long long bh = (long long)B * (long long)H;
-    const long long tiles = ((long long)L + kTileRows - 1) / kTileRows;
-    if (bh > 0x7fffffffLL || tiles * bh > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    const long long qtiles = ((long long)Lq + kTileRows - 1) / kTileRows;
+    const long long ktiles = ((long long)Lk + kTileRows - 1) / kTileRows;
+    if (bh > 0x7fffffffLL || qtiles * bh > 0x7fffffffLL || ktiles * bh > 0x7fffffffLL)
+        return FA_ERR_UNSUPPORTED;
     sh->BH = (int)bh;
-    sh->L = L;
+    sh->H = H;
+    sh->Lq = Lq;
+    sh->Lk = Lk;
     sh->D = D;
-    sh->n_tiles = (int)tiles;
-    sh->Lpad = (int)(tiles * kTileRows);
-    sh->tensor_bytes = (size_t)bh * (size_t)L * (size_t)D * 2u;
-    sh->row_bytes = (size_t)bh * (size_t)L * 4u;
-    sh->empty = (bh == 0 || L == 0);
+    sh->n_qtiles = (int)qtiles;
+    sh->n_ktiles = (int)ktiles;
+    sh->Lqpad = (int)(qtiles * kTileRows);
+    sh->lse_bytes = (size_t)bh * (size_t)Lq * 4u;
+    sh->empty = (bh == 0 || Lq == 0);  // no output row
     return FA_OK;
+}
+
+// A caller's strides, checked for the TMA rules (positive multiples of 8 elements = 16 bytes,
+// below 2^39 elements); a stride of 0 is accepted for a dimension of size 1 and replaced by 8.
+bool take_strides(const fa_strides& in, int B, int H, Strides* out) {
+    long long v[3] = {in.batch, in.head, in.row};
+    const int size[3] = {B, H, 2};  // the row dimension always counts
+    for (int i = 0; i < 3; ++i) {
+        if (v[i] == 0 && size[i] == 1) v[i] = 8;
+        if (v[i] <= 0 || (v[i] & 7) != 0 || v[i] >= (1LL << 39)) return false;
+    }
+    *out = {v[0], v[1], v[2]};
+    return true;
+}
+
+// Bytes from the first to one past the last element of a strided [B, H, L, D] 16-bit operand.
+Range extent(const void* p, const Strides& s, int B, int H, int L, int D) {
+    const long long last = (long long)(B - 1) * s.b + (long long)(H - 1) * s.h +
+                           (long long)(L - 1) * s.l + D;
+    return range(p, (size_t)last * 2u);
+}
+
+// Two outputs of the same shape and strides whose extents overlap are still disjoint element by
+// element when they are interleaved parts of one packed tensor: the H heads of a row lie
+// together (head stride D), the two bases are at least H*D elements apart and the second's heads
+// end before the first's next row, and rows of different batches do not interleave.
+bool interleaved_disjoint(const void* a, const void* b, const Strides& s, int L, int H, int D) {
+    const long long da = reinterpret_cast<intptr_t>(a), db = reinterpret_cast<intptr_t>(b);
+    const long long delta = (da > db ? da - db : db - da) / 2;
+    const long long span = (long long)H * D;
+    return s.h == D && delta >= span && delta + span <= s.l && s.b >= (long long)L * s.l;
+}
+
+bool same_strides(const Strides& a, const Strides& b) {
+    return a.b == b.b && a.h == b.h && a.l == b.l;
 }
 
 }  // namespace
@@ -164,11 +218,11 @@ int bwd_check_args(const void* q, const void* k, const void* v, const void* o, c
                    int L, int D, float scale, int causal, int dtype, size_t* ws_need) {
     Shape sh;
     *ws_need = 0;
-    fa_status st = check_shape(B, H, L, D, scale, causal, dtype, &sh);
+    fa_status st = check_shape(B, H, L, L, D, scale, causal, dtype, &sh);
     if (st != FA_OK) return st;
     if (sh.empty) return FA_OK;
     if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-    *ws_need = 2u * (size_t)sh.BH * (size_t)sh.Lpad * 4u;
+    *ws_need = 2u * (size_t)sh.BH * (size_t)sh.Lqpad * 4u;
     return FA_OK;
 }
 
@@ -190,8 +244,7 @@ __global__ void fa_wait_selftest_kernel(int* status, uint64_t timeout_ns) {
 }  // namespace
 
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s) {
-    fa_wait_selftest_kernel<<<1, 32, 0, s>>>(status, timeout_ns);
-    return cudaGetLastError();
+    return launch_kernel(fa_wait_selftest_kernel, 1, 32, 0, s, status, timeout_ns);
 }
 
 }  // namespace fa
@@ -229,19 +282,25 @@ fa_status fa_trace_next_call(void* const* events, int n_pairs) {
 
 uint64_t fa_launch_count(void) { return g_launches.load(); }
 
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                 int L, int D, float scale, int causal, int dtype, void* stream) {
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const fa_strides* strides, int B, int H, int Lq, int Lk, int D, float scale,
+                    int causal, int dtype, void* stream) {
     TraceDisarm disarm;
     Shape sh;
-    fa_status st = check_shape(B, H, L, D, scale, causal, dtype, &sh);
+    fa_status st = check_shape(B, H, Lq, Lk, D, scale, causal, dtype, &sh);
     if (st != FA_OK) return st;
     if (sh.empty) return FA_OK;
-    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (Lk == 0) return FA_ERR_UNSUPPORTED;  // queries but no key at all
+    if (!q || !k || !v || !o || !lse || !strides) return FA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FA_ERR_INVALID_ARG;
-    const Range rq = range(q, sh.tensor_bytes), rk = range(k, sh.tensor_bytes),
-                rv = range(v, sh.tensor_bytes), ro = range(o, sh.tensor_bytes),
-                rl = range(lse, sh.row_bytes);
+    Strides sq, sk, sv, so;
+    if (!take_strides(strides[0], B, H, &sq) || !take_strides(strides[1], B, H, &sk) ||
+        !take_strides(strides[2], B, H, &sv) || !take_strides(strides[3], B, H, &so))
+        return FA_ERR_INVALID_ARG;
+    const Range rq = extent(q, sq, B, H, Lq, D), rk = extent(k, sk, B, H, Lk, D),
+                rv = extent(v, sv, B, H, Lk, D), ro = extent(o, so, B, H, Lq, D),
+                rl = range(lse, sh.lse_bytes);
     for (Range out : {ro, rl})
         for (Range in : {rq, rk, rv})
             if (overlap(out, in)) return FA_ERR_INVALID_ARG;
@@ -250,15 +309,20 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     FwdParams p;
     std::memset(&p, 0, sizeof(p));
     const bool bf16 = dtype == FA_BF16;
-    if (!make_map(&p.tm_q, q, sh.BH, L, D, bf16) || !make_map(&p.tm_k, k, sh.BH, L, D, bf16) ||
-        !make_map(&p.tm_v, v, sh.BH, L, D, bf16))
+    if (!bind_context()) return FA_ERR_CUDA;
+    if (!make_map(&p.tm_q, q, B, H, Lq, D, sq, bf16) || !make_map(&p.tm_k, k, B, H, Lk, D, sk, bf16) ||
+        !make_map(&p.tm_v, v, B, H, Lk, D, sv, bf16))
         return FA_ERR_CUDA;
     p.o = o;
+    p.so = so;
     p.lse = lse;
-    p.L = L;
+    p.Lq = Lq;
+    p.Lk = Lk;
+    p.H = H;
     p.BH = sh.BH;
-    p.n_tiles = sh.n_tiles;
-    p.group = schedule_group(sh.BH, L, D);
+    p.n_qtiles = sh.n_qtiles;
+    p.n_ktiles = sh.n_ktiles;
+    p.group = schedule_group(sh.BH, Lk, D);
     // The softmax takes the row maximum of the stored S, so it must work with a non-negative
     // multiplier: a negative scale is moved into the S contraction as an exact sign flip.  The
     // multiplier is at least the smallest normal float, so that a masked logit (-inf) stays
@@ -271,61 +335,99 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     if (!p.status) return FA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = traced_launch(0, s, [&] { return launch_fwd(p, D, bf16, causal != 0, s); });
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    // Under the causal mask the first Lq - Lk query rows see no key when Lq > Lk.
+    const int empty_rows = (causal && Lq > Lk) ? Lq - Lk : 0;
+    if (empty_rows > 0)
+        e = traced_launch(1, s, [&] { return launch_fwd_empty_rows(p, D, empty_rows, s); });
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int L, int D, float scale, int causal, int dtype, void* stream) {
+    const fa_strides c = {(int64_t)H * L * D, (int64_t)L * D, (int64_t)D};
+    const fa_strides all[4] = {c, c, c, c};
+    return fa_fwd_ex(q, k, v, o, lse, all, B, H, L, L, D, scale, causal, dtype, stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int L, int D) {
     Shape sh;
-    if (check_shape(B, H, L, D, 1.0f, 0, FA_BF16, &sh) != FA_OK || sh.empty) return 0;
-    return 2u * (size_t)sh.BH * (size_t)sh.Lpad * 4u;
+    if (check_shape(B, H, L, L, D, 1.0f, 0, FA_BF16, &sh) != FA_OK || sh.empty) return 0;
+    return 2u * (size_t)sh.BH * (size_t)sh.Lqpad * 4u;
 }
 
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                 const float* lse, void* dq, void* dk, void* dv, void* workspace,
-                 size_t workspace_bytes, int B, int H, int L, int D, float scale, int causal,
-                 int dtype, void* stream) {
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                    const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                    size_t workspace_bytes, const fa_strides* strides, int B, int H, int Lq,
+                    int Lk, int D, float scale, int causal, int dtype, void* stream) {
     TraceDisarm disarm;
     Shape sh;
-    fa_status st = check_shape(B, H, L, D, scale, causal, dtype, &sh);
+    fa_status st = check_shape(B, H, Lq, Lk, D, scale, causal, dtype, &sh);
     if (st != FA_OK) return st;
-    if (sh.empty) return FA_OK;
-    const size_t ws_need = 2u * (size_t)sh.BH * (size_t)sh.Lpad * 4u;
-    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
+    if (sh.BH == 0 || (Lq == 0 && Lk == 0)) return FA_OK;  // nothing to compute
+    if (Lq == 0 || Lk == 0) return FA_ERR_UNSUPPORTED;     // queries without keys, or keys
+                                                           // without queries
+    const size_t ws_need = 2u * (size_t)sh.BH * (size_t)sh.Lqpad * 4u;
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace || !strides)
         return FA_ERR_INVALID_ARG;
     if (workspace_bytes < ws_need) return FA_ERR_INVALID_ARG;
     const void* all[] = {q, k, v, o, dout, lse, dq, dk, dv, workspace};
     for (const void* ptr : all)
         if (!aligned16(ptr)) return FA_ERR_INVALID_ARG;
-    const size_t tb = sh.tensor_bytes;
-    const Range ins[] = {range(q, tb), range(k, tb), range(v, tb), range(o, tb), range(dout, tb),
-                         range(lse, sh.row_bytes)};
-    const Range outs[] = {range(dq, tb), range(dk, tb), range(dv, tb), range(workspace, ws_need)};
-    for (const Range& a : outs) {
+    Strides s8[8];
+    for (int i = 0; i < 8; ++i)
+        if (!take_strides(strides[i], B, H, &s8[i])) return FA_ERR_INVALID_ARG;
+    const Strides &sq = s8[0], &sk = s8[1], &sv = s8[2], &so = s8[3], &sdo = s8[4], &sdq = s8[5],
+                  &sdk = s8[6], &sdv = s8[7];
+    const Range ins[] = {extent(q, sq, B, H, Lq, D),    extent(k, sk, B, H, Lk, D),
+                         extent(v, sv, B, H, Lk, D),    extent(o, so, B, H, Lq, D),
+                         extent(dout, sdo, B, H, Lq, D), range(lse, sh.lse_bytes)};
+    const void* out_ptr[3] = {dq, dk, dv};
+    const Strides out_st[3] = {sdq, sdk, sdv};
+    const int out_len[3] = {Lq, Lk, Lk};
+    Range outs[4];
+    for (int i = 0; i < 3; ++i) outs[i] = extent(out_ptr[i], out_st[i], B, H, out_len[i], D);
+    outs[3] = range(workspace, ws_need);
+    for (int a = 0; a < 4; ++a) {
         for (const Range& b : ins)
-            if (overlap(a, b)) return FA_ERR_INVALID_ARG;
-        for (const Range& b : outs)
-            if (&a != &b && overlap(a, b)) return FA_ERR_INVALID_ARG;
+            if (overlap(outs[a], b)) return FA_ERR_INVALID_ARG;
+        for (int b = a + 1; b < 4; ++b) {
+            if (!overlap(outs[a], outs[b])) continue;
+            // dQ, dK, dV may be the interleaved parts of one packed gradient tensor.
+            const bool packed = a < 3 && b < 3 && Lq == Lk && same_strides(out_st[a], out_st[b]) &&
+                                interleaved_disjoint(out_ptr[a], out_ptr[b], out_st[a], Lq, H, D);
+            if (!packed) return FA_ERR_INVALID_ARG;
+        }
     }
 
     const bool bf16 = dtype == FA_BF16;
     BwdParams p;
     std::memset(&p, 0, sizeof(p));
-    if (!make_map(&p.tm_q, q, sh.BH, L, D, bf16) || !make_map(&p.tm_k, k, sh.BH, L, D, bf16) ||
-        !make_map(&p.tm_v, v, sh.BH, L, D, bf16) || !make_map(&p.tm_do, dout, sh.BH, L, D, bf16))
+    if (!bind_context()) return FA_ERR_CUDA;
+    if (!make_map(&p.tm_q, q, B, H, Lq, D, sq, bf16) || !make_map(&p.tm_k, k, B, H, Lk, D, sk, bf16) ||
+        !make_map(&p.tm_v, v, B, H, Lk, D, sv, bf16) ||
+        !make_map(&p.tm_do, dout, B, H, Lq, D, sdo, bf16))
         return FA_ERR_CUDA;
     float* nlse2_pad = static_cast<float*>(workspace);
-    float* delta_pad = nlse2_pad + (size_t)sh.BH * sh.Lpad;
+    float* delta_pad = nlse2_pad + (size_t)sh.BH * sh.Lqpad;
     p.dout = dout;
+    p.sdo = sdo;
     p.nlse2_pad = nlse2_pad;
     p.delta_pad = delta_pad;
     p.dq = dq;
     p.dk = dk;
     p.dv = dv;
-    p.L = L;
-    p.Lpad = sh.Lpad;
+    p.sdq = sdq;
+    p.sdk = sdk;
+    p.sdv = sdv;
+    p.Lq = Lq;
+    p.Lk = Lk;
+    p.Lqpad = sh.Lqpad;
+    p.H = H;
     p.BH = sh.BH;
-    p.n_tiles = sh.n_tiles;
-    p.group = schedule_group(sh.BH, L, D);
+    p.n_qtiles = sh.n_qtiles;
+    p.n_ktiles = sh.n_ktiles;
+    p.group = schedule_group(sh.BH, Lq > Lk ? Lq : Lk, D);
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.status = status_ptr();
@@ -333,15 +435,24 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     if (!p.status) return FA_ERR_CUDA;
 
     BwdPreParams pp;
+    std::memset(&pp, 0, sizeof(pp));
     pp.o = o;
     pp.dout = dout;
+    pp.dq = dq;
+    pp.so = so;
+    pp.sdo = sdo;
+    pp.sdq = sdq;
     pp.lse = lse;
     pp.nlse2_pad = nlse2_pad;
     pp.delta_pad = delta_pad;
-    pp.L = L;
-    pp.Lpad = sh.Lpad;
+    pp.Lq = Lq;
+    pp.Lqpad = sh.Lqpad;
+    pp.H = H;
     pp.BH = sh.BH;
     pp.D = D;
+    // Under the causal mask query row i sees key j iff j <= i + Lk - Lq: rows below Lq - Lk
+    // see none (their dQ is zero).
+    pp.first_seen_row = (causal && Lq > Lk) ? Lq - Lk : 0;
     pp.bf16 = bf16 ? 1 : 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -354,6 +465,16 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
         cudaSuccess)
         return FA_ERR_CUDA;
     return FA_OK;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                 size_t workspace_bytes, int B, int H, int L, int D, float scale, int causal,
+                 int dtype, void* stream) {
+    const fa_strides c = {(int64_t)H * L * D, (int64_t)L * D, (int64_t)D};
+    const fa_strides all[8] = {c, c, c, c, c, c, c, c};
+    return fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, all, B, H, L,
+                     L, D, scale, causal, dtype, stream);
 }
 
 fa_status fa_get_device_status(void* stream) {

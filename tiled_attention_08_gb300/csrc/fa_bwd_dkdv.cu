@@ -104,16 +104,18 @@ constexpr int dkdv_smem_bytes() {
 
 // One work item: key tile kt of head bh and the query tiles [it0, it0 + n_it) that see it.
 struct DkdvItem {
-    int bh, kt, it0, n_it;
+    int bh, b, h, kt, it0, n_it;
 };
 
 template <bool CAUSAL>
 __device__ __forceinline__ bool dkdv_item(const BwdParams& p, int round, DkdvItem& it) {
-    const int id = persistent_tile(round, (int)blockIdx.x, (int)gridDim.x, p.n_tiles * p.BH);
+    const int id = persistent_tile(round, (int)blockIdx.x, (int)gridDim.x, p.n_ktiles * p.BH);
     if (id < 0) return false;
-    tile_coords(id, p.BH, p.n_tiles, p.group, it.bh, it.kt);  // key tile 0 (heaviest) first
-    it.it0 = CAUSAL ? it.kt : 0;
-    it.n_it = p.n_tiles - it.it0;
+    tile_coords(id, p.BH, p.n_ktiles, p.group, it.bh, it.kt);  // key tile 0 (heaviest) first
+    it.b = it.bh / p.H;
+    it.h = it.bh - it.b * p.H;
+    it.it0 = k_tile_q0(it.kt, p.Lq, p.Lk, CAUSAL);
+    it.n_it = p.n_qtiles - it.it0;
     return true;
 }
 
@@ -154,9 +156,10 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
     // Heads in L2-sized groups (their Q/dO/LSE/Delta are streamed by every key tile); inside
     // a group key tile 0 first: it has the most query tiles under the causal mask.
     int bh, kt;
-    tile_coords(blockIdx.x, p.BH, p.n_tiles, p.group, bh, kt);
-    const int it0 = CAUSAL ? kt : 0;
-    const int n_it = p.n_tiles - it0;
+    tile_coords(blockIdx.x, p.BH, p.n_ktiles, p.group, bh, kt);
+    const int hb = bh / p.H, hh = bh - hb * p.H;  // batch and head of bh
+    const int it0 = k_tile_q0(kt, p.Lq, p.Lk, CAUSAL);
+    const int n_it = p.n_qtiles - it0;
     volatile int* abort_v = &abort_flag;
 
     if (threadIdx.x == 0) {
@@ -193,11 +196,10 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
             tma_prefetch_desc(&p.tm_do);
             mbar_arrive_expect_tx(&bar_kv, 2 * C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c) {
-                tma_load_3d(smem + C::kOffK + c * kChunkBytes, &p.tm_k, &bar_kv, c * kChunkElems,
-                            kt * kTileRows, bh);
-                tma_load_3d(smem + C::kOffK + C::kTileBytes + c * kChunkBytes, &p.tm_v, &bar_kv,
-                            c * kChunkElems,
-                            kt * kTileRows, bh);
+                tma_load_4d(smem + C::kOffK + c * kChunkBytes, &p.tm_k, &bar_kv, c * kChunkElems,
+                            kt * kTileRows, hh, hb);
+                tma_load_4d(smem + C::kOffK + C::kTileBytes + c * kChunkBytes, &p.tm_v, &bar_kv,
+                            c * kChunkElems, kt * kTileRows, hh, hb);
             }
             bool ok = true;
             int issued_q = 0, issued_o = 0;
@@ -210,10 +212,10 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                 const int it = it0 + t;
                 mbar_arrive_expect_tx(&bar_qf[st], C::kTileBytes + C::kVecBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(smem + C::kOffQ + st * C::kTileBytes + c * kChunkBytes, &p.tm_q,
-                                &bar_qf[st], c * kChunkElems, it * kTileRows, bh);
+                    tma_load_4d(smem + C::kOffQ + st * C::kTileBytes + c * kChunkBytes, &p.tm_q,
+                                &bar_qf[st], c * kChunkElems, it * kTileRows, hh, hb);
                 bulk_load(smem + C::kOffNlse + st * C::kVecBytes,
-                          p.nlse2_pad + (size_t)bh * p.Lpad + (size_t)it * kTileRows, C::kVecBytes,
+                          p.nlse2_pad + (size_t)bh * p.Lqpad + (size_t)it * kTileRows, C::kVecBytes,
                           &bar_qf[st]);
                 issued_q = t + 1;
                 return true;
@@ -227,10 +229,10 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                 const int it = it0 + t;
                 mbar_arrive_expect_tx(&bar_of[st], C::kTileBytes + C::kVecBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(smem + C::kOffDO + st * C::kTileBytes + c * kChunkBytes, &p.tm_do,
-                                &bar_of[st], c * kChunkElems, it * kTileRows, bh);
+                    tma_load_4d(smem + C::kOffDO + st * C::kTileBytes + c * kChunkBytes, &p.tm_do,
+                                &bar_of[st], c * kChunkElems, it * kTileRows, hh, hb);
                 bulk_load(smem + C::kOffDelta + st * C::kVecBytes,
-                          p.delta_pad + (size_t)bh * p.Lpad + (size_t)it * kTileRows, C::kVecBytes,
+                          p.delta_pad + (size_t)bh * p.Lqpad + (size_t)it * kTileRows, C::kVecBytes,
                           &bar_of[st]);
                 issued_o = t + 1;
                 return true;
@@ -369,8 +371,8 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
             const uint32_t nlse2_addr = smem_u32(smem + C::kOffNlse + qs * C::kVecBytes) + c0 * 4;
             const uint32_t dlt_addr = smem_u32(smem + C::kOffDelta + os * C::kVecBytes) + c0 * 4;
             const int q0 = it * kTileRows + c0;
-            const bool masked = (CAUSAL && it == kt) || (it * kTileRows + kTileRows > p.L);
-            const int qlim = p.L - 1;  // last valid query
+            const bool masked = tile_masked(it, kt, p.Lq, p.Lk, CAUSAL);
+            const int qlim = p.Lq - 1;  // last valid query
             // Phase 1: P^T = exp2(S^T * scale*log2e - LSE*log2e) on this warp's columns; kept
             // in registers, and the S^T columns are released at once.
             ok = wait_bounded(&bar_qf[qs], qph, abort_v, p.timeout_ns) &&
@@ -404,7 +406,7 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < kC; ++i) {
                         const int qg = q0 + i;
-                        if (qg > qlim || (CAUSAL && key > qg)) pv[i] = 0.0f;
+                        if (qg > qlim || (CAUSAL && key > qg + (p.Lk - p.Lq))) pv[i] = 0.0f;
                     }
                 }
 #pragma unroll
@@ -461,14 +463,16 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
             if (lane == 0) record_timeout(p.status, abort_v);
         } else {
             tc_fence_after_sync();
-            const bool valid = key < p.L;
-            const size_t roff = ((size_t)bh * p.L + key) * D * 2 + part * C::kOutCols * 2;
+            const bool valid = key < p.Lk;
+            const size_t coff = (size_t)part * C::kOutCols * 2;
             tmem_row_to_global<BF16, C::kOutCols>(
                 tmem + lane_off + C::kTmDV + part * C::kOutCols,
-                reinterpret_cast<uint8_t*>(p.dv) + roff, 1.0f, valid);
+                reinterpret_cast<uint8_t*>(p.dv) + row_offset(p.sdv, bh, p.H, key) + coff, 1.0f,
+                valid);
             tmem_row_to_global<BF16, C::kOutCols>(
                 tmem + lane_off + C::kTmDK + part * C::kOutCols,
-                reinterpret_cast<uint8_t*>(p.dk) + roff, p.scale, valid);
+                reinterpret_cast<uint8_t*>(p.dk) + row_offset(p.sdk, bh, p.H, key) + coff, p.scale,
+                valid);
         }
     }
 
@@ -557,7 +561,7 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
             int issued_kv = 0, issued_q = 0, issued_o = 0;
             // Q_u and -LSE*log2e into Q slot u % kQStages (u counts query tiles over the CTA's
             // lifetime); query tile `qi` of head `bh`.
-            auto load_q = [&](int u, int bh, int qi) -> bool {
+            auto load_q = [&](int u, const DkdvItem& it, int qi) -> bool {
                 const int st = u % C::kQStages;
                 if (u >= C::kQStages &&
                     !wait_bounded(&bar_qe[st], ((uint32_t)(u / C::kQStages) & 1u) ^ 1u, abort_v,
@@ -565,15 +569,16 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                     return false;
                 mbar_arrive_expect_tx(&bar_qf[st], C::kTileBytes + C::kVecBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(smem + C::kOffQ + st * C::kTileBytes + c * kChunkBytes, &p.tm_q,
-                                &bar_qf[st], c * kChunkElems, qi * kTileRows, bh);
+                    tma_load_4d(smem + C::kOffQ + st * C::kTileBytes + c * kChunkBytes, &p.tm_q,
+                                &bar_qf[st], c * kChunkElems, qi * kTileRows, it.h, it.b);
                 bulk_load(smem + C::kOffNlse + st * C::kVecBytes,
-                          p.nlse2_pad + (size_t)bh * p.Lpad + (size_t)qi * kTileRows, C::kVecBytes,
+                          p.nlse2_pad + (size_t)it.bh * p.Lqpad + (size_t)qi * kTileRows,
+                          C::kVecBytes,
                           &bar_qf[st]);
                 issued_q = u + 1;
                 return true;
             };
-            auto load_do = [&](int u, int bh, int qi) -> bool {  // dO_u and Delta_u
+            auto load_do = [&](int u, const DkdvItem& it, int qi) -> bool {  // dO_u, Delta_u
                 const int st = u % C::kOStages;
                 if (u >= C::kOStages &&
                     !wait_bounded(&bar_oe[st], ((uint32_t)(u / C::kOStages) & 1u) ^ 1u, abort_v,
@@ -581,10 +586,11 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                     return false;
                 mbar_arrive_expect_tx(&bar_of[st], C::kTileBytes + C::kVecBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(smem + C::kOffDO + st * C::kTileBytes + c * kChunkBytes, &p.tm_do,
-                                &bar_of[st], c * kChunkElems, qi * kTileRows, bh);
+                    tma_load_4d(smem + C::kOffDO + st * C::kTileBytes + c * kChunkBytes, &p.tm_do,
+                                &bar_of[st], c * kChunkElems, qi * kTileRows, it.h, it.b);
                 bulk_load(smem + C::kOffDelta + st * C::kVecBytes,
-                          p.delta_pad + (size_t)bh * p.Lpad + (size_t)qi * kTileRows, C::kVecBytes,
+                          p.delta_pad + (size_t)it.bh * p.Lqpad + (size_t)qi * kTileRows,
+                          C::kVecBytes,
                           &bar_of[st]);
                 issued_o = u + 1;
                 return true;
@@ -603,17 +609,17 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                 }
                 mbar_arrive_expect_tx(&bar_kvf[kvs], 2 * C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_3d(k_tile(kvs) + c * kChunkBytes, &p.tm_k, &bar_kvf[kvs],
-                                c * kChunkElems, it.kt * kTileRows, it.bh);
-                    tma_load_3d(v_tile(kvs) + c * kChunkBytes, &p.tm_v, &bar_kvf[kvs],
-                                c * kChunkElems, it.kt * kTileRows, it.bh);
+                    tma_load_4d(k_tile(kvs) + c * kChunkBytes, &p.tm_k, &bar_kvf[kvs],
+                                c * kChunkElems, it.kt * kTileRows, it.h, it.b);
+                    tma_load_4d(v_tile(kvs) + c * kChunkBytes, &p.tm_v, &bar_kvf[kvs],
+                                c * kChunkElems, it.kt * kTileRows, it.h, it.b);
                 }
                 issued_kv = round + 1;
                 // Q runs one tile ahead of dO: Q_{t+1} only waits for dK_{t+1-kQStages}.
-                ok = load_q(u, it.bh, it.it0);
+                ok = load_q(u, it, it.it0);
                 for (int t = 0; ok && t < it.n_it; ++t) {
-                    if (t + 1 < it.n_it) ok = load_q(u + t + 1, it.bh, it.it0 + t + 1);
-                    ok = ok && load_do(u + t, it.bh, it.it0 + t);
+                    if (t + 1 < it.n_it) ok = load_q(u + t + 1, it, it.it0 + t + 1);
+                    ok = ok && load_do(u + t, it, it.it0 + t);
                 }
                 u += it.n_it;
             }
@@ -773,8 +779,8 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                     smem_u32(smem + C::kOffNlse + qs * C::kVecBytes) + c0 * 4;
                 const uint32_t dlt_addr = smem_u32(smem + C::kOffDelta + os * C::kVecBytes) + c0 * 4;
                 const int q0 = qi * kTileRows + c0;
-                const bool masked = (CAUSAL && qi == it.kt) || (qi * kTileRows + kTileRows > p.L);
-                const int qlim = p.L - 1;  // last valid query
+                const bool masked = tile_masked(qi, it.kt, p.Lq, p.Lk, CAUSAL);
+                const int qlim = p.Lq - 1;  // last valid query
                 // Phase 1: P^T = exp2(S^T * scale*log2e - LSE*log2e) on this warp's columns;
                 // kept in registers, and the S^T columns are released at once.
                 ok = wait_bounded(&bar_qf[qs], qph, abort_v, p.timeout_ns) &&
@@ -807,7 +813,7 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < kC; ++i) {
                             const int qg = q0 + i;
-                            if (qg > qlim || (CAUSAL && key > qg)) pv[i] = 0.0f;
+                            if (qg > qlim || (CAUSAL && key > qg + (p.Lk - p.Lq))) pv[i] = 0.0f;
                         }
                     }
 #pragma unroll
@@ -864,14 +870,16 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
             tc_fence_after_sync();
             // tcgen05.ld waits for its data: the read-out is complete before this warp publishes
             // P^T / dS^T of the next item, which is what lets dK / dV of that item start.
-            const bool valid = key < p.L;
-            const size_t roff = ((size_t)it.bh * p.L + key) * D * 2 + part * C::kOutCols * 2;
+            const bool valid = key < p.Lk;
+            const size_t coff = (size_t)part * C::kOutCols * 2;
             tmem_row_to_global<BF16, C::kOutCols>(
                 tmem + lane_off + C::kTmDV + part * C::kOutCols,
-                reinterpret_cast<uint8_t*>(p.dv) + roff, 1.0f, valid);
+                reinterpret_cast<uint8_t*>(p.dv) + row_offset(p.sdv, it.bh, p.H, key) + coff, 1.0f,
+                valid);
             tmem_row_to_global<BF16, C::kOutCols>(
                 tmem + lane_off + C::kTmDK + part * C::kOutCols,
-                reinterpret_cast<uint8_t*>(p.dk) + roff, p.scale, valid);
+                reinterpret_cast<uint8_t*>(p.dk) + row_offset(p.sdk, it.bh, p.H, key) + coff,
+                p.scale, valid);
             u = u_end;
         }
         if (!ok && lane == 0) record_timeout(p.status, abort_v);
@@ -890,14 +898,13 @@ cudaError_t launch_t(const BwdParams& p, cudaStream_t s) {
     using C = DkdvCfg<D, BF16, CAUSAL>;
     constexpr int kSmem = dkdv_smem_bytes<D, BF16, CAUSAL>();
     static_assert(kSmem <= 232448, "dynamic shared memory over the 227 KB per-block limit");
-    const int total = p.n_tiles * p.BH;
-    const int grid = dkdv_grid(p.n_tiles, p.BH, CAUSAL, sm_count());
+    const int total = p.n_ktiles * p.BH;
+    const int grid = dkdv_grid(p.Lq, p.Lk, p.BH, CAUSAL, sm_count());
     auto kern = grid < total ? fa_bwd_dkdv_kernel_persistent<D, BF16, CAUSAL>
                              : fa_bwd_dkdv_kernel<D, BF16, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)grid, C::kThreads, kSmem, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(kern, (unsigned)grid, C::kThreads, kSmem, s, p);
 }
 
 }  // namespace

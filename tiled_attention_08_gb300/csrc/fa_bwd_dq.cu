@@ -100,9 +100,13 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
     // Heads in L2-sized groups (their K/V are streamed by every query tile); inside a group
     // the heaviest query tiles first.
     int bh, rank;
-    tile_coords(blockIdx.x, p.BH, p.n_tiles, p.group, bh, rank);
-    const int qt = p.n_tiles - 1 - rank;
-    const int n_kv = CAUSAL ? (qt + 1) : p.n_tiles;
+    tile_coords(blockIdx.x, p.BH, p.n_qtiles, p.group, bh, rank);
+    const int hb = bh / p.H, hh = bh - hb * p.H;  // batch and head of bh
+    const int qt = p.n_qtiles - 1 - rank;
+    const int n_kv = q_tile_kv(qt, p.Lq, p.Lk, CAUSAL);
+    // No row of this query tile sees a key (causal with Lq > Lk): the preprocess kernel has
+    // written its dQ rows (zeros), so the whole CTA leaves before setting anything up.
+    if (n_kv == 0) return;
     volatile int* abort_v = &abort_flag;
 
     if (threadIdx.x == 0) {
@@ -137,8 +141,8 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
             tma_prefetch_desc(&p.tm_q);
             mbar_arrive_expect_tx(&bar_q, C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c)
-                tma_load_3d(smem + C::kOffQ + c * kChunkBytes, &p.tm_q, &bar_q, c * kChunkElems,
-                            qt * kTileRows, bh);
+                tma_load_4d(smem + C::kOffQ + c * kChunkBytes, &p.tm_q, &bar_q, c * kChunkElems,
+                            qt * kTileRows, hh, hb);
             bool ok = true;
             int issued = 0;
             for (int j = 0; j < n_kv; ++j) {
@@ -150,10 +154,10 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
                 }
                 mbar_arrive_expect_tx(&bar_kvf[st], 2 * C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_3d(smem + C::kOffK + st * C::kTileBytes + c * kChunkBytes, &p.tm_k,
-                                &bar_kvf[st], c * kChunkElems, j * kTileRows, bh);
-                    tma_load_3d(smem + C::kOffV + st * C::kTileBytes + c * kChunkBytes, &p.tm_v,
-                                &bar_kvf[st], c * kChunkElems, j * kTileRows, bh);
+                    tma_load_4d(smem + C::kOffK + st * C::kTileBytes + c * kChunkBytes, &p.tm_k,
+                                &bar_kvf[st], c * kChunkElems, j * kTileRows, hh, hb);
+                    tma_load_4d(smem + C::kOffV + st * C::kTileBytes + c * kChunkBytes, &p.tm_v,
+                                &bar_kvf[st], c * kChunkElems, j * kTileRows, hh, hb);
                 }
                 issued = j + 1;
             }
@@ -251,17 +255,17 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
         const int part = warp >> 2;             // which kC key columns
         const int row = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        const int q_row = qt * kTileRows + row;  // < Lpad always
+        const int q_row = qt * kTileRows + row;  // < Lqpad always
         const int c0 = part * kC;
         // Stage this warp's slice (D/kSplit elements) of the dO row into TMEM as packed 16-bit
         // pairs; rows past L are zeros.
         {
             constexpr int kE = D / C::kSplit;       // elements per warp slice
             constexpr int kW = C::kStageCols;       // packed 32-bit columns per slice
-            const bool valid = q_row < p.L;
-            const size_t eoff = ((size_t)bh * p.L + q_row) * D + part * kE;
+            const bool valid = q_row < p.Lq;
             const uint4* src = reinterpret_cast<const uint4*>(
-                reinterpret_cast<const uint8_t*>(p.dout) + eoff * 2);
+                reinterpret_cast<const uint8_t*>(p.dout) + row_offset(p.sdo, bh, p.H, q_row) +
+                (size_t)part * kE * 2);
             uint32_t w[kW];
 #pragma unroll
             for (int v = 0; v < kW / 4; ++v) {
@@ -276,14 +280,14 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
             tc_fence_before_sync();
             mbar_arrive(&bar_qt);
         }
-        const float nlse2 = p.nlse2_pad[(size_t)bh * p.Lpad + q_row];  // -LSE * log2(e)
-        const float dlt = p.delta_pad[(size_t)bh * p.Lpad + q_row];
+        const float nlse2 = p.nlse2_pad[(size_t)bh * p.Lqpad + q_row];  // -LSE * log2(e)
+        const float dlt = p.delta_pad[(size_t)bh * p.Lqpad + q_row];
         const uint64_t dlt2 = f2_make(dlt, dlt);
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             const int key0 = j * kTileRows + c0;
-            const bool masked = (CAUSAL && j == n_kv - 1) || (j * kTileRows + kTileRows > p.L);
-            const int klim = CAUSAL ? min(p.L - 1, q_row) : (p.L - 1);
+            const bool masked = tile_masked(qt, j, p.Lq, p.Lk, CAUSAL);
+            const int klim = CAUSAL ? min(p.Lk - 1, q_row + (p.Lk - p.Lq)) : (p.Lk - 1);
             const uint32_t par = (uint32_t)j & 1u;
             float pv[kC];
             ok = wait_bounded(&bar_sf, par, abort_v, p.timeout_ns);
@@ -360,9 +364,9 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
         } else {
             tc_fence_after_sync();
             uint8_t* dst_row = reinterpret_cast<uint8_t*>(p.dq) +
-                               ((size_t)bh * p.L + q_row) * D * 2 + part * C::kOutCols * 2;
+                               row_offset(p.sdq, bh, p.H, q_row) + part * C::kOutCols * 2;
             tmem_row_to_global<BF16, C::kOutCols>(tmem + lane_off + C::kTmDQ + part * C::kOutCols,
-                                                  dst_row, p.scale, q_row < p.L);
+                                                  dst_row, p.scale, q_row < p.Lq);
         }
     }
 
@@ -403,17 +407,20 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
     volatile int* abort_v = &abort_flag;
     // Persistent CTAs: this CTA's query tiles in round order (persistent_tile); inside each
     // round the ids follow tile_coords (heads in L2-sized groups, heaviest tiles first).
-    const int total = p.n_tiles * p.BH;
+    // (The launcher uses this kernel only when every query tile sees at least one key.)
+    const int total = p.n_qtiles * p.BH;
     struct Tile {
-        int bh, qt, n_kv;
+        int bh, b, h, qt, n_kv;
     };
     auto tile_of = [&](int round, Tile& t) -> bool {
         const int id = persistent_tile(round, (int)blockIdx.x, (int)gridDim.x, total);
         if (id < 0) return false;
         int rank;
-        tile_coords(id, p.BH, p.n_tiles, p.group, t.bh, rank);
-        t.qt = p.n_tiles - 1 - rank;
-        t.n_kv = CAUSAL ? (t.qt + 1) : p.n_tiles;
+        tile_coords(id, p.BH, p.n_qtiles, p.group, t.bh, rank);
+        t.b = t.bh / p.H;
+        t.h = t.bh - t.b * p.H;
+        t.qt = p.n_qtiles - 1 - rank;
+        t.n_kv = q_tile_kv(t.qt, p.Lq, p.Lk, CAUSAL);
         return true;
     };
 
@@ -464,8 +471,8 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
                 }
                 mbar_arrive_expect_tx(&bar_q, C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(smem + C::kOffQ + c * kChunkBytes, &p.tm_q, &bar_q,
-                                c * kChunkElems, t.qt * kTileRows, t.bh);
+                    tma_load_4d(smem + C::kOffQ + c * kChunkBytes, &p.tm_q, &bar_q,
+                                c * kChunkElems, t.qt * kTileRows, t.h, t.b);
                 ++q_loads;
                 for (int j = 0; j < t.n_kv; ++j) {
                     const int st = gk % C::kStages;
@@ -477,10 +484,12 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
                     }
                     mbar_arrive_expect_tx(&bar_kvf[st], 2 * C::kTileBytes);
                     for (int c = 0; c < C::kChunks; ++c) {
-                        tma_load_3d(smem + C::kOffK + st * C::kTileBytes + c * kChunkBytes,
-                                    &p.tm_k, &bar_kvf[st], c * kChunkElems, j * kTileRows, t.bh);
-                        tma_load_3d(smem + C::kOffV + st * C::kTileBytes + c * kChunkBytes,
-                                    &p.tm_v, &bar_kvf[st], c * kChunkElems, j * kTileRows, t.bh);
+                        tma_load_4d(smem + C::kOffK + st * C::kTileBytes + c * kChunkBytes,
+                                    &p.tm_k, &bar_kvf[st], c * kChunkElems, j * kTileRows, t.h,
+                                    t.b);
+                        tma_load_4d(smem + C::kOffV + st * C::kTileBytes + c * kChunkBytes,
+                                    &p.tm_v, &bar_kvf[st], c * kChunkElems, j * kTileRows, t.h,
+                                    t.b);
                     }
                     ++gk;
                 }
@@ -603,11 +612,11 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
         auto stage_do = [&](const Tile& t, float& nl, float& dl) {
             constexpr int kE = D / C::kSplit;       // elements per warp slice
             constexpr int kW = C::kStageCols;       // packed 32-bit columns per slice
-            const int q_row = t.qt * kTileRows + row;  // < Lpad always
-            const bool valid = q_row < p.L;
-            const size_t eoff = ((size_t)t.bh * p.L + q_row) * D + part * kE;
+            const int q_row = t.qt * kTileRows + row;  // < Lqpad always
+            const bool valid = q_row < p.Lq;
             const uint4* src = reinterpret_cast<const uint4*>(
-                reinterpret_cast<const uint8_t*>(p.dout) + eoff * 2);
+                reinterpret_cast<const uint8_t*>(p.dout) + row_offset(p.sdo, t.bh, p.H, q_row) +
+                (size_t)part * kE * 2);
             uint32_t w[kW];
 #pragma unroll
             for (int v = 0; v < kW / 4; ++v) {
@@ -617,8 +626,8 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
                 w[4 * v + 2] = x.z;
                 w[4 * v + 3] = x.w;
             }
-            nl = p.nlse2_pad[(size_t)t.bh * p.Lpad + q_row];
-            dl = p.delta_pad[(size_t)t.bh * p.Lpad + q_row];
+            nl = p.nlse2_pad[(size_t)t.bh * p.Lqpad + q_row];
+            dl = p.delta_pad[(size_t)t.bh * p.Lqpad + q_row];
             tmem_st<kW>(tmem + lane_off + C::kTmDO + part * kW, w);
             tmem_st_wait();
             tc_fence_before_sync();
@@ -633,13 +642,13 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
             const bool has_next = tile_of(round + 1, nxt);
             const int n = cur.n_kv;
             const int q_row = cur.qt * kTileRows + row;
-            const int klim = CAUSAL ? min(p.L - 1, q_row) : (p.L - 1);
+            const int klim = CAUSAL ? min(p.Lk - 1, q_row + (p.Lk - p.Lq)) : (p.Lk - 1);
             const uint64_t dlt2 = f2_make(dlt, dlt);
             float nlse2_n = 0.0f, dlt_n = 0.0f;
             for (int j = 0; j < n; ++j) {
                 const int gg = g + j;
                 const int key0 = j * kTileRows + c0;
-                const bool masked = (CAUSAL && j == n - 1) || (j * kTileRows + kTileRows > p.L);
+                const bool masked = tile_masked(cur.qt, j, p.Lq, p.Lk, CAUSAL);
                 const uint32_t par = (uint32_t)gg & 1u;
                 float pv[kC];
                 ok = wait_bounded(&bar_sf, par, abort_v, p.timeout_ns);
@@ -719,9 +728,9 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
             if (!ok) break;
             tc_fence_after_sync();
             uint8_t* dst_row = reinterpret_cast<uint8_t*>(p.dq) +
-                               ((size_t)cur.bh * p.L + q_row) * D * 2 + part * C::kOutCols * 2;
+                               row_offset(p.sdq, cur.bh, p.H, q_row) + part * C::kOutCols * 2;
             tmem_row_to_global<BF16, C::kOutCols>(tmem + lane_off + C::kTmDQ + part * C::kOutCols,
-                                                  dst_row, p.scale, q_row < p.L);
+                                                  dst_row, p.scale, q_row < p.Lq);
             tc_fence_before_sync();
             mbar_arrive(&bar_dqr);  // the accumulator is read: the next tile may overwrite it
             g += n;
@@ -744,23 +753,22 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
 template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_t(const BwdParams& p, cudaStream_t s) {
     using C = DqCfg<D, BF16, CAUSAL>;
-    const int total = p.n_tiles * p.BH;
-    const int grid = dq_grid(p.n_tiles, p.BH, CAUSAL, sm_count());
-    if (grid < total) {
+    const int total = p.n_qtiles * p.BH;
+    const int grid = dq_grid(p.Lq, p.Lk, p.BH, CAUSAL, sm_count());
+    // The persistent kernel needs every query tile to see a key; only the first tile can fail to.
+    if (grid < total && q_tile_kv(0, p.Lq, p.Lk, CAUSAL) > 0) {
         // Persistent: one CTA per SM (each fills an SM).
         auto kern = fa_bwd_dq_kernel_persistent<D, BF16, CAUSAL>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
-        kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, s>>>(p);
-        return cudaGetLastError();
+        return launch_kernel(kern, (unsigned)grid, C::kThreads, C::kSmemBytes, s, p);
     }
     auto kern = fa_bwd_dq_kernel<D, BF16, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)total, C::kThreads, C::kSmemBytes, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(kern, (unsigned)total, C::kThreads, C::kSmemBytes, s, p);
 }
 
 }  // namespace

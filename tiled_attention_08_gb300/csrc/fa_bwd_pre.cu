@@ -5,7 +5,9 @@
 // dS = P o (dP - Delta) needs one scalar per query row, Delta_i = rowsum(P o dP), which equals
 // rowsum(dO o O) because O = P V; this kernel computes it from O and dO in one streaming pass.
 // Both per-row vectors go to a workspace padded to a whole number of 128-row tiles (zeros past
-// L), so the backward kernels can copy them tile by tile with aligned bulk copies.
+// Lq), so the backward kernels can copy them tile by tile with aligned bulk copies.  Rows that
+// see no key (the first Lq - Lk queries under the causal mask when Lq > Lk) get dQ = 0 here;
+// the dQ pass skips query tiles in which no row sees a key.
 //
 // HBM-bound: every (row, D) element of O and dO is read once, with 16-byte loads; D/8 threads
 // share a row and reduce with shuffles.
@@ -17,26 +19,32 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Block (x, y) covers 128-row tile x of heads y, y + gridDim.y, ...: the head's base addresses
+// are worked out once per block, so a row costs one multiply-add per operand, and the block's
+// threads walk the tile in passes of 256/G rows, one row per thread per pass.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdPreParams p) {
-    constexpr int G = D / 8;              // threads per row (8 elements each)
-    constexpr int kRowsPerBlock = 256 / G;
+    constexpr int G = D / 8;                   // threads per row (8 elements each)
+    constexpr int kRowsPerPass = 256 / G;
     const int g = threadIdx.x % G;
-    const long long total = (long long)p.BH * p.Lpad;
-    const long long stride = (long long)gridDim.x * kRowsPerBlock;
-    for (long long base = (long long)blockIdx.x * kRowsPerBlock; base < total; base += stride) {
-        const long long row = base + threadIdx.x / G;  // uniform loop trip count per warp
-        float acc = 0.0f;
-        int bh = 0, i = 0;
-        if (row < total) {
-            bh = (int)(row / p.Lpad);
-            i = (int)(row % p.Lpad);
-            if (i < p.L) {
-                const size_t off = ((size_t)bh * p.L + i) * D + g * 8;
-                const uint4 a = *reinterpret_cast<const uint4*>(
-                    reinterpret_cast<const uint8_t*>(p.o) + off * 2);
-                const uint4 b = *reinterpret_cast<const uint4*>(
-                    reinterpret_cast<const uint8_t*>(p.dout) + off * 2);
+    const int i0 = blockIdx.x * kTileRows + threadIdx.x / G;
+    for (int bh = blockIdx.y; bh < p.BH; bh += gridDim.y) {
+        const uint8_t* o_head =
+            reinterpret_cast<const uint8_t*>(p.o) + row_offset(p.so, bh, p.H, 0) + g * 16;
+        const uint8_t* d_head =
+            reinterpret_cast<const uint8_t*>(p.dout) + row_offset(p.sdo, bh, p.H, 0) + g * 16;
+        uint8_t* q_head = reinterpret_cast<uint8_t*>(p.dq) + row_offset(p.sdq, bh, p.H, 0) + g * 16;
+        const size_t o_step = (size_t)p.so.l * 2u, d_step = (size_t)p.sdo.l * 2u;
+#pragma unroll 2
+        for (int pass = 0; pass < kTileRows / kRowsPerPass; ++pass) {
+            const int i = i0 + pass * kRowsPerPass;
+            float acc = 0.0f;
+            if (i < p.Lq) {
+                const uint4 a = *reinterpret_cast<const uint4*>(o_head + (size_t)i * o_step);
+                const uint4 b = *reinterpret_cast<const uint4*>(d_head + (size_t)i * d_step);
+                if (i < p.first_seen_row)
+                    *reinterpret_cast<uint4*>(q_head + (size_t)i * (size_t)p.sdq.l * 2u) =
+                        make_uint4(0u, 0u, 0u, 0u);
                 const uint32_t av[4] = {a.x, a.y, a.z, a.w};
                 const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
@@ -47,29 +55,22 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdPreParams p) {
                     acc = fmaf(x.y, y.y, acc);
                 }
             }
-        }
 #pragma unroll
-        for (int w = G / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w, G);
-        if (g == 0 && row < total) {
-            p.delta_pad[row] = acc;
-            p.nlse2_pad[row] = (i < p.L) ? -(p.lse[(size_t)bh * p.L + i] * kLog2e) : 0.0f;
+            for (int w = G / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w, G);
+            if (g == 0) {
+                const size_t row = (size_t)bh * p.Lqpad + i;
+                p.delta_pad[row] = acc;
+                p.nlse2_pad[row] = (i < p.Lq) ? -(p.lse[(size_t)bh * p.Lq + i] * kLog2e) : 0.0f;
+            }
         }
     }
 }
 
 template <int D, bool BF16>
 cudaError_t launch_t(const BwdPreParams& p, cudaStream_t s) {
-    constexpr int kRowsPerBlock = 256 / (D / 8);
-    const long long total = (long long)p.BH * p.Lpad;
-    long long blocks = (total + kRowsPerBlock - 1) / kRowsPerBlock;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long cap = (long long)sms * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    fa_bwd_pre_kernel<D, BF16><<<(unsigned)blocks, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    const unsigned tiles = (unsigned)(p.Lqpad / kTileRows);
+    const unsigned heads = p.BH < 65535 ? (unsigned)p.BH : 65535u;
+    return launch_kernel(fa_bwd_pre_kernel<D, BF16>, dim3(tiles, heads), dim3(256), 0, s, p);
 }
 
 }  // namespace

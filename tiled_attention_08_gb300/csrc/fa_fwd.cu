@@ -97,12 +97,14 @@ struct FwdCfg {
 
 // One work item: a pair of query tiles of one head and the key tiles each of them sees.
 struct FwdItem {
-    int bh, q_a, q_b, n_kv_a, n_kv_b, n_kv;  // n_kv_b = 0 when the pair has no tile B
+    int bh, q_a, q_b;
+    int n_kv_a, n_kv_b, n_kv;  // key tiles of tile A, of tile B (0 also when there is no tile
+                               // B) and of the pair; 0 when no row of the tile (pair) sees a key
 };
 
 template <bool CAUSAL>
 __device__ __forceinline__ bool fwd_item(const FwdParams& p, int round, FwdItem& it) {
-    const int n_pairs = (p.n_tiles + 1) >> 1;
+    const int n_pairs = (p.n_qtiles + 1) >> 1;
     const int id = persistent_tile(round, (int)blockIdx.x, (int)gridDim.x, n_pairs * p.BH);
     if (id < 0) return false;
     int rank;
@@ -110,10 +112,10 @@ __device__ __forceinline__ bool fwd_item(const FwdParams& p, int round, FwdItem&
     const int pair = n_pairs - 1 - rank;  // heaviest pairs (most key tiles) first
     it.q_a = 2 * pair;
     it.q_b = 2 * pair + 1;
-    const bool has_b = it.q_b < p.n_tiles;
-    it.n_kv_a = CAUSAL ? it.q_a + 1 : p.n_tiles;
-    it.n_kv_b = has_b ? (CAUSAL ? it.q_b + 1 : p.n_tiles) : 0;
-    it.n_kv = has_b ? it.n_kv_b : it.n_kv_a;  // n_kv_a <= n_kv_b
+    const bool has_b = it.q_b < p.n_qtiles;
+    it.n_kv_a = q_tile_kv(it.q_a, p.Lq, p.Lk, CAUSAL);
+    it.n_kv_b = has_b ? q_tile_kv(it.q_b, p.Lq, p.Lk, CAUSAL) : 0;
+    it.n_kv = it.n_kv_b > it.n_kv_a ? it.n_kv_b : it.n_kv_a;  // n_kv_a <= n_kv_b
     return true;
 }
 
@@ -186,6 +188,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
             int n_q = 0;     // Q pair fills handed to the TMA unit
             FwdItem it;
             for (int round = 0; ok && fwd_item<CAUSAL>(p, round, it); ++round) {
+                if (it.n_kv == 0) continue;  // no row sees a key: the softmax warps write it
+                const int hb = it.bh / p.H, hh = it.bh - hb * p.H;  // batch and head
                 if (is_k) {
                     const int qs = n_q % C::kQSlots;
                     const int use = n_q / C::kQSlots;  // earlier uses of this slot
@@ -198,8 +202,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                     mbar_arrive_expect_tx(&bar_qf[qs], nt * C::kTileBytes);
                     for (int t = 0; t < nt; ++t)
                         for (int c = 0; c < C::kChunks; ++c)
-                            tma_load_3d(q_tile(qs, t) + c * kChunkBytes, &p.tm_q, &bar_qf[qs],
-                                        c * kChunkElems, (t ? it.q_b : it.q_a) * kTileRows, it.bh);
+                            tma_load_4d(q_tile(qs, t) + c * kChunkBytes, &p.tm_q, &bar_qf[qs],
+                                        c * kChunkElems, (t ? it.q_b : it.q_a) * kTileRows, hh, hb);
                     ++n_q;
                 }
                 for (int j = 0; j < it.n_kv; ++j) {
@@ -212,11 +216,11 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                     }
                     mbar_arrive_expect_tx(&full[st], kFill);
                     for (int c = 0; c < C::kChunks; ++c) {
-                        tma_load_3d(ring + st * C::kTileBytes + c * kChunkBytes, map, &full[st],
-                                    c * kChunkElems, j * kTileRows, it.bh);
+                        tma_load_4d(ring + st * C::kTileBytes + c * kChunkBytes, map, &full[st],
+                                    c * kChunkElems, j * kTileRows, hh, hb);
                         if constexpr (C::kMergedKV)
-                            tma_load_3d(smem + C::kOffV + st * C::kTileBytes + c * kChunkBytes,
-                                        &p.tm_v, &full[st], c * kChunkElems, j * kTileRows, it.bh);
+                            tma_load_4d(smem + C::kOffV + st * C::kTileBytes + c * kChunkBytes,
+                                        &p.tm_v, &full[st], c * kChunkElems, j * kTileRows, hh, hb);
                     }
                     ++issued;
                 }
@@ -251,7 +255,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
             return true;
         };
         FwdItem it;
-        for (int round = 0; ok && fwd_item<CAUSAL>(p, round, it); ++round, ++n_item) {
+        for (int round = 0; ok && fwd_item<CAUSAL>(p, round, it); ++round) {
+            if (it.n_kv == 0) continue;  // no row of the pair sees a key
             const int qs = n_item % C::kQSlots;
             const int n_kv = it.n_kv;
             const int nk[2] = {it.n_kv_a, it.n_kv_b};
@@ -290,7 +295,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
             tc_fence_after_sync();
             ok = ok && wait_k(g);
             if (!ok) break;
-            issue_s(0, g);
+            if (nk[0] > 0) issue_s(0, g);
             if (nk[1] > 0) issue_s(1, g);
             if (n_kv == 1) mma_commit_w(&bar_qe[qs]);  // every S of the item issued
             if constexpr (!C::kMergedKV) mma_commit_w(&bar_ke[g % C::kKStages]);  // K_0 read
@@ -335,6 +340,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
             g += n_kv;
             ps[0] += nk[0];
             ps[1] += nk[1];
+            ++n_item;
         }
         if (!ok && lane == 0) record_timeout(p.status, abort_v);
         // Every issued MMA must finish before TMEM is released.
@@ -355,8 +361,9 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
         FwdItem it;
         for (int round = 0; ok && fwd_item<CAUSAL>(p, round, it); ++round) {
             const int n_mine = t ? it.n_kv_b : it.n_kv_a;
-            if (n_mine == 0) continue;  // a pair without tile B
             const int q_row = (t ? it.q_b : it.q_a) * kTileRows + row;
+            // No tile B, or no row of this tile sees a key (fa_fwd_empty_rows_kernel writes it).
+            if (n_mine == 0) continue;
             float m_ref = -INFINITY;
             float l_sum = 0.0f;
             for (int j = 0; j < n_mine; ++j) {
@@ -372,8 +379,9 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                     for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(r[i]);
                 }
                 const int key0 = j * kTileRows;
-                if ((CAUSAL && j == n_mine - 1) || key0 + kTileRows > p.L) {
-                    const int lim = CAUSAL ? min(p.L - 1, q_row) : (p.L - 1);
+                if (key0 + kTileRows - 1 >
+                    (CAUSAL ? min(p.Lk - 1, (q_row & ~(kTileRows - 1)) + (p.Lk - p.Lq)) : p.Lk - 1)) {
+                    const int lim = CAUSAL ? min(p.Lk - 1, q_row + (p.Lk - p.Lq)) : p.Lk - 1;
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
                         if (key0 + c > lim) s[c] = -INFINITY;
@@ -430,13 +438,14 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after_sync();
-            const bool valid = q_row < p.L;
-            if (valid) p.lse[(size_t)it.bh * p.L + q_row] = (m_ref + log2f(l_sum)) * kLn2;
-            uint8_t* orow =
-                reinterpret_cast<uint8_t*>(p.o) + ((size_t)it.bh * p.L + q_row) * D * 2;
+            const bool valid = q_row < p.Lq;
+            if (valid)
+                p.lse[(size_t)it.bh * p.Lq + q_row] =
+                    l_sum > 0.0f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
+            uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) + row_offset(p.so, it.bh, p.H, q_row);
             // The read-out finishes (tcgen05.ld waits) before this group publishes P_t0 of the
             // next item, which is what lets PV_t0 overwrite O_t.
-            tmem_row_to_global<BF16, D>(o_addr, orow, 1.0f / l_sum, valid);
+            tmem_row_to_global<BF16, D>(o_addr, orow, l_sum > 0.0f ? 1.0f / l_sum : 0.0f, valid);
             ps += n_mine;
             ++n_done;
         }
@@ -451,6 +460,25 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
     }
 }
 
+// Rows that see no key (the first Lq - Lk query rows under the causal mask when Lq > Lk): O = 0
+// and LSE = -inf.  Enqueued only for such shapes; the attention kernel skips the query tiles in
+// which no row sees a key and writes the same values for such rows of the tiles it does run.
+template <int D>
+__global__ void __launch_bounds__(256) fa_fwd_empty_rows_kernel(const FwdParams p, int rows) {
+    constexpr int kChunks16 = D / 8;  // 16-byte pieces of a row
+    const long long total = (long long)p.BH * rows * kChunks16;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int c = (int)(e % kChunks16);
+        const long long r_all = e / kChunks16;
+        const int bh = (int)(r_all / rows), r = (int)(r_all - (long long)bh * rows);
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.o) +
+                                              row_offset(p.so, bh, p.H, r));
+        dst[c] = make_uint4(0u, 0u, 0u, 0u);
+        if (c == 0) p.lse[(size_t)bh * p.Lq + r] = -INFINITY;
+    }
+}
+
 template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_t(const FwdParams& p, cudaStream_t s) {
     using C = FwdCfg<D, BF16, CAUSAL>;
@@ -458,13 +486,25 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int n_pairs = (p.n_tiles + 1) / 2;
-    const int grid = fwd_grid(n_pairs, p.n_tiles, p.BH, CAUSAL, sm_count());
+    const int n_pairs = (p.n_qtiles + 1) / 2;
+    const int grid = fwd_grid(p.Lq, p.Lk, p.BH, CAUSAL, sm_count());
     kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+cudaError_t launch_fwd_empty_rows(const FwdParams& p, int D, int rows, cudaStream_t s) {
+    const long long work = (long long)p.BH * rows * (D / 8);
+    const int sms = sm_count() > 0 ? sm_count() : 148;
+    long long blocks = (work + 255) / 256;
+    if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
+    if (blocks < 1) blocks = 1;
+    return D == 64 ? launch_kernel(fa_fwd_empty_rows_kernel<64>, dim3((unsigned)blocks), dim3(256),
+                                   0, s, p, rows)
+                   : launch_kernel(fa_fwd_empty_rows_kernel<128>, dim3((unsigned)blocks),
+                                   dim3(256), 0, s, p, rows);
+}
 
 cudaError_t launch_fwd(const FwdParams& p, int D, bool bf16, bool causal, cudaStream_t s) {
     if (D == 64) {

@@ -35,13 +35,25 @@ __host__ __device__ __forceinline__ void tile_coords(int tile_id, int BH, int n_
     bh = g * group + (r - rank * heads);
 }
 
+// Element strides of a [B, H, L, D] view whose D elements are contiguous (a row): contiguous
+// [B,H,L,D], [B,L,H,D] and the q/k/v parts of a packed [B,L,3,H,D] tensor are all of this form.
+struct Strides {
+    long long b, h, l;
+};
+
+// Byte offset of row `row` of head `bh` (= b*H + h) of a 16-bit tensor with strides `s`.
+__host__ __device__ __forceinline__ size_t row_offset(const Strides& s, int bh, int H, int row) {
+    const int b = bh / H, h = bh - b * H;
+    return (size_t)((long long)b * s.b + (long long)h * s.h + (long long)row * s.l) * 2u;
+}
+
 struct FwdParams {
-    CUtensorMap tm_q, tm_k, tm_v;  // [BH, L, D] 16-bit, box {64, 128, 1}
-    void* o;                       // [BH, L, D] 16-bit
-    float* lse;                    // [BH, L] natural-log LSE
-    int L;
-    int BH;
-    int n_tiles;        // ceil(L / 128)
+    CUtensorMap tm_q, tm_k, tm_v;  // 16-bit {D, L, H, B} (strided), box {64, 128, 1, 1}
+    void* o;                       // [B, H, Lq, D] 16-bit, strides so
+    Strides so;
+    float* lse;                    // [B*H, Lq] natural-log LSE (contiguous)
+    int Lq, Lk, H, BH;
+    int n_qtiles, n_ktiles;  // ceil(Lq / 128), ceil(Lk / 128)
     int group;          // heads per schedule group (tile_coords)
     float scale_log2;   // |scale| * log2(e)
     uint32_t s_negate;  // kIdescNegateA when scale < 0 (S is computed as -Q K^T), else 0
@@ -50,24 +62,29 @@ struct FwdParams {
 };
 
 struct BwdPreParams {
-    const void* o;       // [BH, L, D]
-    const void* dout;    // [BH, L, D]
-    const float* lse;    // [BH, L]
-    float* nlse2_pad;    // [BH, Lpad]: -LSE * log2(e), zero past L
-    float* delta_pad;    // [BH, Lpad]: rowsum(dO * O), zero past L
-    int L, Lpad, BH, D;
+    const void* o;       // [B, H, Lq, D], strides so
+    const void* dout;    // [B, H, Lq, D], strides sdo
+    void* dq;            // [B, H, Lq, D], strides sdq: rows that see no key are zeroed here
+    Strides so, sdo, sdq;
+    const float* lse;    // [BH, Lq]
+    float* nlse2_pad;    // [BH, Lqpad]: -LSE * log2(e), zero past Lq
+    float* delta_pad;    // [BH, Lqpad]: rowsum(dO * O), zero past Lq
+    int Lq, Lqpad, H, BH, D;
+    int first_seen_row;  // rows below this see no key (causal with Lq > Lk), else 0
     int bf16;
 };
 
 struct BwdParams {
-    CUtensorMap tm_q, tm_k, tm_v, tm_do;  // [BH, L, D] 16-bit, box {64, 128, 1}
-    const void* dout;                     // [BH, L, D] (rows staged into TMEM by the dQ pass)
-    const float* nlse2_pad;               // [BH, Lpad]: -LSE * log2(e)
-    const float* delta_pad;               // [BH, Lpad]
-    void* dq;                             // [BH, L, D]
-    void* dk;
-    void* dv;
-    int L, Lpad, BH, n_tiles;
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 16-bit {D, L, H, B} (strided), box {64, 128, 1, 1}
+    const void* dout;                     // rows staged into TMEM by the dQ pass
+    Strides sdo;
+    const float* nlse2_pad;               // [BH, Lqpad]: -LSE * log2(e)
+    const float* delta_pad;               // [BH, Lqpad]
+    void* dq;                             // [B, H, Lq, D]
+    void* dk;                             // [B, H, Lk, D]
+    void* dv;                             // [B, H, Lk, D]
+    Strides sdq, sdk, sdv;
+    int Lq, Lk, Lqpad, H, BH, n_qtiles, n_ktiles;
     int group;          // heads per schedule group (tile_coords)
     float scale;        // softmax scale (applied to dQ and dK)
     float scale_log2;   // scale * log2(e)
@@ -86,8 +103,23 @@ int bwd_check_args(const void* q, const void* k, const void* v, const void* o, c
                    const float* lse, const void* dq, const void* dk, const void* dv, int B, int H,
                    int L, int D, float scale, int causal, int dtype, size_t* ws_need);
 
+// Enqueues kern<<<grid, block, smem, s>>>(args...) and returns the status of that launch alone.
+// (cudaGetLastError after a <<<>>> launch would also report a stale error left on the calling
+// thread by any earlier runtime call, for example by a framework's set-up of its own threads.)
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Launchers (one per kernel unit).  Return the launch error, if any.
 cudaError_t launch_fwd(const FwdParams& p, int D, bool bf16, bool causal, cudaStream_t s);
+cudaError_t launch_fwd_empty_rows(const FwdParams& p, int D, int rows, cudaStream_t s);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdParams& p, int D, bool bf16, bool causal, cudaStream_t s);
 cudaError_t launch_bwd_dq(const BwdParams& p, int D, bool bf16, bool causal, cudaStream_t s);
