@@ -7,6 +7,8 @@ never does, and shares no code with it.
 * ``forward`` / ``backward`` call the plain C definition in ``oracle.c`` (materialised S
   and P in fp64; see the header of that file for the formulas and their sources).
 * ``probs`` returns the full probability matrix of one head.
+* ``decode_paged`` is one decode step over a paged key/value cache (one new query row per
+  sequence attending to its cached tokens, gathered through the block table).
 * ``online_forward`` is a second, independent fp64 routine in numpy that runs the
   streaming recurrence the pages describe ("FlashAttention data-flow optimisation: MI50
   memory and bandwidth bottlenecks", section 2.2, first layer: Q split into row blocks
@@ -64,6 +66,10 @@ def _load():
             lib.oracle_probs_f64.argtypes = [dp, dp, dp, L, L, L, ctypes.c_double,
                                              ctypes.c_int]
             lib.oracle_probs_f64.restype = ctypes.c_int
+            ip = ctypes.POINTER(ctypes.c_int)
+            lib.oracle_decode_paged_f64.argtypes = [dp, dp, dp, ip, ip, dp, dp, L, L, L, L, L, L,
+                                                    ctypes.c_double]
+            lib.oracle_decode_paged_f64.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -198,4 +204,29 @@ def online_forward(q, k, v, scale: float, causal: bool, block_q: int, block_k: i
             m = m_new
         o[r0:r1] = acc / l[:, None]
         lse[r0:r1] = m + np.log(l)
+    return o, lse
+
+
+def decode_paged(q, k_cache, v_cache, block_tables, seq_lens, scale: float):
+    """O [B,H,D] and LSE [B,H] of one decode step over a paged cache, in fp64.
+
+    q: [B,H,D]; k_cache, v_cache: [num_pages, H, page, D]; block_tables: [B, max_pages] ints;
+    seq_lens: [B] ints (cached tokens per sequence, the newest included)."""
+    q = _f64(q)
+    kc = _f64(k_cache)
+    vc = _f64(v_cache)
+    bt = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    B, H, D = q.shape
+    num_pages, Hc, page, Dc = kc.shape
+    if Hc != H or Dc != D or vc.shape != kc.shape or bt.shape[0] != B or sl.shape != (B,):
+        raise ValueError("shapes of q, the caches, the block table and seq_lens disagree")
+    o = np.empty_like(q)
+    lse = np.empty((B, H), dtype=np.float64)
+    ip = ctypes.POINTER(ctypes.c_int)
+    rc = _load().oracle_decode_paged_f64(_ptr(q), _ptr(kc), _ptr(vc), bt.ctypes.data_as(ip),
+                                         sl.ctypes.data_as(ip), _ptr(o), _ptr(lse), B, H, D,
+                                         num_pages, page, bt.shape[1], float(scale))
+    if rc != 0:
+        raise RuntimeError(f"oracle_decode_paged_f64 failed with code {rc}")
     return o, lse

@@ -112,18 +112,20 @@ static double softmax_row(double* s, long n) {
     return m + log(sum);
 }
 
-static long block_rows(long L, long block_doubles) {
+/* Rows of S/P materialised at once: as many rows of `row_len` doubles as fit the budget, at
+ * least one and at most `rows` (the number of query rows; never 0, so the row loops advance). */
+static long block_rows(long row_len, long rows, long block_doubles) {
     if (block_doubles <= 0) block_doubles = ORACLE_DEFAULT_BLOCK_DOUBLES;
-    long r = block_doubles / (L > 0 ? L : 1);
+    long r = block_doubles / (row_len > 0 ? row_len : 1);
+    if (r > rows) r = rows;
     if (r < 1) r = 1;
-    if (r > L) r = L;
     return r;
 }
 
 /* Forward pass for one head: Q, O [Lq,D], K, V [Lk,D], lse [Lq]. */
 static int fwd_head(const double* Q, const double* K, const double* V, double* O, double* lse,
                     long Lq, long Lk, long D, double scale, int causal, long block_doubles) {
-    long R = block_rows(Lk, block_doubles);
+    long R = block_rows(Lk, Lq, block_doubles);
     double* P = (double*)malloc(sizeof(double) * (size_t)R * (size_t)(Lk > 0 ? Lk : 1));
     if (!P) return ORACLE_NO_MEMORY;
     for (long i0 = 0; i0 < Lq; i0 += R) {
@@ -150,7 +152,7 @@ static int fwd_head(const double* Q, const double* K, const double* V, double* O
 static int bwd_head(const double* Q, const double* K, const double* V, const double* dO,
                     double* dQ, double* dK, double* dV, double* delta, long Lq, long Lk, long D,
                     double scale, int causal, long block_doubles) {
-    long R = block_rows(Lk, block_doubles / 2);
+    long R = block_rows(Lk, Lq, block_doubles / 2);
     size_t row = (size_t)(Lk > 0 ? Lk : 1);
     double* P = (double*)malloc(sizeof(double) * (size_t)R * row);
     double* dS = (double*)malloc(sizeof(double) * (size_t)R * row);
@@ -263,6 +265,63 @@ int oracle_probs_f64(const double* q, const double* k, double* p, long Lq, long 
         long n = logits_row(q, k, i, Lq, Lk, D, scale, causal, row);
         (void)softmax_row(row, n);
         for (long j = n; j < Lk; ++j) row[j] = 0.0;
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Decode over a paged key/value cache ("FlashAttention principles and engineering practice",
+ * section 4.2: served through vLLM with PagedAttention and block_size 16).  Each sequence b has
+ * one new query row q[b, h, :] per head and a cache of seq_lens[b] tokens stored in pages of
+ * `page` tokens: token t of sequence b lives in physical page block_tables[b*max_pages + t/page]
+ * at slot t % page, head h, i.e. at k_cache[((phys*H + h)*page + t%page)*D ...].  The query is the
+ * newest position, so it sees every cached token: per (b, h) this is the plain definition with
+ * one query row and the sequence's tokens gathered in order as keys and values.  A sequence with
+ * no cached token has O = 0 and LSE = -inf.  Returns ORACLE_BAD_ARG for a page index or length
+ * out of range.
+ *   q, o: [B, H, D]; lse: [B, H]; k_cache, v_cache: [num_pages, H, page, D];
+ *   block_tables: [B, max_pages]; seq_lens: [B].
+ */
+int oracle_decode_paged_f64(const double* q, const double* k_cache, const double* v_cache,
+                            const int* block_tables, const int* seq_lens, double* o, double* lse,
+                            long B, long H, long D, long num_pages, long page, long max_pages,
+                            double scale) {
+    if (B < 0 || H < 0 || D < 1 || num_pages < 0 || page < 1 || max_pages < 0)
+        return ORACLE_BAD_ARG;
+    for (long b = 0; b < B; ++b) {
+        const long n = seq_lens[b];
+        if (n < 0 || n > max_pages * page) return ORACLE_BAD_ARG;
+        for (long t = 0; t < n; t += page) {
+            const long phys = block_tables[b * max_pages + t / page];
+            if (phys < 0 || phys >= num_pages) return ORACLE_BAD_ARG;
+        }
+        double* kb = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * (size_t)D);
+        double* vb = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * (size_t)D);
+        if (!kb || !vb) {
+            free(kb);
+            free(vb);
+            return ORACLE_NO_MEMORY;
+        }
+        for (long h = 0; h < H; ++h) {
+            /* Gather the sequence's keys and values of head h in token order. */
+            for (long t = 0; t < n; ++t) {
+                const long phys = block_tables[b * max_pages + t / page];
+                const size_t src = ((size_t)(phys * H + h) * (size_t)page + (size_t)(t % page)) *
+                                   (size_t)D;
+                memcpy(kb + t * D, k_cache + src, sizeof(double) * (size_t)D);
+                memcpy(vb + t * D, v_cache + src, sizeof(double) * (size_t)D);
+            }
+            const size_t qo = (size_t)(b * H + h) * (size_t)D;
+            /* One query row that sees all n keys (non-causal, Lq = 1). */
+            int rc = fwd_head(q + qo, kb, vb, o + qo, lse + b * H + h, 1, n, D, scale, 0, 0);
+            if (rc) {
+                free(kb);
+                free(vb);
+                return rc;
+            }
+        }
+        free(kb);
+        free(vb);
     }
     return ORACLE_OK;
 }

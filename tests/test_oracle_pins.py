@@ -86,3 +86,17 @@ def test_empty_sequence(oracle_mod):
     z = np.zeros((1, 2, 0, 8))
     o, lse = oracle_mod.forward(z, z, z, 1.0, True)
     assert o.shape == (1, 2, 0, 8) and lse.shape == (1, 2, 0)
+
+
+@pytest.mark.parametrize("block_doubles", [0, 40], ids=["whole_head", "row_blocks"])
+def test_queries_without_keys(oracle_mod, block_doubles):
+    """Lk = 0: every query row's softmax is over an empty set (O = 0, LSE = -inf, dQ = 0), in both
+    the whole-head and the row-block paths."""
+    r = np.random.default_rng(14)
+    q, do = r.standard_normal((5, 3)), r.standard_normal((5, 3))
+    k = np.zeros((0, 3))
+    for causal in (False, True):
+        o, lse = oracle_mod.forward(q, k, k, 0.5, causal, block_doubles=block_doubles)
+        assert np.all(o == 0.0) and np.all(np.isneginf(lse))
+        dq, dk, dv, _ = oracle_mod.backward(q, k, k, do, 0.5, causal, block_doubles=block_doubles)
+        assert np.all(dq == 0.0) and dk.shape == (0, 3) and dv.shape == (0, 3)
