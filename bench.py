@@ -614,8 +614,72 @@ def _time_forward_latency(w, dev, launches=1000):
             "l2": "warm (the 66 KB problem stays in L2)", "clocks": clocks}
 
 
+def _time_decode(w, dev, peaks, steps=50):
+    """One decode step over a paged cache (fa_decode_paged) timed with the library's per-kernel
+    CUDA events.  The cache (several GB) is far larger than L2, so no flush is needed.  HBM
+    bytes are algorithmic: every cached token's K and V row read once, plus q, O, LSE, the
+    sequence lengths and the table entries in use."""
+    import torch
+    import tiled_attention_08_gb300 as fa
+    import workloads
+    inp = workloads.make_decode_inputs(w, seed=0, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    o = torch.empty_like(inp["q"])
+    lse = torch.empty((w.B, w.H), device=dev, dtype=torch.float32)
+
+    def call(ev=None):
+        if ev is not None:
+            fa.fa_trace_next_call([e.cuda_event for e in ev], 2)
+        fa.decode_paged(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_tables"],
+                        inp["seq_lens"], w.scale, out=o, lse=lse)
+
+    def events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        for e in evs:
+            e.record(stream)
+        return evs
+
+    for _ in range(3):
+        call()
+    evs = [events() for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(gpu_selector(dev))
+    sampler.start()
+    time.sleep(0.3)
+    t0 = time.perf_counter()
+    for ev in evs:
+        call(ev)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    st = fa.fa_get_device_status(stream.cuda_stream)
+    if st != fa.FA_OK:
+        raise fa.FaError(w.name, st)
+    n_kern = 1 if fa.fa_decode_workspace_bytes(w.B, w.H, w.D, inp["block_tables"].shape[1]) == 0 \
+        else 2
+    ms = statistics.mean(sum(ev[2 * j].elapsed_time(ev[2 * j + 1]) for j in range(n_kern))
+                         for ev in evs)
+    lens = inp["seq_lens"].long()
+    tokens = int(lens.sum())
+    pages = int(((lens + workloads.PAGE_TOKENS - 1) // workloads.PAGE_TOKENS).sum())
+    elt = 2
+    by = (2 * tokens * w.H * w.D * elt + 2 * w.B * w.H * w.D * elt + w.B * w.H * 4 + w.B * 4 +
+          pages * 4)
+    peak_bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gbs = by / (ms * 1e-3) / 1e9
+    flops = 4.0 * tokens * w.H * w.D
+    return dict(w.describe(), steps=steps, kernels=n_kern, tokens=tokens,
+                us_per_step=round(ms * 1e3, 2), hbm_gbs=round(gbs, 1),
+                hbm_frac_of_peak=round(gbs / peak_bw, 4),
+                tflops=round(flops / (ms * 1e-3) / 1e12, 2),
+                algorithmic_bytes=by, l2="cache larger than L2 (no flush)",
+                roofline={"bound": "hbm", "achieved": round(gbs, 1), "peak": peak_bw,
+                          "unit": "GB/s", "frac": round(gbs / peak_bw, 4)},
+                clocks=clocks)
+
+
 def run_configs(dev, skip):
-    """Every other workload of the path, each timed on its own (see _time_config)."""
+    """Every other workload of the path, each timed on its own (see _time_config), and the
+    decode step over a paged cache (_time_decode)."""
     import workloads
     peaks, _ = load_peaks()
     out = {}
@@ -623,6 +687,8 @@ def run_configs(dev, skip):
         if name == skip:
             continue
         out[name] = _time_config(w, dev, peaks) if w.backward else _time_forward_latency(w, dev)
+    for name, w in workloads.DECODE_WORKLOADS.items():
+        out[name] = _time_decode(w, dev, peaks)
     return out
 
 

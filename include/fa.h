@@ -166,9 +166,42 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
                          int H, int L, int D, float scale, int causal, int dtype, void* stream);
 
+/* Tokens per page of the paged key/value cache of fa_decode_paged. */
+#define FA_PAGE_TOKENS 16
+
+/*
+ * Bytes of device workspace fa_decode_paged needs for this shape: 0 when every (sequence, head)
+ * pair is one CTA, else room for the per-split partial results (fp32).  0 for invalid sizes.
+ */
+size_t fa_decode_workspace_bytes(int B, int H, int D, int max_pages);
+
+/*
+ * One decode step over a paged key/value cache ("FlashAttention principles and engineering
+ * practice", section 4.2: serving with PagedAttention, block_size 16, continuous batching).
+ * Sequence b adds one token; its query rows q[b, h, :] attend to all seq_lens[b] tokens cached
+ * for it (the new token's key and value already written to the cache by the caller):
+ *     O[b,h] = softmax(scale * q[b,h] K_bh^T) V_bh,   LSE[b,h] = log sum_t exp(scale q.k_t),
+ * with token t of sequence b in physical page block_tables[b*max_pages + t/16], slot t % 16.
+ *   q, o:             [B, H, D] 16-bit (dtype), contiguous, 16-byte aligned;
+ *   k_cache, v_cache: [num_pages, H, FA_PAGE_TOKENS, D] 16-bit, contiguous, 16-byte aligned
+ *                     (the 16 tokens of one head in one page are contiguous);
+ *   block_tables:     [B, max_pages] int32, device; entries past a sequence's pages are unread;
+ *   seq_lens:         [B] int32, device, 0 <= seq_lens[b] <= 16 * max_pages;
+ *   lse:              [B, H] fp32; workspace: fa_decode_workspace_bytes(B, H, D, max_pages).
+ * A sequence with no cached token gets O = 0 and LSE = -inf.  Host-side argument errors return
+ * before anything is enqueued; a page index outside [0, num_pages) or a length outside its range
+ * (device data, checked by the kernel before any copy) is skipped and reported by
+ * fa_get_device_status() as FA_ERR_INVALID_ARG, with the outputs of that call undefined.
+ */
+fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, const int32_t* seq_lens, void* o,
+                          float* lse, void* workspace, size_t workspace_bytes, int B, int H, int D,
+                          int num_pages, int max_pages, float scale, int dtype, void* stream);
+
 /*
  * Synchronises `stream`, then reads and clears the current device's status word.  Returns
- * FA_OK, FA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last call, or
+ * FA_OK, FA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last call,
+ * FA_ERR_INVALID_ARG if a decode kernel found a page index or sequence length out of range, or
  * FA_ERR_CUDA if synchronisation itself failed or a kernel refused to run (its dynamic shared
  * memory was not 1024-byte aligned; it then wrote nothing).
  * The pages are silent on failure detection; this call is the library's own way of making a

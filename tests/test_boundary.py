@@ -163,6 +163,32 @@ def test_backward_ex_refuses_one_sided_empty_and_overlapping_outputs(lib):
     assert call([c] * 5 + [pk] * 3, dk=p[6] + 64 * 2) == fa.FA_ERR_INVALID_ARG
 
 
+def test_decode_workspace_and_argument_checks(lib):
+    # Enough (sequence, head) pairs: one CTA each, no workspace.  Few: splits need one.
+    assert fa.fa_decode_workspace_bytes(256, 32, 128, 256) == 0
+    assert fa.fa_decode_workspace_bytes(1, 2, 128, 188) == 1 * 2 * 188 * (128 + 1) * 4
+    assert fa.fa_decode_workspace_bytes(1, 2, 96, 10) == 0  # unsupported head size
+    p = [A + i * MB for i in range(8)]
+
+    def call(B=2, H=2, D=64, num_pages=10, max_pages=4, dtype=0, ws_bytes=1 << 20, **kw):
+        q = dict(zip(("q", "kc", "vc", "bt", "sl", "o", "lse", "ws"), p))
+        q.update(kw)
+        return fa.fa_decode_paged(q["q"], q["kc"], q["vc"], q["bt"], q["sl"], q["o"], q["lse"],
+                                  q["ws"], ws_bytes, B, H, D, num_pages, max_pages, 0.125, dtype,
+                                  None)
+
+    assert call(dtype=3) == fa.FA_ERR_INVALID_ARG
+    assert call(D=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(B=70000) == fa.FA_ERR_UNSUPPORTED
+    assert call(B=0) == fa.FA_OK
+    assert call(q=0) == fa.FA_ERR_INVALID_ARG
+    assert call(bt=0) == fa.FA_ERR_INVALID_ARG
+    assert call(o=A + 8) == fa.FA_ERR_INVALID_ARG             # o overlaps q, misaligned
+    assert call(o=p[1] + 64) == fa.FA_ERR_INVALID_ARG         # o inside the key cache
+    assert call(lse=p[5] + 16) == fa.FA_ERR_INVALID_ARG       # lse overlaps o
+    assert call(B=1, H=1, max_pages=64, ws_bytes=16) == fa.FA_ERR_INVALID_ARG  # workspace short
+
+
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(fa, "_lib", None)
     monkeypatch.setattr(fa, "_LIB_PATH", str(tmp_path / "missing" / "libfa.so"))

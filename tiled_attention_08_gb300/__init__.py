@@ -26,12 +26,14 @@ __all__ = ["FaError", "load_library", "library_path", "fa_fwd", "fa_fwd_ex", "fa
            "fa_bwd_workspace_bytes", "fa_get_device_status", "fa_set_wait_timeout_ns",
            "fa_selftest_wait_timeout", "fa_trace_next_call", "fa_launch_count", "fa_status_string",
            "fa_bwd_noalloc", "forward", "backward", "attention", "attention_blhd",
-           "attention_qkvpacked", "FaStrides",
+           "attention_qkvpacked", "FaStrides", "fa_decode_paged", "fa_decode_workspace_bytes",
+           "decode_paged", "FA_PAGE_TOKENS",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
            "FA_BF16", "FA_FP16"]
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 1, 2, 3, 4
 FA_BF16, FA_FP16 = 0, 1
+FA_PAGE_TOKENS = 16
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "_build", "libfa.so")
@@ -41,7 +43,8 @@ _lock = threading.Lock()
 EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_ex", "fa_bwd_workspace_bytes",
             "fa_get_device_status",
             "fa_set_wait_timeout_ns", "fa_selftest_wait_timeout", "fa_trace_next_call",
-            "fa_launch_count", "fa_status_string", "fa_bwd_noalloc")
+            "fa_launch_count", "fa_status_string", "fa_bwd_noalloc", "fa_decode_paged",
+            "fa_decode_workspace_bytes")
 
 
 class FaStrides(ctypes.Structure):
@@ -82,6 +85,10 @@ def load_library():
         lib.fa_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, sp, i, i, i, i, i, f,
                                   i, i, vp]
         lib.fa_bwd_ex.restype = i
+        lib.fa_decode_workspace_bytes.argtypes = [i, i, i, i]
+        lib.fa_decode_workspace_bytes.restype = sz
+        lib.fa_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
+        lib.fa_decode_paged.restype = i
         lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i,
                                        vp]
         lib.fa_bwd_noalloc.restype = i
@@ -125,6 +132,17 @@ def fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, str
     return load_library().fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace,
                                     workspace_bytes, _strides_array(strides), B, H, Lq, Lk, D,
                                     scale, int(causal), dtype, stream)
+
+
+def fa_decode_workspace_bytes(B, H, D, max_pages) -> int:
+    return int(load_library().fa_decode_workspace_bytes(B, H, D, max_pages))
+
+
+def fa_decode_paged(q, k_cache, v_cache, block_tables, seq_lens, o, lse, workspace,
+                    workspace_bytes, B, H, D, num_pages, max_pages, scale, dtype, stream) -> int:
+    return load_library().fa_decode_paged(q, k_cache, v_cache, block_tables, seq_lens, o, lse,
+                                          workspace, workspace_bytes, B, H, D, num_pages,
+                                          max_pages, scale, dtype, stream)
 
 
 def fa_bwd_workspace_bytes(B, H, L, D) -> int:
@@ -317,3 +335,38 @@ def attention_qkvpacked(qkv, causal: bool = False, scale: float | None = None):
             return dqkv
 
     return _Packed.apply(qkv)
+
+
+def decode_paged(q, k_cache, v_cache, block_tables, seq_lens, scale: float | None = None,
+                 out=None, lse=None, workspace=None):
+    """One decode step over a paged cache: q [B, H, D]; k_cache, v_cache
+    [num_pages, H, FA_PAGE_TOKENS, D] (bf16 or fp16, contiguous); block_tables [B, max_pages] and
+    seq_lens [B] int32 CUDA tensors.  Returns O [B, H, D] and LSE [B, H] (fp32)."""
+    import torch
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("block_tables", block_tables), ("seq_lens", seq_lens)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    B, H, D = q.shape
+    num_pages = k_cache.shape[0]
+    if tuple(k_cache.shape) != (num_pages, H, FA_PAGE_TOKENS, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("caches must be [num_pages, H, FA_PAGE_TOKENS, D]")
+    max_pages = block_tables.shape[1] if block_tables.dim() == 2 else 0
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = out if out is not None else torch.empty_like(q)
+    l = lse if lse is not None else torch.empty((B, H), device=q.device, dtype=torch.float32)
+    ws_bytes = fa_decode_workspace_bytes(B, H, D, max_pages)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), device=q.device, dtype=torch.uint8)
+    status = fa_decode_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                             block_tables.data_ptr(), seq_lens.data_ptr(), o.data_ptr(),
+                             l.data_ptr(), workspace.data_ptr(),
+                             workspace.numel() * workspace.element_size(), B, H, D, num_pages,
+                             max_pages, float(scale), dt, _stream_handle(q.device))
+    if status != FA_OK:
+        raise FaError("fa_decode_paged", status)
+    return o, l

@@ -477,6 +477,78 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                      L, D, scale, causal, dtype, stream);
 }
 
+size_t fa_decode_workspace_bytes(int B, int H, int D, int max_pages) {
+    if (B <= 0 || H <= 0 || (D != 64 && D != 128) || max_pages < 0) return 0;
+    const int splits = decode_splits(B, H, max_pages);
+    if (splits <= 1) return 0;
+    return (size_t)B * H * splits * (size_t)(D + 1) * 4u;
+}
+
+fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, const int32_t* seq_lens, void* o,
+                          float* lse, void* workspace, size_t workspace_bytes, int B, int H, int D,
+                          int num_pages, int max_pages, float scale, int dtype, void* stream) {
+    TraceDisarm disarm;
+    if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || D <= 0 || num_pages < 0 || max_pages < 0) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (B > 65535 || H > 65535) return FA_ERR_UNSUPPORTED;  // grid dimensions
+    if (B == 0 || H == 0) return FA_OK;
+    if (!q || !o || !lse || !seq_lens || (num_pages > 0 && (!k_cache || !v_cache)) ||
+        (max_pages > 0 && !block_tables))
+        return FA_ERR_INVALID_ARG;
+    const void* al16[] = {q, o, lse, k_cache, v_cache};
+    for (const void* ptr : al16)
+        if (ptr && !aligned16(ptr)) return FA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u))
+        return FA_ERR_INVALID_ARG;
+    const int splits = decode_splits(B, H, max_pages);
+    const size_t ws_need = splits > 1 ? (size_t)B * H * splits * (size_t)(D + 1) * 4u : 0;
+    if (ws_need > 0 && (!workspace || workspace_bytes < ws_need || !aligned16(workspace)))
+        return FA_ERR_INVALID_ARG;
+    const size_t rows = (size_t)B * H;
+    const size_t cache_bytes = (size_t)num_pages * H * kPageTokens * D * 2u;
+    const Range ins[] = {range(q, rows * D * 2u), range(k_cache, cache_bytes),
+                         range(v_cache, cache_bytes),
+                         range(block_tables, (size_t)B * max_pages * 4u),
+                         range(seq_lens, (size_t)B * 4u)};
+    const Range outs[] = {range(o, rows * D * 2u), range(lse, rows * 4u),
+                          range(workspace, ws_need)};
+    for (int a = 0; a < 3; ++a) {
+        for (const Range& in : ins)
+            if (overlap(outs[a], in)) return FA_ERR_INVALID_ARG;
+        for (int b2 = a + 1; b2 < 3; ++b2)
+            if (overlap(outs[a], outs[b2])) return FA_ERR_INVALID_ARG;
+    }
+    DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.o = o;
+    p.lse = lse;
+    p.part_o = static_cast<float*>(workspace);
+    p.part_lse = ws_need ? static_cast<float*>(workspace) + rows * splits * D : nullptr;
+    p.B = B;
+    p.H = H;
+    p.num_pages = num_pages;
+    p.max_pages = max_pages;
+    p.splits = splits;
+    p.pages_per_split = max_pages > 0 ? (max_pages + splits - 1) / splits : 1;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    if (!bind_context()) return FA_ERR_CUDA;
+    p.status = status_ptr();
+    p.timeout_ns = g_timeout_ns.load();
+    if (!p.status) return FA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = traced_launch(0, s, [&] { return launch_decode(p, D, dtype == FA_BF16, s); });
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 fa_status fa_get_device_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
     if (!status_ptr()) return FA_ERR_CUDA;
@@ -485,6 +557,7 @@ fa_status fa_get_device_status(void* stream) {
     const int zero = 0;
     if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
     if (word == 0) return FA_OK;
+    if (word == (int)kDevBadArg) return FA_ERR_INVALID_ARG;
     return word == (int)kDevTimeout ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
 }
 

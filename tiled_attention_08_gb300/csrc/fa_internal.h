@@ -12,6 +12,7 @@ enum DeviceError : int {
     kDevOk = 0,
     kDevBadShared = 3,  // dynamic shared memory not 1024-byte aligned (kernel did nothing)
     kDevTimeout = 4,    // a bounded wait ran out
+    kDevBadArg = 5,     // device-side argument out of range (a page index or sequence length)
 };
 
 // Tile geometry shared by every kernel: 128 query rows x 128 keys per tile; operands are
@@ -74,6 +75,25 @@ struct BwdPreParams {
     int bf16;
 };
 
+// Decode over a paged key/value cache: tokens per page.
+constexpr int kPageTokens = 16;
+
+struct DecodeParams {
+    const void* q;             // [B, H, D] 16-bit: the new token's query rows
+    const void* k_cache;       // [num_pages, H, kPageTokens, D] 16-bit
+    const void* v_cache;       // [num_pages, H, kPageTokens, D] 16-bit
+    const int* block_tables;   // [B, max_pages]: physical page of each sequence's page
+    const int* seq_lens;       // [B]: cached tokens per sequence (the new one included)
+    void* o;                   // [B, H, D] 16-bit
+    float* lse;                // [B, H] natural log
+    float* part_o;             // [B*H*splits, D] fp32 (splits > 1)
+    float* part_lse;           // [B*H*splits] log2 domain (splits > 1)
+    int B, H, num_pages, max_pages, splits, pages_per_split;
+    float scale_log2;          // scale * log2(e), either sign
+    int* status;
+    uint64_t timeout_ns;
+};
+
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 16-bit {D, L, H, B} (strided), box {64, 128, 1, 1}
     const void* dout;                     // rows staged into TMEM by the dQ pass
@@ -124,5 +144,8 @@ cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdParams& p, int D, bool bf16, bool causal, cudaStream_t s);
 cudaError_t launch_bwd_dq(const BwdParams& p, int D, bool bf16, bool causal, cudaStream_t s);
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, int D, bool bf16, cudaStream_t s);
+// Splits of the page range per (sequence, head) for a decode step of this shape.
+int decode_splits(int B, int H, int max_pages);
 
 }  // namespace fa

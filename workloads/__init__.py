@@ -96,3 +96,73 @@ def make_inputs(w: Workload, seed: int = 0, with_do: bool = True):
     if with_do:
         out["do"] = do.to(w.dtype)
     return out
+
+
+# ---------------------------------------------------------------------------------------
+# Decode over a paged key/value cache ("FlashAttention principles and engineering practice",
+# section 4.2: Llama-2-7B served with PagedAttention, block_size 16, up to 256 sequences in a
+# continuous batch).  Synthetic stand-in: N(0,1) queries and cache, sequence lengths drawn
+# uniformly, pages assigned in a shuffled order with spare pages left holding noise.
+# ---------------------------------------------------------------------------------------
+PAGE_TOKENS = 16
+
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    B: int
+    H: int
+    D: int
+    dtype: torch.dtype
+    min_len: int
+    max_len: int
+    extra_pages: int = 64
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def dtype_name(self) -> str:
+        return {torch.bfloat16: "bf16", torch.float16: "fp16"}[self.dtype]
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "B": self.B, "H": self.H, "D": self.D,
+                "page_tokens": PAGE_TOKENS, "seq_len": f"U[{self.min_len}, {self.max_len}]",
+                "dtype": self.dtype_name}
+
+
+DECODE_WORKLOADS = {
+    "decode_llama2_7b_B256": DecodeWorkload("decode_llama2_7b_B256", 256, 32, 128,
+                                            torch.bfloat16, 1, 4096),
+}
+
+
+def make_decode_inputs(w: DecodeWorkload, seed: int = 0, device="cpu", lens=None):
+    """Returns dict q [B,H,D], k_cache, v_cache [num_pages,H,16,D] (w.dtype), block_tables
+    [B,max_pages] int32, seq_lens [B] int32, all on `device`.  Draw order: lengths (unless
+    given), page order, q, k_cache, v_cache.  Table entries past a sequence's pages are 0."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    if lens is None:
+        lens = torch.randint(w.min_len, w.max_len + 1, (w.B,), generator=g)
+    lens = torch.as_tensor(lens, dtype=torch.int64)
+    pages = (lens + PAGE_TOKENS - 1) // PAGE_TOKENS
+    max_pages = max(1, int(pages.max()) if len(pages) else 1)
+    num_pages = int(pages.sum()) + w.extra_pages
+    order = torch.randperm(num_pages, generator=g)
+    table = torch.zeros((w.B, max_pages), dtype=torch.int32)
+    nxt = 0
+    for b in range(w.B):
+        n = int(pages[b])
+        table[b, :n] = order[nxt:nxt + n].to(torch.int32)
+        nxt += n
+    gd = torch.Generator(device=device)
+    gd.manual_seed(int(seed) + 1)
+    q = torch.randn((w.B, w.H, w.D), generator=gd, device=device, dtype=torch.float32)
+    kc = torch.randn((num_pages, w.H, PAGE_TOKENS, w.D), generator=gd, device=device,
+                     dtype=torch.float32)
+    vc = torch.randn((num_pages, w.H, PAGE_TOKENS, w.D), generator=gd, device=device,
+                     dtype=torch.float32)
+    return {"q": q.to(w.dtype), "k_cache": kc.to(w.dtype), "v_cache": vc.to(w.dtype),
+            "block_tables": table.to(device), "seq_lens": lens.to(torch.int32).to(device)}
