@@ -57,11 +57,16 @@ def _load():
             lib = ctypes.CDLL(_SO)
             dp = ctypes.POINTER(ctypes.c_double)
             L = ctypes.c_long
+            u64 = ctypes.c_ulonglong
             lib.oracle_fwd_f64.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, ctypes.c_double,
-                                           ctypes.c_int, L]
+                                           ctypes.c_int, L, ctypes.c_double, u64]
             lib.oracle_fwd_f64.restype = ctypes.c_int
             lib.oracle_bwd_f64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, L, L, L, L, L,
-                                           ctypes.c_double, ctypes.c_int, L]
+                                           ctypes.c_double, ctypes.c_int, L, ctypes.c_double,
+                                           u64]
+            u32p = ctypes.POINTER(ctypes.c_uint)
+            lib.oracle_philox4x32_10.argtypes = [u32p, u32p, u32p]
+            lib.oracle_philox4x32_10.restype = None
             lib.oracle_bwd_f64.restype = ctypes.c_int
             lib.oracle_probs_f64.argtypes = [dp, dp, dp, L, L, L, ctypes.c_double,
                                              ctypes.c_int]
@@ -106,10 +111,12 @@ def _check_qkv(q, k, v, extra=()):
             raise ValueError("dO must have the shape of q")
 
 
-def forward(q, k, v, scale: float, causal: bool, block_doubles: int = 0):
+def forward(q, k, v, scale: float, causal: bool, block_doubles: int = 0, dropout_p: float = 0.0,
+            seed: int = 0):
     """O [B,H,Lq,D] and LSE [B,H,Lq] (natural log) in fp64 for q [B,H,Lq,D] and k, v
     [B,H,Lk,D] (Lq may differ from Lk; causal rows are aligned to the end of the keys).  Also
-    accepts [L,D] inputs."""
+    accepts [L,D] inputs.  ``dropout_p`` > 0 drops entries of P (Philox-4x32-10 keyed by
+    ``seed``; see oracle.c)."""
     q, sq = _as4d(_f64(q))
     k, _ = _as4d(_f64(k))
     v, _ = _as4d(_f64(v))
@@ -119,7 +126,8 @@ def forward(q, k, v, scale: float, causal: bool, block_doubles: int = 0):
     o = np.empty_like(q)
     lse = np.empty((B, H, Lq), dtype=np.float64)
     rc = _load().oracle_fwd_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Lq, Lk, D,
-                                float(scale), int(bool(causal)), int(block_doubles))
+                                float(scale), int(bool(causal)), int(block_doubles),
+                                float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF)
     if rc != 0:
         raise RuntimeError(f"oracle_fwd_f64 failed with code {rc}")
     if sq:
@@ -127,7 +135,8 @@ def forward(q, k, v, scale: float, causal: bool, block_doubles: int = 0):
     return o, lse
 
 
-def backward(q, k, v, do, scale: float, causal: bool, block_doubles: int = 0):
+def backward(q, k, v, do, scale: float, causal: bool, block_doubles: int = 0,
+             dropout_p: float = 0.0, seed: int = 0):
     """dQ [B,H,Lq,D], dK, dV [B,H,Lk,D] and Delta [B,H,Lq] in fp64.  Also accepts [L,D]
     inputs."""
     q, sq = _as4d(_f64(q))
@@ -143,7 +152,8 @@ def backward(q, k, v, do, scale: float, causal: bool, block_doubles: int = 0):
     delta = np.empty((B, H, Lq), dtype=np.float64)
     rc = _load().oracle_bwd_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
                                 _ptr(delta), B, H, Lq, Lk, D, float(scale), int(bool(causal)),
-                                int(block_doubles))
+                                int(block_doubles), float(dropout_p),
+                                int(seed) & 0xFFFFFFFFFFFFFFFF)
     if rc != 0:
         raise RuntimeError(f"oracle_bwd_f64 failed with code {rc}")
     if sq:
@@ -230,3 +240,12 @@ def decode_paged(q, k_cache, v_cache, block_tables, seq_lens, scale: float):
     if rc != 0:
         raise RuntimeError(f"oracle_decode_paged_f64 failed with code {rc}")
     return o, lse
+
+
+def philox4x32_10(counter, key):
+    """The four 32-bit output words of Philox-4x32-10 for a 4-word counter and 2-word key."""
+    c = (ctypes.c_uint * 4)(*[int(x) & 0xFFFFFFFF for x in counter])
+    k = (ctypes.c_uint * 2)(*[int(x) & 0xFFFFFFFF for x in key])
+    out = (ctypes.c_uint * 4)()
+    _load().oracle_philox4x32_10(c, k, out)
+    return [int(x) for x in out]

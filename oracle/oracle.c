@@ -47,6 +47,17 @@
  * of the head whenever R*Lk doubles fit the block budget, so for test sizes the whole
  * Lq x Lk matrix is materialised at once.
  *
+ * Dropout on P ("FlashAttention data-flow optimisation", section 4.1, step 3: the dropout_p
+ * argument of flash_attn_func).  With probability p each entry of P is dropped and the kept ones
+ * are scaled by 1/(1-p): O = (P o Z) V with Z_ij in {0, 1/(1-p)}; the LSE is that of P itself.
+ * The backward then has dV = (P o Z)^T dO and dP = (dO V^T) o Z, with Delta and dS as above
+ * (Delta_i = sum_j P_ij dP_ij still equals sum_d dO_id O_id).  Which entries are dropped is
+ * decided by a counter-based generator, Philox-4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw,
+ * "Parallel random numbers: as easy as 1, 2, 3", SC 2011), written out below from that
+ * definition: entry (bh, i, j) of head bh = b*H + h reads word j % 4 of the block for counter
+ * (j / 4, i, bh, 0) under the key (seed low 32 bits, seed high 32 bits), and is dropped iff that
+ * word is below floor(p * 2^32).  p = 0 keeps every entry.
+ *
  * Layout: every tensor is contiguous [B,H,L,D] (L = Lq for Q, O, dO, dQ and Lk for K, V,
  * dK, dV; LSE, Delta: [B,H,Lq]) in fp64.
  * Parallelism: OpenMP over rows (and over key columns for dK/dV) inside one head.
@@ -64,6 +75,60 @@
 
 /* Default cap on doubles held by one materialised block of S/P (2^25 = 256 MiB). */
 #define ORACLE_DEFAULT_BLOCK_DOUBLES (1L << 25)
+
+/* Philox-4x32-10: ten rounds of the round function on the 4-word counter, the 2-word key
+ * advanced by the Weyl constants between rounds. */
+void oracle_philox4x32_10(const unsigned int ctr_in[4], const unsigned int key_in[2],
+                          unsigned int out[4]) {
+    const unsigned long long M0 = 0xD2511F53ull, M1 = 0xCD9E8D57ull;
+    const unsigned int W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    unsigned int c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    unsigned int k0 = key_in[0], k1 = key_in[1];
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += W0;
+            k1 += W1;
+        }
+        const unsigned long long p0 = M0 * (unsigned long long)c0;
+        const unsigned long long p1 = M1 * (unsigned long long)c2;
+        const unsigned int hi0 = (unsigned int)(p0 >> 32), lo0 = (unsigned int)p0;
+        const unsigned int hi1 = (unsigned int)(p1 >> 32), lo1 = (unsigned int)p1;
+        const unsigned int n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+/* Dropout parameters: no dropout when p_drop == 0. */
+typedef struct {
+    double p;                /* drop probability in [0, 1) */
+    unsigned int threshold;  /* floor(p * 2^32): an entry is dropped iff its word is below it */
+    unsigned int key[2];     /* the seed */
+} dropout_t;
+
+static dropout_t make_dropout(double p, unsigned long long seed) {
+    dropout_t d;
+    d.p = p;
+    d.threshold = (unsigned int)floor(p * 4294967296.0);
+    d.key[0] = (unsigned int)(seed & 0xffffffffull);
+    d.key[1] = (unsigned int)(seed >> 32);
+    return d;
+}
+
+/* The factor Z_ij of entry (bh, i, j): 0 if dropped, 1/(1-p) if kept (1 without dropout). */
+static double dropout_factor(const dropout_t* d, long bh, long i, long j) {
+    if (d->threshold == 0u) return 1.0;
+    const unsigned int ctr[4] = {(unsigned int)(j >> 2), (unsigned int)i, (unsigned int)bh, 0u};
+    unsigned int w[4];
+    oracle_philox4x32_10(ctr, d->key, w);
+    return w[j & 3] < d->threshold ? 0.0 : 1.0 / (1.0 - d->p);
+}
 
 int oracle_num_threads(void) {
 #ifdef _OPENMP
@@ -122,9 +187,11 @@ static long block_rows(long row_len, long rows, long block_doubles) {
     return r;
 }
 
-/* Forward pass for one head: Q, O [Lq,D], K, V [Lk,D], lse [Lq]. */
+/* Forward pass for one head (bh = b*H + h for the dropout counter): Q, O [Lq,D], K, V [Lk,D],
+ * lse [Lq]. */
 static int fwd_head(const double* Q, const double* K, const double* V, double* O, double* lse,
-                    long Lq, long Lk, long D, double scale, int causal, long block_doubles) {
+                    long Lq, long Lk, long D, double scale, int causal, long block_doubles,
+                    const dropout_t* drop, long bh) {
     long R = block_rows(Lk, Lq, block_doubles);
     double* P = (double*)malloc(sizeof(double) * (size_t)R * (size_t)(Lk > 0 ? Lk : 1));
     if (!P) return ORACLE_NO_MEMORY;
@@ -139,7 +206,8 @@ static int fwd_head(const double* Q, const double* K, const double* V, double* O
             for (long d = 0; d < D; ++d) o[d] = 0.0;
             for (long j = 0; j < n; ++j) {
                 const double* v = V + j * D;
-                for (long d = 0; d < D; ++d) o[d] += p[j] * v[d];
+                const double pz = p[j] * dropout_factor(drop, bh, i, j);
+                for (long d = 0; d < D; ++d) o[d] += pz * v[d];
             }
         }
     }
@@ -151,7 +219,8 @@ static int fwd_head(const double* Q, const double* K, const double* V, double* O
  * Q, dO, dQ [Lq,D], K, V, dK, dV [Lk,D], delta [Lq]. */
 static int bwd_head(const double* Q, const double* K, const double* V, const double* dO,
                     double* dQ, double* dK, double* dV, double* delta, long Lq, long Lk, long D,
-                    double scale, int causal, long block_doubles) {
+                    double scale, int causal, long block_doubles, const dropout_t* drop,
+                    long bh) {
     long R = block_rows(Lk, Lq, block_doubles / 2);
     size_t row = (size_t)(Lk > 0 ? Lk : 1);
     double* P = (double*)malloc(sizeof(double) * (size_t)R * row);
@@ -178,6 +247,7 @@ static int bwd_head(const double* Q, const double* K, const double* V, const dou
                 const double* v = V + j * D;
                 double dp = 0.0;
                 for (long d = 0; d < D; ++d) dp += g[d] * v[d];
+                dp *= dropout_factor(drop, bh, i, j); /* dP = (dO V^T) o Z */
                 ds[j] = dp; /* dP_ij for now */
                 dlt += p[j] * dp;
             }
@@ -198,7 +268,7 @@ static int bwd_head(const double* Q, const double* K, const double* V, const dou
             double* dk = dK + j * D;
             for (long i = i0; i < i1; ++i) {
                 if (j >= visible_keys(i, Lq, Lk, causal)) continue; /* P_ij = 0 and dS_ij = 0 */
-                double pij = P[(i - i0) * Lk + j];
+                double pij = P[(i - i0) * Lk + j] * dropout_factor(drop, bh, i, j); /* P o Z */
                 double dsij = dS[(i - i0) * Lk + j];
                 const double* g = dO + i * D;
                 const double* q = Q + i * D;
@@ -224,13 +294,14 @@ static int bad_shape(long B, long H, long Lq, long Lk, long D) {
  */
 int oracle_fwd_f64(const double* q, const double* k, const double* v, double* o, double* lse,
                    long B, long H, long Lq, long Lk, long D, double scale, int causal,
-                   long block_doubles) {
-    if (bad_shape(B, H, Lq, Lk, D)) return ORACLE_BAD_ARG;
+                   long block_doubles, double p_drop, unsigned long long seed) {
+    if (bad_shape(B, H, Lq, Lk, D) || !(p_drop >= 0.0 && p_drop < 1.0)) return ORACLE_BAD_ARG;
+    const dropout_t drop = make_dropout(p_drop, seed);
     for (long bh = 0; bh < B * H; ++bh) {
         size_t oq = (size_t)bh * (size_t)Lq * (size_t)D;
         size_t ok = (size_t)bh * (size_t)Lk * (size_t)D;
         int rc = fwd_head(q + oq, k + ok, v + ok, o + oq, lse + (size_t)bh * (size_t)Lq, Lq, Lk, D,
-                          scale, causal, block_doubles);
+                          scale, causal, block_doubles, &drop, bh);
         if (rc) return rc;
     }
     return ORACLE_OK;
@@ -242,14 +313,16 @@ int oracle_fwd_f64(const double* q, const double* k, const double* v, double* o,
  */
 int oracle_bwd_f64(const double* q, const double* k, const double* v, const double* dO,
                    double* dq, double* dk, double* dv, double* delta, long B, long H, long Lq,
-                   long Lk, long D, double scale, int causal, long block_doubles) {
-    if (bad_shape(B, H, Lq, Lk, D)) return ORACLE_BAD_ARG;
+                   long Lk, long D, double scale, int causal, long block_doubles, double p_drop,
+                   unsigned long long seed) {
+    if (bad_shape(B, H, Lq, Lk, D) || !(p_drop >= 0.0 && p_drop < 1.0)) return ORACLE_BAD_ARG;
+    const dropout_t drop = make_dropout(p_drop, seed);
     for (long bh = 0; bh < B * H; ++bh) {
         size_t oq = (size_t)bh * (size_t)Lq * (size_t)D;
         size_t ok = (size_t)bh * (size_t)Lk * (size_t)D;
         int rc = bwd_head(q + oq, k + ok, v + ok, dO + oq, dq + oq, dk + ok, dv + ok,
                           delta + (size_t)bh * (size_t)Lq, Lq, Lk, D, scale, causal,
-                          block_doubles);
+                          block_doubles, &drop, bh);
         if (rc) return rc;
     }
     return ORACLE_OK;
@@ -313,7 +386,9 @@ int oracle_decode_paged_f64(const double* q, const double* k_cache, const double
             }
             const size_t qo = (size_t)(b * H + h) * (size_t)D;
             /* One query row that sees all n keys (non-causal, Lq = 1). */
-            int rc = fwd_head(q + qo, kb, vb, o + qo, lse + b * H + h, 1, n, D, scale, 0, 0);
+            const dropout_t none = make_dropout(0.0, 0ull);
+            int rc = fwd_head(q + qo, kb, vb, o + qo, lse + b * H + h, 1, n, D, scale, 0, 0, &none,
+                              b * H + h);
             if (rc) {
                 free(kb);
                 free(vb);
