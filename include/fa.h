@@ -87,12 +87,22 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
  * j <= i + Lk - Lq.  A query row that sees no key (only when Lq > Lk) gets O = 0 and
  * LSE = -inf.  Lq = 0 returns FA_OK with nothing to do; Lk = 0 with Lq > 0 returns
  * FA_ERR_UNSUPPORTED.  Extents (first to last element) of the outputs must not overlap those of
- * the inputs or each other.  fa_fwd(..., L, ...) is fa_fwd_ex with Lq = Lk = L and contiguous
- * strides.
+ * the inputs or each other.  fa_fwd(..., L, ...) is fa_fwd_ex with Lq = Lk = L, contiguous
+ * strides and no dropout.
+ *
+ * Dropout on P (flash_attn_func's dropout_p, data-flow page, section 4.1, step 3):
+ * dropout_p in [0, 1) (NaN or outside: FA_ERR_INVALID_ARG); 0 runs the kernels without
+ * dropout.  O = (P o Z) V with Z_ij = 0 for a dropped entry and 1 / (1 - dropout_p) for a kept
+ * one; LSE stays that of P itself.  Entry (i, j) of head bh = b * H + h (query row i, key j) is
+ * kept iff word j % 4 of the Philox-4x32-10 block (Salmon et al., "Parallel random numbers: as
+ * easy as 1, 2, 3", SC 2011) at counter (j / 4, i, bh, 0) under key (seed & 0xffffffff,
+ * seed >> 32) is at least floor(dropout_p * 2^32).  The pages fix no generator; this one is
+ * counter-based, so the backward regenerates the mask from (dropout_p, seed) instead of storing
+ * it.
  */
 fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                     const fa_strides* strides, int B, int H, int Lq, int Lk, int D, float scale,
-                    int causal, int dtype, void* stream);
+                    int causal, double dropout_p, uint64_t seed, int dtype, void* stream);
 
 /*
  * Bytes of device workspace fa_bwd needs for this shape: two fp32 vectors per head padded to
@@ -110,9 +120,10 @@ size_t fa_bwd_workspace_bytes(int B, int H, int L, int D);
  * dq, dk, dv [B,H,L,D] (dtype).  `workspace` is a device buffer of at least
  * fa_bwd_workspace_bytes(B,H,L,D) bytes, 16-byte aligned, owned by the caller; its contents
  * on entry do not matter.  Three kernels are enqueued on `stream`: the Delta/LSE preprocess,
- * the dK/dV pass (one CTA per key tile) and the dQ pass (one CTA per query tile, or, when
- * query tiles see at most 32 key tiles on average, one persistent CTA per SM taking query
- * tiles in turn; the results are the same either way).
+ * the dK/dV pass (one CTA per key tile, or, when key tiles are seen by at most 12 query tiles
+ * on average, one persistent CTA per SM taking key tiles in turn) and the dQ pass (likewise
+ * per query tile, persistent when query tiles see at most 32 key tiles on average); the
+ * results are the same either way.
  * Data-flow page, section 2.2, third layer (recompute P from the saved statistics).
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -128,12 +139,16 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  * interleaved parts of one packed [B,L,3,H,D] gradient (Lq = Lk, equal strides, the heads of a
  * row together, each part's heads ending before the next part's begin); otherwise no two
  * outputs' extents may overlap, and no output may overlap an input.  fa_bwd is fa_bwd_ex with
- * Lq = Lk = L and contiguous strides.
+ * Lq = Lk = L, contiguous strides and no dropout.  dropout_p and seed must be those of the
+ * forward that produced o and lse (the same mask is regenerated): dV = (P o Z)^T dO and
+ * dS = P o ((dO V^T) o Z - Delta), Delta = rowsum(dO o O); the backward under dropout always
+ * runs one CTA per tile.
  */
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,
                     const float* lse, void* dq, void* dk, void* dv, void* workspace,
                     size_t workspace_bytes, const fa_strides* strides, int B, int H, int Lq,
-                    int Lk, int D, float scale, int causal, int dtype, void* stream);
+                    int Lk, int D, float scale, int causal, double dropout_p, uint64_t seed,
+                    int dtype, void* stream);
 
 /* Size of the fixed device scratch array behind fa_bwd_noalloc: 16 MiB. */
 #define FA_BWD_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)

@@ -116,14 +116,14 @@ def test_backward_argument_checks(lib, kw, status):
     assert _bwd(**kw) == status
 
 
-def _fwd_ex(strides=None, B=1, H=2, Lq=256, Lk=256, D=64, **ptrs):
+def _fwd_ex(strides=None, B=1, H=2, Lq=256, Lk=256, D=64, dropout_p=0.0, **ptrs):
     p = dict(q=A, k=A + MB, v=A + 2 * MB, o=A + 3 * MB, lse=A + 4 * MB)
     p.update(ptrs)
     c = (H * Lq * D, Lq * D, D)
     ck = (H * Lk * D, Lk * D, D)
     st = strides or [c, ck, ck, c]
     return fa.fa_fwd_ex(p["q"], p["k"], p["v"], p["o"], p["lse"], st, B, H, Lq, Lk, D, 0.125, 1,
-                        0, None)
+                        dropout_p, 7, 0, None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -136,6 +136,10 @@ def _fwd_ex(strides=None, B=1, H=2, Lq=256, Lk=256, D=64, **ptrs):
     (dict(o=A + 2 * MB + 4096), fa.FA_ERR_INVALID_ARG),               # o inside v's extent
     # [B,L,H,D] views whose extents overlap: o would be read as k
     (dict(strides=[(256 * 2 * 64, 64, 2 * 64)] * 4, o=A + MB), fa.FA_ERR_INVALID_ARG),
+    (dict(dropout_p=1.0), fa.FA_ERR_INVALID_ARG),                      # nothing would be kept
+    (dict(dropout_p=-0.25), fa.FA_ERR_INVALID_ARG),
+    (dict(dropout_p=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(dropout_p=0.5, Lq=0), fa.FA_OK),                             # valid p, empty problem
 ], ids=lambda x: str(x)[:60])
 def test_forward_ex_argument_checks(lib, kw, status):
     assert _fwd_ex(**kw) == status
@@ -147,13 +151,16 @@ def test_backward_ex_refuses_one_sided_empty_and_overlapping_outputs(lib):
     p = [A + i * MB for i in range(10)]
     ws = fa.fa_bwd_workspace_bytes(B, H, L, D)
 
-    def call(strides, Lq=L, Lk=L, **kw):
+    def call(strides, Lq=L, Lk=L, dropout_p=0.0, **kw):
         q = dict(zip(("q", "k", "v", "o", "do", "lse", "dq", "dk", "dv", "ws"), p))
         q.update(kw)
         return fa.fa_bwd_ex(q["q"], q["k"], q["v"], q["o"], q["do"], q["lse"], q["dq"], q["dk"],
-                            q["dv"], q["ws"], ws, strides, B, H, Lq, Lk, D, 0.125, 1, 0, None)
+                            q["dv"], q["ws"], ws, strides, B, H, Lq, Lk, D, 0.125, 1, dropout_p,
+                            7, 0, None)
 
     assert call([c] * 8, Lq=0, Lk=0) == fa.FA_OK
+    assert call([c] * 8, dropout_p=1.0) == fa.FA_ERR_INVALID_ARG
+    assert call([c] * 8, dropout_p=float("inf")) == fa.FA_ERR_INVALID_ARG
     assert call([c] * 8, Lq=0) == fa.FA_ERR_UNSUPPORTED
     assert call([c] * 8, Lk=0) == fa.FA_ERR_UNSUPPORTED
     # dk inside dq's extent with contiguous strides: not the interleaved parts of a packed tensor

@@ -73,6 +73,7 @@ def load_library():
                                "`python -m tiled_attention_08_gb300.build` first")
         lib = ctypes.CDLL(_LIB_PATH)
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        d64, u64 = ctypes.c_double, ctypes.c_uint64
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
         lib.fa_fwd.restype = i
         lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
@@ -80,10 +81,10 @@ def load_library():
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, f, i, i, vp]
         lib.fa_bwd.restype = i
         sp = ctypes.POINTER(FaStrides)
-        lib.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, sp, i, i, i, i, i, f, i, i, vp]
+        lib.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, sp, i, i, i, i, i, f, i, d64, u64, i, vp]
         lib.fa_fwd_ex.restype = i
         lib.fa_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, sp, i, i, i, i, i, f,
-                                  i, i, vp]
+                                  i, d64, u64, i, vp]
         lib.fa_bwd_ex.restype = i
         lib.fa_decode_workspace_bytes.argtypes = [i, i, i, i]
         lib.fa_decode_workspace_bytes.restype = sz
@@ -120,18 +121,21 @@ def _strides_array(strides):
     return (FaStrides * len(strides))(*[FaStrides(*map(int, t)) for t in strides])
 
 
-def fa_fwd_ex(q, k, v, o, lse, strides, B, H, Lq, Lk, D, scale, causal, dtype, stream) -> int:
+def fa_fwd_ex(q, k, v, o, lse, strides, B, H, Lq, Lk, D, scale, causal, dropout_p, seed, dtype,
+              stream) -> int:
     """``strides``: four (batch, head, row) tuples for q, k, v, o."""
     return load_library().fa_fwd_ex(q, k, v, o, lse, _strides_array(strides), B, H, Lq, Lk, D,
-                                    scale, int(causal), dtype, stream)
+                                    scale, int(causal), float(dropout_p),
+                                    int(seed) & 0xFFFFFFFFFFFFFFFF, dtype, stream)
 
 
 def fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, strides, B, H, Lq,
-              Lk, D, scale, causal, dtype, stream) -> int:
+              Lk, D, scale, causal, dropout_p, seed, dtype, stream) -> int:
     """``strides``: eight (batch, head, row) tuples for q, k, v, o, dout, dq, dk, dv."""
     return load_library().fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace,
                                     workspace_bytes, _strides_array(strides), B, H, Lq, Lk, D,
-                                    scale, int(causal), dtype, stream)
+                                    scale, int(causal), float(dropout_p),
+                                    int(seed) & 0xFFFFFFFFFFFFFFFF, dtype, stream)
 
 
 def fa_decode_workspace_bytes(B, H, D, max_pages) -> int:
@@ -219,10 +223,12 @@ def _stream_handle(device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
 
-def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+            dropout_p: float = 0.0, seed: int = 0):
     """O, LSE = attention(q, k, v) for CUDA tensors viewed as [B, H, Lq, D] (q) and
     [B, H, Lk, D] (k, v), bf16 or fp16, with a contiguous last dimension.  O has q's shape (and,
-    where torch can keep them, q's strides); LSE is contiguous [B, H, Lq] fp32."""
+    where torch can keep them, q's strides); LSE is contiguous [B, H, Lq] fp32.  ``dropout_p``
+    drops entries of P with the counter-based mask of ``seed`` (``fa_fwd_ex`` in fa.h)."""
     import torch
     B, H, Lq, D = q.shape
     Lk = k.shape[2]
@@ -239,17 +245,18 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     if not l.is_contiguous() or tuple(l.shape) != (B, H, Lq):
         raise ValueError("lse must be a contiguous [B, H, Lq] tensor")
     status = fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), st,
-                       B, H, Lq, Lk, D, float(scale), causal, dt, _stream_handle(q.device))
+                       B, H, Lq, Lk, D, float(scale), causal, dropout_p, seed, dt,
+                       _stream_handle(q.device))
     if status != FA_OK:
         raise FaError("fa_fwd_ex", status)
     return o, l
 
 
 def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
-             workspace=None, grads=None):
-    """dQ, dK, dV for the forward above.  ``grads`` optionally gives the three output views
-    (for example the parts of one packed gradient tensor); by default they are allocated like
-    q, k, v."""
+             workspace=None, grads=None, dropout_p: float = 0.0, seed: int = 0):
+    """dQ, dK, dV for the forward above (with that forward's ``dropout_p`` and ``seed``).
+    ``grads`` optionally gives the three output views (for example the parts of one packed
+    gradient tensor); by default they are allocated like q, k, v."""
     import torch
     B, H, Lq, D = q.shape
     Lk = k.shape[2]
@@ -272,21 +279,35 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     status = fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
                        lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                        workspace.data_ptr(), workspace.numel() * workspace.element_size(), st,
-                       B, H, Lq, Lk, D, float(scale), causal, dt, _stream_handle(q.device))
+                       B, H, Lq, Lk, D, float(scale), causal, dropout_p, seed, dt,
+                       _stream_handle(q.device))
     if status != FA_OK:
         raise FaError("fa_bwd_ex", status)
     return dq, dk, dv
 
 
-def attention(q, k, v, causal: bool = False, scale: float | None = None):
-    """Differentiable attention for torch autograd (forward and backward run in libfa) over
-    [B, H, L, D] views (Lq may differ from Lk)."""
+def _dropout_seed(dropout_p: float, seed: int | None) -> int:
+    """The caller's seed, or for dropout without one a fresh 64-bit seed from torch's default
+    generator (the mask itself is drawn on the device from the seed)."""
+    if seed is not None or dropout_p == 0.0:
+        return 0 if seed is None else int(seed)
     import torch
+    return int(torch.randint(0, 2**62, (1,)).item())
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None, dropout_p: float = 0.0,
+              seed: int | None = None):
+    """Differentiable attention for torch autograd (forward and backward run in libfa) over
+    [B, H, L, D] views (Lq may differ from Lk).  With ``dropout_p`` > 0 the forward and the
+    backward regenerate the same dropout mask from ``seed`` (drawn from torch's generator when
+    None)."""
+    import torch
+    seed_ = _dropout_seed(dropout_p, seed)
 
     class _Attention(torch.autograd.Function):
         @staticmethod
         def forward(ctx, q_, k_, v_):
-            o_, lse_ = forward(q_, k_, v_, causal, scale)
+            o_, lse_ = forward(q_, k_, v_, causal, scale, dropout_p=dropout_p, seed=seed_)
             ctx.save_for_backward(q_, k_, v_, o_, lse_)
             return o_
 
@@ -295,16 +316,18 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None):
             q_, k_, v_, o_, lse_ = ctx.saved_tensors
             if do_.stride(-1) != 1:
                 do_ = do_.contiguous()
-            return backward(q_, k_, v_, o_, lse_, do_, causal, scale)
+            return backward(q_, k_, v_, o_, lse_, do_, causal, scale, dropout_p=dropout_p,
+                            seed=seed_)
 
     return _Attention.apply(q, k, v)
 
 
-def attention_blhd(q, k, v, causal: bool = False, scale: float | None = None):
+def attention_blhd(q, k, v, causal: bool = False, scale: float | None = None,
+                   dropout_p: float = 0.0, seed: int | None = None):
     """attention() for [B, L, H, D] tensors (the flash_attn_func layout); returns O as
     [B, Lq, H, D].  No copy: the kernels read and write the [B, L, H, D] memory directly."""
     return attention(q.transpose(1, 2), k.transpose(1, 2), v.transpose(1, 2), causal,
-                     scale).transpose(1, 2)
+                     scale, dropout_p, seed).transpose(1, 2)
 
 
 def attention_qkvpacked(qkv, causal: bool = False, scale: float | None = None):

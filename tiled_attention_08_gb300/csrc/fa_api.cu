@@ -196,6 +196,18 @@ bool same_strides(const Strides& a, const Strides& b) {
     return a.b == b.b && a.h == b.h && a.l == b.l;
 }
 
+// Dropout parameters: p in [0, 1); an entry is dropped iff its Philox word is below
+// floor(p * 2^32), and kept ones are scaled by 1 / (1 - p).  p = 0 gives threshold 0 (nothing
+// dropped); the caller then runs the kernels without dropout.
+bool make_dropout(double p, uint64_t seed, Dropout* d) {
+    if (!(p >= 0.0 && p < 1.0)) return false;  // also rejects NaN
+    d->threshold = (uint32_t)std::floor(p * 4294967296.0);
+    d->seed_lo = (uint32_t)(seed & 0xffffffffu);
+    d->seed_hi = (uint32_t)(seed >> 32);
+    d->keep_scale = (float)(1.0 / (1.0 - p));
+    return true;
+}
+
 }  // namespace
 
 void trace_disarm() { t_trace_pairs = 0; }
@@ -284,11 +296,13 @@ uint64_t fa_launch_count(void) { return g_launches.load(); }
 
 fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
                     const fa_strides* strides, int B, int H, int Lq, int Lk, int D, float scale,
-                    int causal, int dtype, void* stream) {
+                    int causal, double dropout_p, uint64_t seed, int dtype, void* stream) {
     TraceDisarm disarm;
     Shape sh;
     fa_status st = check_shape(B, H, Lq, Lk, D, scale, causal, dtype, &sh);
     if (st != FA_OK) return st;
+    Dropout drop;
+    if (!make_dropout(dropout_p, seed, &drop)) return FA_ERR_INVALID_ARG;
     if (sh.empty) return FA_OK;
     if (Lk == 0) return FA_ERR_UNSUPPORTED;  // queries but no key at all
     if (!q || !k || !v || !o || !lse || !strides) return FA_ERR_INVALID_ARG;
@@ -330,11 +344,13 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
     // returns exactly 1, the uniform softmax that scale 0 defines.
     p.scale_log2 = std::fmax(std::fabs(scale) * 1.4426950408889634f, FLT_MIN);
     p.s_negate = scale < 0.0f ? kIdescNegateA : 0u;
+    p.drop = drop;
     p.status = status_ptr();
     p.timeout_ns = g_timeout_ns.load();
     if (!p.status) return FA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = traced_launch(0, s, [&] { return launch_fwd(p, D, bf16, causal != 0, s); });
+    const bool dr = dropout_p > 0.0;
+    cudaError_t e = traced_launch(0, s, [&] { return launch_fwd(p, D, bf16, causal != 0, dr, s); });
     if (e != cudaSuccess) return FA_ERR_CUDA;
     // Under the causal mask the first Lq - Lk query rows see no key when Lq > Lk.
     const int empty_rows = (causal && Lq > Lk) ? Lq - Lk : 0;
@@ -347,7 +363,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int L, int D, float scale, int causal, int dtype, void* stream) {
     const fa_strides c = {(int64_t)H * L * D, (int64_t)L * D, (int64_t)D};
     const fa_strides all[4] = {c, c, c, c};
-    return fa_fwd_ex(q, k, v, o, lse, all, B, H, L, L, D, scale, causal, dtype, stream);
+    return fa_fwd_ex(q, k, v, o, lse, all, B, H, L, L, D, scale, causal, 0.0, 0, dtype, stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int L, int D) {
@@ -359,11 +375,14 @@ size_t fa_bwd_workspace_bytes(int B, int H, int L, int D) {
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,
                     const float* lse, void* dq, void* dk, void* dv, void* workspace,
                     size_t workspace_bytes, const fa_strides* strides, int B, int H, int Lq,
-                    int Lk, int D, float scale, int causal, int dtype, void* stream) {
+                    int Lk, int D, float scale, int causal, double dropout_p, uint64_t seed,
+                    int dtype, void* stream) {
     TraceDisarm disarm;
     Shape sh;
     fa_status st = check_shape(B, H, Lq, Lk, D, scale, causal, dtype, &sh);
     if (st != FA_OK) return st;
+    Dropout drop;
+    if (!make_dropout(dropout_p, seed, &drop)) return FA_ERR_INVALID_ARG;
     if (sh.BH == 0 || (Lq == 0 && Lk == 0)) return FA_OK;  // nothing to compute
     if (Lq == 0 || Lk == 0) return FA_ERR_UNSUPPORTED;     // queries without keys, or keys
                                                            // without queries
@@ -430,6 +449,7 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     p.group = schedule_group(sh.BH, Lq > Lk ? Lq : Lk, D);
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.drop = drop;
     p.status = status_ptr();
     p.timeout_ns = g_timeout_ns.load();
     if (!p.status) return FA_ERR_CUDA;
@@ -458,10 +478,11 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (traced_launch(0, s, [&] { return launch_bwd_pre(pp, s); }) != cudaSuccess)
         return FA_ERR_CUDA;
-    if (traced_launch(1, s, [&] { return launch_bwd_dkdv(p, D, bf16, causal != 0, s); }) !=
+    const bool dr = dropout_p > 0.0;
+    if (traced_launch(1, s, [&] { return launch_bwd_dkdv(p, D, bf16, causal != 0, dr, s); }) !=
         cudaSuccess)
         return FA_ERR_CUDA;
-    if (traced_launch(2, s, [&] { return launch_bwd_dq(p, D, bf16, causal != 0, s); }) !=
+    if (traced_launch(2, s, [&] { return launch_bwd_dq(p, D, bf16, causal != 0, dr, s); }) !=
         cudaSuccess)
         return FA_ERR_CUDA;
     return FA_OK;
@@ -474,7 +495,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     const fa_strides c = {(int64_t)H * L * D, (int64_t)L * D, (int64_t)D};
     const fa_strides all[8] = {c, c, c, c, c, c, c, c};
     return fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, all, B, H, L,
-                     L, D, scale, causal, dtype, stream);
+                     L, D, scale, causal, 0.0, 0, dtype, stream);
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int D, int max_pages) {

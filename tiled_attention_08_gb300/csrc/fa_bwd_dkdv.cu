@@ -121,7 +121,9 @@ __device__ __forceinline__ bool dkdv_item(const BwdParams& p, int round, DkdvIte
 
 // One CTA per (b*h, key tile), in tile_coords order (the hardware's block scheduler balances
 // the causal tiles): for rows of many query tiles, where a CTA's fixed cost is a small share.
-template <int D, bool BF16, bool CAUSAL>
+// DROP: dropout on P (p.drop): dV accumulates (P o keep)^T dO and is scaled by 1/(1-p) on the
+// way out; dS^T = P^T o (dP^T o Z^T - Delta) with Z the keep mask times 1/(1-p).
+template <int D, bool BF16, bool CAUSAL, bool DROP>
 __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = DkdvCfg<D, BF16, CAUSAL>;
@@ -380,6 +382,8 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             float pv[kC];
             uint32_t pk_p[kC / 2];  // P^T, packed to 16 bits
+            uint32_t keep_bits = 0xffffffffu;  // dropout: bit i keeps query column c0 + i
+            static_assert(!DROP || kC <= 32, "one keep word per warp slice");
             if (ok) {
                 tc_fence_after_sync();
                 uint32_t r[kC];
@@ -409,8 +413,33 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                         if (qg > qlim || (CAUSAL && key > qg + (p.Lk - p.Lq))) pv[i] = 0.0f;
                     }
                 }
+                if constexpr (DROP) {
+                    // One generator block holds keys 4m..4m+3 of one query: the four lanes of
+                    // those keys each draw one query of a group of four and swap nibbles, so
+                    // lane 4m+r ends up with key 4m+r's bits of all four queries.
+                    const uint32_t r4 = (uint32_t)lane & 3u;
+                    keep_bits = 0u;
 #pragma unroll
-                for (int i = 0; i < kC / 2; ++i) pk_p[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
+                    for (int g = 0; g < kC; g += 4) {
+                        uint32_t x = dropout_keep4((uint32_t)(key & ~3), (uint32_t)(q0 + g) + r4,
+                                                   (uint32_t)bh, p.drop.seed_lo, p.drop.seed_hi,
+                                                   p.drop.threshold)
+                                     << (4u * r4);
+                        x |= __shfl_xor_sync(0xffffffffu, x, 1);
+                        x |= __shfl_xor_sync(0xffffffffu, x, 2);
+                        // bit 4c + r4 of x: query q0 + g + c
+                        const uint32_t b = ((x >> r4) & 1u) | ((x >> (r4 + 3u)) & 2u) |
+                                           ((x >> (r4 + 6u)) & 4u) | ((x >> (r4 + 9u)) & 8u);
+                        keep_bits |= b << g;
+                    }
+#pragma unroll
+                    for (int i = 0; i < kC / 2; ++i)
+                        pk_p[i] = pack2<BF16>((keep_bits >> (2 * i)) & 1u ? pv[2 * i] : 0.0f,
+                                              (keep_bits >> (2 * i + 1)) & 1u ? pv[2 * i + 1] : 0.0f);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kC / 2; ++i) pk_p[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
+                }
                 // Phase 2: dS^T = P^T o (dP^T - Delta).
                 ok = wait_bounded(&bar_of[os], oph, abort_v, p.timeout_ns) &&
                      wait_bounded(&bar_df, (uint32_t)t & 1u, abort_v, p.timeout_ns);
@@ -423,6 +452,13 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                 for (int h = 0; h < kC / kLd; ++h) {
                     uint32_t r[kLd];
                     tmem_ld<kLd>(tmem + lane_off + C::kTmDPT + c0 + h * kLd, r);
+                    if constexpr (DROP) {  // dP^T o Z^T: dropped entries 0, kept ones / (1 - p)
+#pragma unroll
+                        for (int i = 0; i < kLd; ++i)
+                            r[i] = __float_as_uint((keep_bits >> (h * kLd + i)) & 1u
+                                                       ? __uint_as_float(r[i]) * p.drop.keep_scale
+                                                       : 0.0f);
+                    }
 #pragma unroll
                     for (int i = 0; i < kLd; i += 4) {  // P o (dP - Delta), two per instruction
                         const float4 d = lds_f32x4(dlt_addr + (h * kLd + i) * 4);
@@ -467,8 +503,8 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
             const size_t coff = (size_t)part * C::kOutCols * 2;
             tmem_row_to_global<BF16, C::kOutCols>(
                 tmem + lane_off + C::kTmDV + part * C::kOutCols,
-                reinterpret_cast<uint8_t*>(p.dv) + row_offset(p.sdv, bh, p.H, key) + coff, 1.0f,
-                valid);
+                reinterpret_cast<uint8_t*>(p.dv) + row_offset(p.sdv, bh, p.H, key) + coff,
+                DROP ? p.drop.keep_scale : 1.0f, valid);
             tmem_row_to_global<BF16, C::kOutCols>(
                 tmem + lane_off + C::kTmDK + part * C::kOutCols,
                 reinterpret_cast<uint8_t*>(p.dk) + row_offset(p.sdk, bh, p.H, key) + coff, p.scale,
@@ -893,29 +929,34 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
     }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool DROP>
 cudaError_t launch_t(const BwdParams& p, cudaStream_t s) {
     using C = DkdvCfg<D, BF16, CAUSAL>;
     constexpr int kSmem = dkdv_smem_bytes<D, BF16, CAUSAL>();
     static_assert(kSmem <= 232448, "dynamic shared memory over the 227 KB per-block limit");
     const int total = p.n_ktiles * p.BH;
-    const int grid = dkdv_grid(p.Lq, p.Lk, p.BH, CAUSAL, sm_count());
+    // The persistent kernel has no dropout variant.
+    const int grid = DROP ? total : dkdv_grid(p.Lq, p.Lk, p.BH, CAUSAL, sm_count());
     auto kern = grid < total ? fa_bwd_dkdv_kernel_persistent<D, BF16, CAUSAL>
-                             : fa_bwd_dkdv_kernel<D, BF16, CAUSAL>;
+                             : fa_bwd_dkdv_kernel<D, BF16, CAUSAL, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     return launch_kernel(kern, (unsigned)grid, C::kThreads, kSmem, s, p);
 }
 
+template <int D, bool BF16>
+cudaError_t launch_d(const BwdParams& p, bool causal, bool drop, cudaStream_t s) {
+    if (drop) return causal ? launch_t<D, BF16, true, true>(p, s) : launch_t<D, BF16, false, true>(p, s);
+    return causal ? launch_t<D, BF16, true, false>(p, s) : launch_t<D, BF16, false, false>(p, s);
+}
+
 }  // namespace
 
-cudaError_t launch_bwd_dkdv(const BwdParams& p, int D, bool bf16, bool causal, cudaStream_t s) {
-    if (D == 64) {
-        if (bf16) return causal ? launch_t<64, true, true>(p, s) : launch_t<64, true, false>(p, s);
-        return causal ? launch_t<64, false, true>(p, s) : launch_t<64, false, false>(p, s);
-    }
-    if (bf16) return causal ? launch_t<128, true, true>(p, s) : launch_t<128, true, false>(p, s);
-    return causal ? launch_t<128, false, true>(p, s) : launch_t<128, false, false>(p, s);
+cudaError_t launch_bwd_dkdv(const BwdParams& p, int D, bool bf16, bool causal, bool drop,
+                            cudaStream_t s) {
+    if (D == 64)
+        return bf16 ? launch_d<64, true>(p, causal, drop, s) : launch_d<64, false>(p, causal, drop, s);
+    return bf16 ? launch_d<128, true>(p, causal, drop, s) : launch_d<128, false>(p, causal, drop, s);
 }
 
 }  // namespace fa

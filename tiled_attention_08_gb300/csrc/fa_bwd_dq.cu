@@ -81,7 +81,8 @@ struct DqCfg {
 
 // One CTA per (b*h, query tile), in tile_coords order (the hardware's block scheduler balances
 // the causal tiles): for rows of many key tiles, where a CTA's fixed cost is a small share.
-template <int D, bool BF16, bool CAUSAL>
+// DROP: dropout on P (p.drop): dS = P o (dP o Z - Delta) with Z the keep mask times 1/(1-p).
+template <int D, bool BF16, bool CAUSAL, bool DROP>
 __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = DqCfg<D, BF16, CAUSAL>;
@@ -324,6 +325,19 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
                 for (int h = 0; h < kC / kLd; ++h) {
                     uint32_t r[kLd];
                     tmem_ld<kLd>(tmem + lane_off + C::kTmDP + c0 + h * kLd, r);
+                    if constexpr (DROP) {  // dP o Z: dropped entries 0, kept ones / (1 - p)
+#pragma unroll
+                        for (int g = 0; g < kLd; g += 4) {
+                            const uint32_t keep = dropout_keep4(
+                                (uint32_t)(key0 + h * kLd + g), (uint32_t)q_row, (uint32_t)bh,
+                                p.drop.seed_lo, p.drop.seed_hi, p.drop.threshold);
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                r[g + c] = __float_as_uint(
+                                    (keep >> c) & 1u ? __uint_as_float(r[g + c]) * p.drop.keep_scale
+                                                     : 0.0f);
+                        }
+                    }
 #pragma unroll
                     for (int i = 0; i < kLd; i += 2) {  // P o (dP - Delta), two per instruction
                         float* q = pv + h * kLd + i;
@@ -750,13 +764,14 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
     }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool DROP>
 cudaError_t launch_t(const BwdParams& p, cudaStream_t s) {
     using C = DqCfg<D, BF16, CAUSAL>;
     const int total = p.n_qtiles * p.BH;
     const int grid = dq_grid(p.Lq, p.Lk, p.BH, CAUSAL, sm_count());
     // The persistent kernel needs every query tile to see a key; only the first tile can fail to.
-    if (grid < total && q_tile_kv(0, p.Lq, p.Lk, CAUSAL) > 0) {
+    // It has no dropout variant.
+    if (!DROP && grid < total && q_tile_kv(0, p.Lq, p.Lk, CAUSAL) > 0) {
         // Persistent: one CTA per SM (each fills an SM).
         auto kern = fa_bwd_dq_kernel_persistent<D, BF16, CAUSAL>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -764,22 +779,26 @@ cudaError_t launch_t(const BwdParams& p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         return launch_kernel(kern, (unsigned)grid, C::kThreads, C::kSmemBytes, s, p);
     }
-    auto kern = fa_bwd_dq_kernel<D, BF16, CAUSAL>;
+    auto kern = fa_bwd_dq_kernel<D, BF16, CAUSAL, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     return launch_kernel(kern, (unsigned)total, C::kThreads, C::kSmemBytes, s, p);
 }
 
+template <int D, bool BF16>
+cudaError_t launch_d(const BwdParams& p, bool causal, bool drop, cudaStream_t s) {
+    if (drop) return causal ? launch_t<D, BF16, true, true>(p, s) : launch_t<D, BF16, false, true>(p, s);
+    return causal ? launch_t<D, BF16, true, false>(p, s) : launch_t<D, BF16, false, false>(p, s);
+}
+
 }  // namespace
 
-cudaError_t launch_bwd_dq(const BwdParams& p, int D, bool bf16, bool causal, cudaStream_t s) {
-    if (D == 64) {
-        if (bf16) return causal ? launch_t<64, true, true>(p, s) : launch_t<64, true, false>(p, s);
-        return causal ? launch_t<64, false, true>(p, s) : launch_t<64, false, false>(p, s);
-    }
-    if (bf16) return causal ? launch_t<128, true, true>(p, s) : launch_t<128, true, false>(p, s);
-    return causal ? launch_t<128, false, true>(p, s) : launch_t<128, false, false>(p, s);
+cudaError_t launch_bwd_dq(const BwdParams& p, int D, bool bf16, bool causal, bool drop,
+                          cudaStream_t s) {
+    if (D == 64)
+        return bf16 ? launch_d<64, true>(p, causal, drop, s) : launch_d<64, false>(p, causal, drop, s);
+    return bf16 ? launch_d<128, true>(p, causal, drop, s) : launch_d<128, false>(p, causal, drop, s);
 }
 
 }  // namespace fa

@@ -119,7 +119,9 @@ __device__ __forceinline__ bool fwd_item(const FwdParams& p, int round, FwdItem&
     return true;
 }
 
-template <int D, bool BF16, bool CAUSAL>
+// DROP: dropout on P (p.drop): the PV operand carries the kept entries only, the running sum
+// all of them, and the final 1/l includes 1/(1-p).
+template <int D, bool BF16, bool CAUSAL, bool DROP>
 __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = FwdCfg<D, BF16, CAUSAL>;
@@ -408,6 +410,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {  // 32 columns -> 16 packed TMEM columns at a time
                     uint32_t pk[16];
+                    uint32_t keep = 0xfu;  // dropout: keep bits of the current 4 columns
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         float y0, y1;
@@ -417,7 +420,17 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
                         const float p0 = ex2_approx(y0);
                         const float p1 = ex2_approx(y1);
                         sum2[i & 1] = f2_add(sum2[i & 1], f2_make(p0, p1));
-                        pk[i] = pack2<BF16>(p0, p1);
+                        if constexpr (DROP) {
+                            if ((i & 1) == 0)
+                                keep = dropout_keep4((uint32_t)(key0 + h * 32 + 2 * i),
+                                                     (uint32_t)q_row, (uint32_t)it.bh,
+                                                     p.drop.seed_lo, p.drop.seed_hi,
+                                                     p.drop.threshold);
+                            const uint32_t b2 = keep >> (2 * (i & 1));
+                            pk[i] = pack2<BF16>((b2 & 1u) ? p0 : 0.0f, (b2 & 2u) ? p1 : 0.0f);
+                        } else {
+                            pk[i] = pack2<BF16>(p0, p1);
+                        }
                     }
                     tmem_st16(s_addr + h * 16, pk);
                 }
@@ -445,7 +458,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
             uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) + row_offset(p.so, it.bh, p.H, q_row);
             // The read-out finishes (tcgen05.ld waits) before this group publishes P_t0 of the
             // next item, which is what lets PV_t0 overwrite O_t.
-            tmem_row_to_global<BF16, D>(o_addr, orow, l_sum > 0.0f ? 1.0f / l_sum : 0.0f, valid);
+            const float inv_l = l_sum > 0.0f ? (DROP ? p.drop.keep_scale : 1.0f) / l_sum : 0.0f;
+            tmem_row_to_global<BF16, D>(o_addr, orow, inv_l, valid);
             ps += n_mine;
             ++n_done;
         }
@@ -479,17 +493,21 @@ __global__ void __launch_bounds__(256) fa_fwd_empty_rows_kernel(const FwdParams 
     }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool DROP>
 cudaError_t launch_t(const FwdParams& p, cudaStream_t s) {
     using C = FwdCfg<D, BF16, CAUSAL>;
-    auto kern = fa_fwd_kernel<D, BF16, CAUSAL>;
+    auto kern = fa_fwd_kernel<D, BF16, CAUSAL, DROP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int n_pairs = (p.n_qtiles + 1) / 2;
     const int grid = fwd_grid(p.Lq, p.Lk, p.BH, CAUSAL, sm_count());
-    kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3((unsigned)grid), dim3(C::kThreads), C::kSmemBytes, s, p);
+}
+
+template <int D, bool BF16>
+cudaError_t launch_d(const FwdParams& p, bool causal, bool drop, cudaStream_t s) {
+    if (drop) return causal ? launch_t<D, BF16, true, true>(p, s) : launch_t<D, BF16, false, true>(p, s);
+    return causal ? launch_t<D, BF16, true, false>(p, s) : launch_t<D, BF16, false, false>(p, s);
 }
 
 }  // namespace
@@ -506,13 +524,11 @@ cudaError_t launch_fwd_empty_rows(const FwdParams& p, int D, int rows, cudaStrea
                                    dim3(256), 0, s, p, rows);
 }
 
-cudaError_t launch_fwd(const FwdParams& p, int D, bool bf16, bool causal, cudaStream_t s) {
-    if (D == 64) {
-        if (bf16) return causal ? launch_t<64, true, true>(p, s) : launch_t<64, true, false>(p, s);
-        return causal ? launch_t<64, false, true>(p, s) : launch_t<64, false, false>(p, s);
-    }
-    if (bf16) return causal ? launch_t<128, true, true>(p, s) : launch_t<128, true, false>(p, s);
-    return causal ? launch_t<128, false, true>(p, s) : launch_t<128, false, false>(p, s);
+cudaError_t launch_fwd(const FwdParams& p, int D, bool bf16, bool causal, bool drop,
+                       cudaStream_t s) {
+    if (D == 64)
+        return bf16 ? launch_d<64, true>(p, causal, drop, s) : launch_d<64, false>(p, causal, drop, s);
+    return bf16 ? launch_d<128, true>(p, causal, drop, s) : launch_d<128, false>(p, causal, drop, s);
 }
 
 }  // namespace fa

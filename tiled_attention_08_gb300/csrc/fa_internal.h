@@ -48,6 +48,14 @@ __host__ __device__ __forceinline__ size_t row_offset(const Strides& s, int bh, 
     return (size_t)((long long)b * s.b + (long long)h * s.h + (long long)row * s.l) * 2u;
 }
 
+// Dropout on P: entry (bh, i, j) is dropped iff word j % 4 of Philox-4x32-10 at counter
+// (j / 4, i, bh, 0) under the key (seed_lo, seed_hi) is below `threshold` = floor(p * 2^32); kept
+// entries count 1/(1-p) (`keep_scale`).  threshold = 0: no dropout.
+struct Dropout {
+    uint32_t threshold, seed_lo, seed_hi;
+    float keep_scale;
+};
+
 struct FwdParams {
     CUtensorMap tm_q, tm_k, tm_v;  // 16-bit {D, L, H, B} (strided), box {64, 128, 1, 1}
     void* o;                       // [B, H, Lq, D] 16-bit, strides so
@@ -58,6 +66,7 @@ struct FwdParams {
     int group;          // heads per schedule group (tile_coords)
     float scale_log2;   // |scale| * log2(e)
     uint32_t s_negate;  // kIdescNegateA when scale < 0 (S is computed as -Q K^T), else 0
+    Dropout drop;
     int* status;        // device status word
     uint64_t timeout_ns;
 };
@@ -108,6 +117,7 @@ struct BwdParams {
     int group;          // heads per schedule group (tile_coords)
     float scale;        // softmax scale (applied to dQ and dK)
     float scale_log2;   // scale * log2(e)
+    Dropout drop;
     int* status;
     uint64_t timeout_ns;
 };
@@ -138,11 +148,14 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 }
 
 // Launchers (one per kernel unit).  Return the launch error, if any.
-cudaError_t launch_fwd(const FwdParams& p, int D, bool bf16, bool causal, cudaStream_t s);
+cudaError_t launch_fwd(const FwdParams& p, int D, bool bf16, bool causal, bool drop,
+                       cudaStream_t s);
 cudaError_t launch_fwd_empty_rows(const FwdParams& p, int D, int rows, cudaStream_t s);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t s);
-cudaError_t launch_bwd_dkdv(const BwdParams& p, int D, bool bf16, bool causal, cudaStream_t s);
-cudaError_t launch_bwd_dq(const BwdParams& p, int D, bool bf16, bool causal, cudaStream_t s);
+cudaError_t launch_bwd_dkdv(const BwdParams& p, int D, bool bf16, bool causal, bool drop,
+                            cudaStream_t s);
+cudaError_t launch_bwd_dq(const BwdParams& p, int D, bool bf16, bool causal, bool drop,
+                          cudaStream_t s);
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int D, bool bf16, cudaStream_t s);
 // Splits of the page range per (sequence, head) for a decode step of this shape.

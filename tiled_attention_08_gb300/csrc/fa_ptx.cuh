@@ -368,6 +368,47 @@ __device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
 }
 
 // ---------------------------------------------------------------------------------------
+// Counter-based random numbers for dropout: Philox-4x32 with 10 rounds (Salmon, Moraes, Dror,
+// Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011), from that definition: each
+// round multiplies words 0 and 2 by fixed odd constants, and the high halves, xored with words 1
+// and 3 and the key, become the new words 0 and 2 (the low halves words 3 and 1); the key
+// advances by two Weyl constants between rounds.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                              uint32_t k0, uint32_t k1, uint32_t (&out)[4]) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+// Dropout keep bits of four consecutive keys j4..j4+3 (j4 a multiple of 4) of query row i of
+// head bh: bit c set iff word c of the Philox block at counter (j4/4, i, bh, 0) is at least the
+// threshold floor(p * 2^32).
+__device__ __forceinline__ uint32_t dropout_keep4(uint32_t j4, uint32_t i, uint32_t bh,
+                                                  uint32_t seed_lo, uint32_t seed_hi,
+                                                  uint32_t threshold) {
+    uint32_t w[4];
+    philox4x32_10(j4 >> 2, i, bh, 0u, seed_lo, seed_hi, w);
+    return (w[0] >= threshold ? 1u : 0u) | (w[1] >= threshold ? 2u : 0u) |
+           (w[2] >= threshold ? 4u : 0u) | (w[3] >= threshold ? 8u : 0u);
+}
+
+// ---------------------------------------------------------------------------------------
 // Math helpers
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ float ex2_approx(float x) {
