@@ -459,9 +459,10 @@ def run_ours(args, w):
 L2_BYTES = 129 * 2**20  # GB300 L2
 
 
-def _time_config(w, dev, peaks):
+def _time_config(w, dev, peaks, dropout_p=0.0):
     """Times one workload's fa_fwd + fa_bwd through the C ABI with every kernel bracketed by
-    CUDA events, sampling clocks meanwhile.  Inputs that fit in L2 get an L2 flush before every
+    CUDA events, sampling clocks meanwhile (with dropout on P: fa_fwd_ex + fa_bwd_ex on the
+    same contiguous tensors; the FLOP count stays that of the attention itself).  Inputs that fit in L2 get an L2 flush before every
     step, outside the kernels' events: a write of a 256 MiB buffer, then a read of another one,
     so each step starts with none of its data in L2 and with no dirty lines left for its own
     kernels to write back.  The step count is chosen from the warm-up so the timed region lasts
@@ -486,21 +487,35 @@ def _time_config(w, dev, peaks):
         flush = (torch.empty(256 * 2**20, dtype=torch.uint8, device=dev),
                  torch.ones(64 * 2**20, dtype=torch.float32, device=dev))
 
+    contig = (H * L * D, L * D, D)
+
     def step(ev=None):
         if flush is not None:
             flush[0].fill_(1)
             flush[1].sum()
         if ev is not None:
             fa.fa_trace_next_call([ev[0].cuda_event, ev[1].cuda_event], 1)
-        st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                       B, H, L, D, w.scale, int(w.causal), dt, sh)
+        if dropout_p > 0.0:
+            st = fa.fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), [contig] * 4, B, H, L, L, D, w.scale,
+                              int(w.causal), dropout_p, 1234, dt, sh)
+        else:
+            st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           lse.data_ptr(), B, H, L, D, w.scale, int(w.causal), dt, sh)
         if st != fa.FA_OK:
             raise fa.FaError("fa_fwd", st)
         if ev is not None:
             fa.fa_trace_next_call([x.cuda_event for x in ev[2:8]], 3)
-        st = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
-                       ws_bytes, B, H, L, D, w.scale, int(w.causal), dt, sh)
+        if dropout_p > 0.0:
+            st = fa.fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                              dv.data_ptr(), ws.data_ptr(), ws_bytes, [contig] * 8, B, H, L, L,
+                              D, w.scale, int(w.causal), dropout_p, 1234, dt, sh)
+        else:
+            st = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                           dv.data_ptr(), ws.data_ptr(), ws_bytes, B, H, L, D, w.scale,
+                           int(w.causal), dt, sh)
         if st != fa.FA_OK:
             raise fa.FaError("fa_bwd", st)
 
@@ -541,7 +556,7 @@ def _time_config(w, dev, peaks):
     tot_flops = pm.flops_fwd(B, H, L, D, w.causal) + pm.flops_bwd(B, H, L, D, w.causal)
     return {
         "B": B, "H": H, "L": L, "D": D, "causal": w.causal, "dtype": w.dtype_name,
-        "row_scaled": w.row_scaled, "steps": steps,
+        "row_scaled": w.row_scaled, "dropout_p": dropout_p, "steps": steps,
         "l2": ("flushed before every step (256 MiB written, then 256 MiB read)"
                if flush is not None else "inputs larger than L2"),
         "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4),
@@ -677,9 +692,13 @@ def _time_decode(w, dev, peaks, steps=50):
                 clocks=clocks)
 
 
+DROPOUT_CONFIG = ("llama2_7b_L2048", 0.1)  # the Llama-2-7B layer with dropout on P
+
+
 def run_configs(dev, skip):
-    """Every other workload of the path, each timed on its own (see _time_config), and the
-    decode step over a paged cache (_time_decode)."""
+    """Every other workload of the path, each timed on its own (see _time_config), the
+    Llama-2-7B layer once more with dropout on P, and the decode step over a paged cache
+    (_time_decode)."""
     import workloads
     peaks, _ = load_peaks()
     out = {}
@@ -687,6 +706,8 @@ def run_configs(dev, skip):
         if name == skip:
             continue
         out[name] = _time_config(w, dev, peaks) if w.backward else _time_forward_latency(w, dev)
+    name, p = DROPOUT_CONFIG
+    out[f"{name}_dropout{p}"] = _time_config(workloads.WORKLOADS[name], dev, peaks, dropout_p=p)
     for name, w in workloads.DECODE_WORKLOADS.items():
         out[name] = _time_decode(w, dev, peaks)
     return out
