@@ -116,6 +116,17 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
 size_t fa_bwd_workspace_bytes(int B, int H, int L, int D);
 
 /*
+ * Bytes of device workspace fa_bwd_ex needs for q of [B, H, Lq, D] and the given
+ * `deterministic` flag (0 or 1; else 0 is returned): with deterministic = 0 at D = 64 the
+ * backward reduces dQ into an fp32 accumulator [B*H, Lqpad, D] kept in the workspace after the
+ * two per-row vectors (Lqpad = Lq rounded up to a multiple of 128).  A workspace of this size
+ * also serves the same shape with dropout (which always takes the deterministic path).
+ * fa_bwd_workspace_bytes(B, H, L, D) = fa_bwd_workspace_bytes_ex(B, H, L, D, 1).
+ * Pages: silent (as for fa_bwd_workspace_bytes).
+ */
+size_t fa_bwd_workspace_bytes_ex(int B, int H, int Lq, int D, int deterministic);
+
+/*
  * Backward.  Given q, k, v, the forward's o and lse, and the output gradient dout, writes
  * dq, dk, dv [B,H,L,D] (dtype).  `workspace` is a device buffer of at least
  * fa_bwd_workspace_bytes(B,H,L,D) bytes, 16-byte aligned, owned by the caller; its contents
@@ -139,16 +150,25 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  * interleaved parts of one packed [B,L,3,H,D] gradient (Lq = Lk, equal strides, the heads of a
  * row together, each part's heads ending before the next part's begin); otherwise no two
  * outputs' extents may overlap, and no output may overlap an input.  fa_bwd is fa_bwd_ex with
- * Lq = Lk = L, contiguous strides and no dropout.  dropout_p and seed must be those of the
- * forward that produced o and lse (the same mask is regenerated): dV = (P o Z)^T dO and
- * dS = P o ((dO V^T) o Z - Delta), Delta = rowsum(dO o O); the backward under dropout always
- * runs one CTA per tile.
+ * Lq = Lk = L, contiguous strides, no dropout and deterministic = 1.  dropout_p and seed must
+ * be those of the forward that produced o and lse (the same mask is regenerated):
+ * dV = (P o Z)^T dO and dS = P o ((dO V^T) o Z - Delta), Delta = rowsum(dO o O); the backward
+ * under dropout always runs one CTA per tile.
+ *
+ * deterministic (0 or 1, else FA_ERR_INVALID_ARG): 1 computes dQ in its own pass, one CTA (or
+ * persistent CTA) per query tile summing its key tiles in a fixed order, so every call gives
+ * the same bits.  0 allows dQ to be computed inside the dK/dV pass ("dQ by atomics or a
+ * separate pass", the method's two options): at D = 64 without dropout each (key tile, query
+ * tile) pair adds its dS K into an fp32 accumulator in the workspace with vector reductions
+ * (additions in arrival order: the result may differ in the last bits between calls) and a
+ * third kernel converts it to dq; elsewhere 0 takes the deterministic path.  The workspace is
+ * then fa_bwd_workspace_bytes_ex(B, H, Lq, D, 0) bytes.
  */
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,
                     const float* lse, void* dq, void* dk, void* dv, void* workspace,
                     size_t workspace_bytes, const fa_strides* strides, int B, int H, int Lq,
                     int Lk, int D, float scale, int causal, double dropout_p, uint64_t seed,
-                    int dtype, void* stream);
+                    int deterministic, int dtype, void* stream);
 
 /* Size of the fixed device scratch array behind fa_bwd_noalloc: 16 MiB. */
 #define FA_BWD_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)

@@ -151,16 +151,19 @@ def test_backward_ex_refuses_one_sided_empty_and_overlapping_outputs(lib):
     p = [A + i * MB for i in range(10)]
     ws = fa.fa_bwd_workspace_bytes(B, H, L, D)
 
-    def call(strides, Lq=L, Lk=L, dropout_p=0.0, **kw):
+    def call(strides, Lq=L, Lk=L, dropout_p=0.0, deterministic=1, **kw):
         q = dict(zip(("q", "k", "v", "o", "do", "lse", "dq", "dk", "dv", "ws"), p))
         q.update(kw)
         return fa.fa_bwd_ex(q["q"], q["k"], q["v"], q["o"], q["do"], q["lse"], q["dq"], q["dk"],
                             q["dv"], q["ws"], ws, strides, B, H, Lq, Lk, D, 0.125, 1, dropout_p,
-                            7, 0, None)
+                            7, deterministic, 0, None)
 
     assert call([c] * 8, Lq=0, Lk=0) == fa.FA_OK
     assert call([c] * 8, dropout_p=1.0) == fa.FA_ERR_INVALID_ARG
     assert call([c] * 8, dropout_p=float("inf")) == fa.FA_ERR_INVALID_ARG
+    assert call([c] * 8, deterministic=2) == fa.FA_ERR_INVALID_ARG
+    # dQ by reduction needs the accumulator: the deterministic-size workspace is too small
+    assert call([c] * 8, deterministic=0) == fa.FA_ERR_INVALID_ARG
     assert call([c] * 8, Lq=0) == fa.FA_ERR_UNSUPPORTED
     assert call([c] * 8, Lk=0) == fa.FA_ERR_UNSUPPORTED
     # dk inside dq's extent with contiguous strides: not the interleaved parts of a packed tensor
@@ -213,3 +216,16 @@ def test_product_package_does_not_touch_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle", text, re.M), f
                 assert "liboracle" not in text and "oracle.c" not in text, f
+
+
+def test_backward_workspace_sizes(lib):
+    B, H, L = 2, 3, 300
+    Lp = 384
+    for D in (64, 128):
+        assert fa.fa_bwd_workspace_bytes(B, H, L, D) == 2 * B * H * Lp * 4
+        assert fa.fa_bwd_workspace_bytes_ex(B, H, L, D, 1) == 2 * B * H * Lp * 4
+    # dQ by reduction (D = 64 only): the fp32 accumulator [B*H, Lqpad, D] follows
+    assert fa.fa_bwd_workspace_bytes_ex(B, H, L, 64, 0) == 2 * B * H * Lp * 4 + B * H * Lp * 64 * 4
+    assert fa.fa_bwd_workspace_bytes_ex(B, H, L, 128, 0) == 2 * B * H * Lp * 4
+    assert fa.fa_bwd_workspace_bytes_ex(B, H, L, 64, 2) == 0
+    assert fa.fa_bwd_workspace_bytes_ex(B, H, 0, 64, 0) == 0

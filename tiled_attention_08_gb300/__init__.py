@@ -23,7 +23,8 @@ import os
 import threading
 
 __all__ = ["FaError", "load_library", "library_path", "fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_ex",
-           "fa_bwd_workspace_bytes", "fa_get_device_status", "fa_set_wait_timeout_ns",
+           "fa_bwd_workspace_bytes", "fa_bwd_workspace_bytes_ex", "fa_get_device_status",
+           "fa_set_wait_timeout_ns",
            "fa_selftest_wait_timeout", "fa_trace_next_call", "fa_launch_count", "fa_status_string",
            "fa_bwd_noalloc", "forward", "backward", "attention", "attention_blhd",
            "attention_qkvpacked", "FaStrides", "fa_decode_paged", "fa_decode_workspace_bytes",
@@ -41,7 +42,7 @@ _lib = None
 _lock = threading.Lock()
 
 EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_ex", "fa_bwd_workspace_bytes",
-            "fa_get_device_status",
+            "fa_bwd_workspace_bytes_ex", "fa_get_device_status",
             "fa_set_wait_timeout_ns", "fa_selftest_wait_timeout", "fa_trace_next_call",
             "fa_launch_count", "fa_status_string", "fa_bwd_noalloc", "fa_decode_paged",
             "fa_decode_workspace_bytes")
@@ -84,7 +85,9 @@ def load_library():
         lib.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, sp, i, i, i, i, i, f, i, d64, u64, i, vp]
         lib.fa_fwd_ex.restype = i
         lib.fa_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, sp, i, i, i, i, i, f,
-                                  i, d64, u64, i, vp]
+                                  i, d64, u64, i, i, vp]
+        lib.fa_bwd_workspace_bytes_ex.argtypes = [i, i, i, i, i]
+        lib.fa_bwd_workspace_bytes_ex.restype = sz
         lib.fa_bwd_ex.restype = i
         lib.fa_decode_workspace_bytes.argtypes = [i, i, i, i]
         lib.fa_decode_workspace_bytes.restype = sz
@@ -130,12 +133,17 @@ def fa_fwd_ex(q, k, v, o, lse, strides, B, H, Lq, Lk, D, scale, causal, dropout_
 
 
 def fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, strides, B, H, Lq,
-              Lk, D, scale, causal, dropout_p, seed, dtype, stream) -> int:
+              Lk, D, scale, causal, dropout_p, seed, deterministic, dtype, stream) -> int:
     """``strides``: eight (batch, head, row) tuples for q, k, v, o, dout, dq, dk, dv."""
     return load_library().fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace,
                                     workspace_bytes, _strides_array(strides), B, H, Lq, Lk, D,
                                     scale, int(causal), float(dropout_p),
-                                    int(seed) & 0xFFFFFFFFFFFFFFFF, dtype, stream)
+                                    int(seed) & 0xFFFFFFFFFFFFFFFF, int(deterministic), dtype,
+                                    stream)
+
+
+def fa_bwd_workspace_bytes_ex(B, H, Lq, D, deterministic) -> int:
+    return int(load_library().fa_bwd_workspace_bytes_ex(B, H, Lq, D, int(deterministic)))
 
 
 def fa_decode_workspace_bytes(B, H, D, max_pages) -> int:
@@ -253,10 +261,12 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
 
 
 def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
-             workspace=None, grads=None, dropout_p: float = 0.0, seed: int = 0):
+             workspace=None, grads=None, dropout_p: float = 0.0, seed: int = 0,
+             deterministic: bool = True):
     """dQ, dK, dV for the forward above (with that forward's ``dropout_p`` and ``seed``).
     ``grads`` optionally gives the three output views (for example the parts of one packed
-    gradient tensor); by default they are allocated like q, k, v."""
+    gradient tensor); by default they are allocated like q, k, v.  ``deterministic=False``
+    lets the library reduce dQ inside the dK/dV pass (D = 64, no dropout; see fa_bwd_ex)."""
     import torch
     B, H, Lq, D = q.shape
     Lk = k.shape[2]
@@ -268,7 +278,7 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     dt = _dtype_code(q)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    ws_bytes = fa_bwd_workspace_bytes(B, H, Lq, D)
+    ws_bytes = fa_bwd_workspace_bytes_ex(B, H, Lq, D, deterministic)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), device=q.device, dtype=torch.uint8)
     if grads is None:
@@ -279,8 +289,8 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     status = fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
                        lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                        workspace.data_ptr(), workspace.numel() * workspace.element_size(), st,
-                       B, H, Lq, Lk, D, float(scale), causal, dropout_p, seed, dt,
-                       _stream_handle(q.device))
+                       B, H, Lq, Lk, D, float(scale), causal, dropout_p, seed, deterministic,
+                       dt, _stream_handle(q.device))
     if status != FA_OK:
         raise FaError("fa_bwd_ex", status)
     return dq, dk, dv
@@ -296,7 +306,7 @@ def _dropout_seed(dropout_p: float, seed: int | None) -> int:
 
 
 def attention(q, k, v, causal: bool = False, scale: float | None = None, dropout_p: float = 0.0,
-              seed: int | None = None):
+              seed: int | None = None, deterministic: bool = True):
     """Differentiable attention for torch autograd (forward and backward run in libfa) over
     [B, H, L, D] views (Lq may differ from Lk).  With ``dropout_p`` > 0 the forward and the
     backward regenerate the same dropout mask from ``seed`` (drawn from torch's generator when
@@ -317,7 +327,7 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, dropout
             if do_.stride(-1) != 1:
                 do_ = do_.contiguous()
             return backward(q_, k_, v_, o_, lse_, do_, causal, scale, dropout_p=dropout_p,
-                            seed=seed_)
+                            seed=seed_, deterministic=deterministic)
 
     return _Attention.apply(q, k, v)
 

@@ -208,6 +208,20 @@ bool make_dropout(double p, uint64_t seed, Dropout* d) {
     return true;
 }
 
+// Whether the backward reduces dQ inside the dK/dV pass (non-deterministic: fp32 additions in
+// arrival order) instead of running the separate dQ pass: only when the caller allows it, at
+// D = 64 (TMEM holds the extra accumulators only there) and without dropout.
+bool dq_reduce_path(int D, int deterministic, double dropout_p) {
+    return deterministic == 0 && D == 64 && !(dropout_p > 0.0);
+}
+
+// Backward workspace: -LSE*log2(e) and Delta ([BH, Lqpad] fp32 each), then for dQ by reduction
+// the fp32 accumulator [BH, Lqpad, D].
+size_t bwd_workspace_need(const Shape& sh, int D, bool dq_reduce) {
+    const size_t rows = (size_t)sh.BH * (size_t)sh.Lqpad;
+    return 2u * rows * 4u + (dq_reduce ? rows * (size_t)D * 4u : 0u);
+}
+
 }  // namespace
 
 void trace_disarm() { t_trace_pairs = 0; }
@@ -367,26 +381,34 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int L, int D) {
+    return fa_bwd_workspace_bytes_ex(B, H, L, D, 1);
+}
+
+size_t fa_bwd_workspace_bytes_ex(int B, int H, int Lq, int D, int deterministic) {
     Shape sh;
-    if (check_shape(B, H, L, L, D, 1.0f, 0, FA_BF16, &sh) != FA_OK || sh.empty) return 0;
-    return 2u * (size_t)sh.BH * (size_t)sh.Lqpad * 4u;
+    if ((deterministic != 0 && deterministic != 1) ||
+        check_shape(B, H, Lq, Lq, D, 1.0f, 0, FA_BF16, &sh) != FA_OK || sh.empty)
+        return 0;
+    return bwd_workspace_need(sh, D, dq_reduce_path(D, deterministic, 0.0));
 }
 
 fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,
                     const float* lse, void* dq, void* dk, void* dv, void* workspace,
                     size_t workspace_bytes, const fa_strides* strides, int B, int H, int Lq,
                     int Lk, int D, float scale, int causal, double dropout_p, uint64_t seed,
-                    int dtype, void* stream) {
+                    int deterministic, int dtype, void* stream) {
     TraceDisarm disarm;
     Shape sh;
     fa_status st = check_shape(B, H, Lq, Lk, D, scale, causal, dtype, &sh);
     if (st != FA_OK) return st;
     Dropout drop;
     if (!make_dropout(dropout_p, seed, &drop)) return FA_ERR_INVALID_ARG;
+    if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID_ARG;
     if (sh.BH == 0 || (Lq == 0 && Lk == 0)) return FA_OK;  // nothing to compute
     if (Lq == 0 || Lk == 0) return FA_ERR_UNSUPPORTED;     // queries without keys, or keys
                                                            // without queries
-    const size_t ws_need = 2u * (size_t)sh.BH * (size_t)sh.Lqpad * 4u;
+    const bool dqr = dq_reduce_path(D, deterministic, dropout_p);
+    const size_t ws_need = bwd_workspace_need(sh, D, dqr);
     if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace || !strides)
         return FA_ERR_INVALID_ARG;
     if (workspace_bytes < ws_need) return FA_ERR_INVALID_ARG;
@@ -450,6 +472,7 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.drop = drop;
+    p.dq_acc = dqr ? delta_pad + (size_t)sh.BH * sh.Lqpad : nullptr;
     p.status = status_ptr();
     p.timeout_ns = g_timeout_ns.load();
     if (!p.status) return FA_ERR_CUDA;
@@ -465,6 +488,7 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     pp.lse = lse;
     pp.nlse2_pad = nlse2_pad;
     pp.delta_pad = delta_pad;
+    pp.dq_acc = p.dq_acc;
     pp.Lq = Lq;
     pp.Lqpad = sh.Lqpad;
     pp.H = H;
@@ -472,13 +496,22 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     pp.D = D;
     // Under the causal mask query row i sees key j iff j <= i + Lk - Lq: rows below Lq - Lk
     // see none (their dQ is zero).
-    pp.first_seen_row = (causal && Lq > Lk) ? Lq - Lk : 0;
+    // (With dQ by reduction the conversion writes every row, zeros included.)
+    pp.first_seen_row = (causal && Lq > Lk && !dqr) ? Lq - Lk : 0;
     pp.bf16 = bf16 ? 1 : 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (traced_launch(0, s, [&] { return launch_bwd_pre(pp, s); }) != cudaSuccess)
         return FA_ERR_CUDA;
     const bool dr = dropout_p > 0.0;
+    if (dqr) {
+        if (traced_launch(1, s, [&] { return launch_bwd_dkdv_dq_reduce(p, bf16, causal != 0, s); }) !=
+            cudaSuccess)
+            return FA_ERR_CUDA;
+        if (traced_launch(2, s, [&] { return launch_bwd_dq_convert(p, D, bf16, s); }) != cudaSuccess)
+            return FA_ERR_CUDA;
+        return FA_OK;
+    }
     if (traced_launch(1, s, [&] { return launch_bwd_dkdv(p, D, bf16, causal != 0, dr, s); }) !=
         cudaSuccess)
         return FA_ERR_CUDA;
@@ -495,7 +528,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     const fa_strides c = {(int64_t)H * L * D, (int64_t)L * D, (int64_t)D};
     const fa_strides all[8] = {c, c, c, c, c, c, c, c};
     return fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, all, B, H, L,
-                     L, D, scale, causal, 0.0, 0, dtype, stream);
+                     L, D, scale, causal, 0.0, 0, 1, dtype, stream);
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int D, int max_pages) {

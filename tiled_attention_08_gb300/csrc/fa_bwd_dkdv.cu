@@ -45,7 +45,9 @@
 namespace fa {
 namespace {
 
-template <int D, bool BF16, bool CAUSAL>
+// DQA: the dK/dV pass also computes dQ_i += dS_i K_j and reduces it into an fp32 accumulator in
+// global memory (the deterministic alternative is the separate dQ pass).
+template <int D, bool BF16, bool CAUSAL, bool DQA = false>
 struct DkdvCfg {
     static constexpr int kChunks = D / kChunkElems;
     static constexpr int kTileBytes = kTileRows * D * 2;
@@ -54,11 +56,11 @@ struct DkdvCfg {
     // D = 128 the tiles then fill 224 KB of the 227 KB a block may have, so everything else
     // (the -LSE*log2e and Delta vectors, the barriers) lives in the same 1024-aligned dynamic
     // allocation and no alignment slack is requested.
-    static constexpr int kQStages = (D == 128) ? 3 : 5;
+    static constexpr int kQStages = (D == 128 || DQA) ? 3 : 5;
     static constexpr int kOStages = (D == 128) ? 2 : 4;
     // K_j / V_j slots: two at D = 64, so the next item's key tile lands while this one runs;
     // one at D = 128, where the tiles already take 224 KB.
-    static constexpr int kKVSlots = (D == 128) ? 1 : 2;
+    static constexpr int kKVSlots = (D == 128 || DQA) ? 1 : 2;
     // With three or more dO slots the MMA warp waits for dO_{t+1} before issuing dK_t, and the
     // producer issues dO_{t+1} only after Q_{t+2}, whose slot dK_{t+2-kQStages} frees: with two
     // Q slots that is dK_t itself, a circular wait.
@@ -67,7 +69,14 @@ struct DkdvCfg {
     static constexpr int kOffK = 0;           // slot s: K at kOffK + 2*s*kTileBytes, then V
     static constexpr int kOffQ = 2 * kKVSlots * kTileBytes;
     static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;
-    static constexpr int kOffNlse = kOffDO + kOStages * kTileBytes;  // per Q slot
+    // DQA: dS_i (128 queries x 128 keys, 16-bit), the A operand of dQ_i = dS_i K_j, written by
+    // the elementwise warps in the MN-major 128-byte-swizzled layout (queries contiguous); two
+    // buffers (query tile i in buffer i % 2), so dS_{i+1} never waits for dQ_i.  They take the
+    // room of two Q slots (three instead of five).
+    static constexpr int kOffDS = kOffDO + kOStages * kTileBytes;
+    static constexpr int kDSTile = kTileRows * kTileRows * 2;
+    static constexpr int kDSBytes = DQA ? 2 * kDSTile : 0;
+    static constexpr int kOffNlse = kOffDS + kDSBytes;                // per Q slot
     static constexpr int kOffDelta = kOffNlse + kQStages * kVecBytes;  // per dO slot
     static constexpr int kOffBar = kOffDelta + kOStages * kVecBytes;
     static constexpr int kSplit = 4;  // elementwise warps per TMEM lane quadrant
@@ -82,24 +91,31 @@ struct DkdvCfg {
     static constexpr uint32_t kTmST = 0, kTmDPT = 128, kTmDV = 256, kTmDK = 256 + D;
     static constexpr uint32_t kIdescS = idesc_f16(BF16, 128, 128, false, false);
     static constexpr uint32_t kIdescG = idesc_f16(BF16, 128, D, false, true);
+    // DQA: two dQ accumulators of D columns after dK (TMEM has room for them at D = 64 only).
+    static constexpr uint32_t kTmDQ = 256 + 2 * D;
+    static constexpr uint32_t kIdescQ = idesc_f16(BF16, 128, D, true, true);
+    static_assert(!DQA || D == 64, "dQ by reduction needs 2*D more TMEM columns: D = 64 only");
 };
 
-// Barriers and small shared state, placed after the tiles in dynamic shared memory.
+// Barriers and small shared state, placed after the tiles in dynamic shared memory.  dqf / dqe
+// (DQA only): dQ accumulator b computed / read out.
 template <int KVS, int QS, int OS>
 struct DkdvBars {
     uint64_t kvf[KVS], kve[KVS], qf[QS], qe[QS], of[OS], oe[OS], sf, df, sr, ppd, done, fin;
+    uint64_t dqf[2], dqe[2];
     uint32_t tmem_base;
     int abort;
 };
 
-template <int D, bool BF16, bool CAUSAL>
-using DkdvBarsT = DkdvBars<DkdvCfg<D, BF16, CAUSAL>::kKVSlots, DkdvCfg<D, BF16, CAUSAL>::kQStages,
-                           DkdvCfg<D, BF16, CAUSAL>::kOStages>;
+template <int D, bool BF16, bool CAUSAL, bool DQA = false>
+using DkdvBarsT = DkdvBars<DkdvCfg<D, BF16, CAUSAL, DQA>::kKVSlots,
+                           DkdvCfg<D, BF16, CAUSAL, DQA>::kQStages,
+                           DkdvCfg<D, BF16, CAUSAL, DQA>::kOStages>;
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool DQA = false>
 constexpr int dkdv_smem_bytes() {
-    using C = DkdvCfg<D, BF16, CAUSAL>;
-    return C::kOffBar + (int)sizeof(DkdvBarsT<D, BF16, CAUSAL>);
+    using C = DkdvCfg<D, BF16, CAUSAL, DQA>;
+    return C::kOffBar + (int)sizeof(DkdvBarsT<D, BF16, CAUSAL, DQA>);
 }
 
 // One work item: key tile kt of head bh and the query tiles [it0, it0 + n_it) that see it.
@@ -123,10 +139,17 @@ __device__ __forceinline__ bool dkdv_item(const BwdParams& p, int round, DkdvIte
 // the causal tiles): for rows of many query tiles, where a CTA's fixed cost is a small share.
 // DROP: dropout on P (p.drop): dV accumulates (P o keep)^T dO and is scaled by 1/(1-p) on the
 // way out; dS^T = P^T o (dP^T o Z^T - Delta) with Z the keep mask times 1/(1-p).
-template <int D, bool BF16, bool CAUSAL, bool DROP>
-__global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
+// DQA: also dQ_i += dS_i K_j into p.dq_acc.  The elementwise warps write dS_i to shared memory
+// (buffer i % 2) beside the 16-bit dS_i^T they put in TMEM; the MMA warp issues dQ_i = dS_i K_j
+// (A = dS_i from shared memory, B = the K tile read MN-major) into TMEM accumulator i % 2 after
+// dP^T of the next query tile; the elementwise warps wait for it, read it out and reduce it
+// into global memory with 16-byte red.add after publishing P^T / dS^T of the next query tile,
+// then free the accumulator.  Buffer i % 2 is written again (dS_{i+2}) only after that
+// read-out has seen dQ_i complete.
+template <int D, bool BF16, bool CAUSAL, bool DROP, bool DQA>
+__global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL, DQA>::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
-    using C = DkdvCfg<D, BF16, CAUSAL>;
+    using C = DkdvCfg<D, BF16, CAUSAL, DQA>;
     // The kernel declares no static shared memory, so its dynamic shared memory starts at the
     // block's shared window, which is 1024-byte aligned; checked here (the 128-byte swizzle
     // needs it) before any barrier, TMEM or copy is touched.
@@ -138,7 +161,7 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
     // Q_i (+ LSE_i) and dO_i (+ Delta_i) have their own rings and full/empty barriers: Q_i is
     // released by dK_i, issued first, so the load of a later Q tile (needed early, by S^T)
     // starts sooner.
-    auto& bars = *reinterpret_cast<DkdvBarsT<D, BF16, CAUSAL>*>(smem + C::kOffBar);
+    auto& bars = *reinterpret_cast<DkdvBarsT<D, BF16, CAUSAL, DQA>*>(smem + C::kOffBar);
     uint64_t& bar_kv = bars.kvf[0];
     uint64_t* bar_qf = bars.qf;
     uint64_t* bar_qe = bars.qe;
@@ -181,6 +204,10 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
         mbar_init(&bar_ppd, C::kEwThreads);  // P^T and dS^T written into the dP^T columns
         mbar_init(&bar_done, 1);
         mbar_init(&bar_fin, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars.dqf[b], 1);
+            mbar_init(&bars.dqe[b], C::kEwThreads);
+        }
         mbar_fence_init();
     }
     if (warp == C::kMmaWarp) tmem_alloc(&tmem_base_sh, C::kTmemCols);
@@ -347,6 +374,23 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
                 }
                 issue_dpt(t + 1);
             }
+            if constexpr (DQA) {  // dQ_t = dS_t K into accumulator t % 2, once read out twice ago
+                const int b = t & 1;
+                if (t >= 2 && !wait_warp(&bars.dqe[b], ((uint32_t)(t - 2) >> 1) & 1u, abort_v,
+                                         p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint64_t dsd =
+                    sdesc_mnmajor_sw128(smem_u32(smem + C::kOffDS + b * C::kDSTile), kChunkBytes);
+                const uint64_t kmd = sdesc_mnmajor_sw128(k_base, kChunkBytes);
+#pragma unroll
+                for (int kk = 0; kk < kTileRows / 16; ++kk)
+                    mma_ss_w(tmem + C::kTmDQ + b * D, sdesc_advance(dsd, kk * 2048),
+                             sdesc_advance(kmd, kk * 2048), C::kIdescQ, kk > 0 ? 1u : 0u);
+                mma_commit_w(&bars.dqf[b]);
+            }
         }
         if (ok) mma_commit_w(&bar_done);
         if (!ok && lane == 0) record_timeout(p.status, abort_v);
@@ -363,6 +407,48 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const int key = kt * kTileRows + row;
         const int c0 = part * kC;
+        // DQA: dQ_tq (TMEM accumulator tq % 2; lane = query row (it0 + tq) * 128 + lane) into
+        // p.dq_acc.  A TMEM load gives each thread 16 columns of one row, and 16-byte
+        // reductions from 32 rows at once would touch 32 memory lines per instruction; so the
+        // quadrant's four warps stage their rows in shared memory (the dS buffer of query tile
+        // tq, which dQ_tq has finished reading: the 8 KB that this quadrant's dS rows occupy,
+        // rows 256 B apart with the 16-byte unit index XORed by row % 16) and each warp then
+        // reduces 8 whole rows, two 256-byte rows per instruction.  Every warp of the quadrant
+        // calls it the same number of times (it holds the quadrant's named barrier); `go`
+        // false skips the work, and the result is the quadrant's AND of it.
+        auto dq_reduce = [&](int tq, bool go) -> bool {
+            constexpr int kQc = 16;
+            static_assert(!DQA || D / C::kSplit == kQc, "16 dQ columns per warp slice");
+            static_assert(!DQA || D == 64, "256-byte dQ rows");
+            uint8_t* stage = smem + C::kOffDS + (tq & 1) * C::kDSTile + quad * 4096;
+            auto unit = [&](int r, int u) {  // 16-byte unit u of the quadrant's row r
+                return stage + (r >> 4) * kChunkBytes + (r & 15) * 256 + ((u ^ (r & 15)) << 4);
+            };
+            if (go) {
+                tc_fence_after_sync();
+                uint32_t r[kQc];
+                tmem_ld16(tmem + lane_off + C::kTmDQ + (tq & 1) * D + part * kQc, r);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4*>(unit(lane, part * 4 + j)) =
+                        make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+            }
+            go = bar_and(grp_bar, kGrpThreads, go);
+            if (go) {
+                const int r0 = part * 8 + (lane >> 4), u = lane & 15;
+                float* dst = p.dq_acc +
+                             ((size_t)bh * p.Lqpad + (size_t)(it0 + tq) * kTileRows + quad * 32) *
+                                 D +
+                             u * 4;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int rr = r0 + 2 * i;
+                    const float4 x = *reinterpret_cast<const float4*>(unit(rr, u));
+                    red_add_v4(dst + (size_t)rr * D, x.x, x.y, x.z, x.w);
+                }
+            }
+            return go;
+        };
         bool ok = true;
         for (int t = 0; t < n_it; ++t) {
             const int it = it0 + t;
@@ -376,8 +462,9 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
             const bool masked = tile_masked(it, kt, p.Lq, p.Lk, CAUSAL);
             const int qlim = p.Lq - 1;  // last valid query
             // Phase 1: P^T = exp2(S^T * scale*log2e - LSE*log2e) on this warp's columns; kept
-            // in registers, and the S^T columns are released at once.
-            ok = wait_bounded(&bar_qf[qs], qph, abort_v, p.timeout_ns) &&
+            // in registers, and the S^T columns are released at once.  (ok is false here only
+            // after a failed wait of the dQ read-out.)
+            ok = ok && wait_bounded(&bar_qf[qs], qph, abort_v, p.timeout_ns) &&
                  wait_bounded(&bar_sf, (uint32_t)t & 1u, abort_v, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
             float pv[kC];
@@ -486,15 +573,41 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < kC / 2; ++i) pk[i] = pack2<BF16>(pv[2 * i], pv[2 * i + 1]);
                 tmem_st<kC / 2>(tmem + lane_off + C::kTmDPT + 64 + part * (kC / 2), pk);
+                if constexpr (DQA) {
+                    // dS row `row` (a key), queries c0..c0+31: four 16-byte units of the
+                    // MN-major tile (64-query chunks 16 KB apart, 128-byte rows per key, the
+                    // unit index XORed with key % 8).
+                    static_assert(kC == 32, "four 16-byte units per warp slice");
+                    uint8_t* ds_row = smem + C::kOffDS + (t & 1) * C::kDSTile +
+                                      (c0 >> 6) * kChunkBytes + (row >> 3) * 1024 + (row & 7) * 128;
+                    const int u0 = (c0 & 63) >> 3;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<uint4*>(ds_row + (((u0 + j) ^ (row & 7)) << 4)) =
+                            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    fence_proxy_async_smem();
+                }
             }
             tmem_st_wait();
             tc_fence_before_sync();
             mbar_arrive(&bar_ppd);
+            if constexpr (DQA) {  // dQ_{t-1}: read out and reduce, then free its accumulator
+                if (t > 0) {
+                    ok = wait_warp(&bars.dqf[(t - 1) & 1], ((uint32_t)(t - 1) >> 1) & 1u, abort_v,
+                                   p.timeout_ns);
+                    ok = dq_reduce(t - 1, ok);
+                    if (ok) {
+                        tc_fence_before_sync();
+                        mbar_arrive(&bars.dqe[(t - 1) & 1]);
+                    }
+                }
+            }
         }
         if (ok) {
             ok = wait_bounded(&bar_done, 0, abort_v, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
         }
+        if constexpr (DQA) ok = dq_reduce(n_it - 1, ok);  // every warp of the quadrant
         if (!ok) {
             if (lane == 0) record_timeout(p.status, abort_v);
         } else {
@@ -929,16 +1042,16 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
     }
 }
 
-template <int D, bool BF16, bool CAUSAL, bool DROP>
+template <int D, bool BF16, bool CAUSAL, bool DROP, bool DQA>
 cudaError_t launch_t(const BwdParams& p, cudaStream_t s) {
-    using C = DkdvCfg<D, BF16, CAUSAL>;
-    constexpr int kSmem = dkdv_smem_bytes<D, BF16, CAUSAL>();
+    using C = DkdvCfg<D, BF16, CAUSAL, DQA>;
+    constexpr int kSmem = dkdv_smem_bytes<D, BF16, CAUSAL, DQA>();
     static_assert(kSmem <= 232448, "dynamic shared memory over the 227 KB per-block limit");
     const int total = p.n_ktiles * p.BH;
-    // The persistent kernel has no dropout variant.
-    const int grid = DROP ? total : dkdv_grid(p.Lq, p.Lk, p.BH, CAUSAL, sm_count());
+    // The persistent kernel has neither a dropout nor a dQ-reduction variant.
+    const int grid = (DROP || DQA) ? total : dkdv_grid(p.Lq, p.Lk, p.BH, CAUSAL, sm_count());
     auto kern = grid < total ? fa_bwd_dkdv_kernel_persistent<D, BF16, CAUSAL>
-                             : fa_bwd_dkdv_kernel<D, BF16, CAUSAL, DROP>;
+                             : fa_bwd_dkdv_kernel<D, BF16, CAUSAL, DROP, DQA>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     return launch_kernel(kern, (unsigned)grid, C::kThreads, kSmem, s, p);
@@ -946,8 +1059,11 @@ cudaError_t launch_t(const BwdParams& p, cudaStream_t s) {
 
 template <int D, bool BF16>
 cudaError_t launch_d(const BwdParams& p, bool causal, bool drop, cudaStream_t s) {
-    if (drop) return causal ? launch_t<D, BF16, true, true>(p, s) : launch_t<D, BF16, false, true>(p, s);
-    return causal ? launch_t<D, BF16, true, false>(p, s) : launch_t<D, BF16, false, false>(p, s);
+    if (drop)
+        return causal ? launch_t<D, BF16, true, true, false>(p, s)
+                      : launch_t<D, BF16, false, true, false>(p, s);
+    return causal ? launch_t<D, BF16, true, false, false>(p, s)
+                  : launch_t<D, BF16, false, false, false>(p, s);
 }
 
 }  // namespace
@@ -957,6 +1073,14 @@ cudaError_t launch_bwd_dkdv(const BwdParams& p, int D, bool bf16, bool causal, b
     if (D == 64)
         return bf16 ? launch_d<64, true>(p, causal, drop, s) : launch_d<64, false>(p, causal, drop, s);
     return bf16 ? launch_d<128, true>(p, causal, drop, s) : launch_d<128, false>(p, causal, drop, s);
+}
+
+cudaError_t launch_bwd_dkdv_dq_reduce(const BwdParams& p, bool bf16, bool causal, cudaStream_t s) {
+    if (bf16)
+        return causal ? launch_t<64, true, true, false, true>(p, s)
+                      : launch_t<64, true, false, false, true>(p, s);
+    return causal ? launch_t<64, false, true, false, true>(p, s)
+                  : launch_t<64, false, false, false, true>(p, s);
 }
 
 }  // namespace fa

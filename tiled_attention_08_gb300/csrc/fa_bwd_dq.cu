@@ -792,7 +792,43 @@ cudaError_t launch_d(const BwdParams& p, bool causal, bool drop, cudaStream_t s)
     return causal ? launch_t<D, BF16, true, false>(p, s) : launch_t<D, BF16, false, false>(p, s);
 }
 
+// dQ by reduction: dQ = scale * dq_acc rounded to 16 bits, for every row < Lq (rows that see
+// no key hold zeros).  HBM-bound: 16-byte stores, two 16-byte loads per store.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const BwdParams p) {
+    constexpr int kPieces = D / 8;  // 8 elements (16 output bytes) per piece
+    const long long total = (long long)p.BH * p.Lq * kPieces;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int c = (int)(e % kPieces);
+        const long long r_all = e / kPieces;
+        const int bh = (int)(r_all / p.Lq), i = (int)(r_all - (long long)bh * p.Lq);
+        const float4* src = reinterpret_cast<const float4*>(
+            p.dq_acc + ((size_t)bh * p.Lqpad + i) * D + c * 8);
+        const float4 a = src[0], b = src[1];
+        const float m = p.scale;
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dq) +
+                                  row_offset(p.sdq, bh, p.H, i) + c * 16) =
+            make_uint4(pack2<BF16>(a.x * m, a.y * m), pack2<BF16>(a.z * m, a.w * m),
+                       pack2<BF16>(b.x * m, b.y * m), pack2<BF16>(b.z * m, b.w * m));
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_dq_convert(const BwdParams& p, int D, bool bf16, cudaStream_t s) {
+    const long long work = (long long)p.BH * p.Lq * (D / 8);
+    const int sms = sm_count() > 0 ? sm_count() : 148;
+    long long blocks = (work + 255) / 256;
+    if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
+    if (blocks < 1) blocks = 1;
+    const dim3 g((unsigned)blocks), b(256);
+    if (D == 64)
+        return bf16 ? launch_kernel(fa_bwd_dq_convert_kernel<64, true>, g, b, 0, s, p)
+                    : launch_kernel(fa_bwd_dq_convert_kernel<64, false>, g, b, 0, s, p);
+    return bf16 ? launch_kernel(fa_bwd_dq_convert_kernel<128, true>, g, b, 0, s, p)
+                : launch_kernel(fa_bwd_dq_convert_kernel<128, false>, g, b, 0, s, p);
+}
 
 cudaError_t launch_bwd_dq(const BwdParams& p, int D, bool bf16, bool causal, bool drop,
                           cudaStream_t s) {

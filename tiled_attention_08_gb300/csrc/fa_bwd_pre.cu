@@ -7,7 +7,9 @@
 // Both per-row vectors go to a workspace padded to a whole number of 128-row tiles (zeros past
 // Lq), so the backward kernels can copy them tile by tile with aligned bulk copies.  Rows that
 // see no key (the first Lq - Lk queries under the causal mask when Lq > Lk) get dQ = 0 here;
-// the dQ pass skips query tiles in which no row sees a key.
+// the dQ pass skips query tiles in which no row sees a key.  When dQ is reduced into an fp32
+// accumulator by the dK/dV pass instead, this kernel zeroes the accumulator's rows (all Lqpad
+// of them) as it goes.
 //
 // HBM-bound: every (row, D) element of O and dO is read once, with 16-byte loads; D/8 threads
 // share a row and reduce with shuffles.
@@ -34,10 +36,16 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdPreParams p) {
         const uint8_t* d_head =
             reinterpret_cast<const uint8_t*>(p.dout) + row_offset(p.sdo, bh, p.H, 0) + g * 16;
         uint8_t* q_head = reinterpret_cast<uint8_t*>(p.dq) + row_offset(p.sdq, bh, p.H, 0) + g * 16;
+        float* acc_head = p.dq_acc ? p.dq_acc + (size_t)bh * p.Lqpad * D + g * 8 : nullptr;
         const size_t o_step = (size_t)p.so.l * 2u, d_step = (size_t)p.sdo.l * 2u;
 #pragma unroll 2
         for (int pass = 0; pass < kTileRows / kRowsPerPass; ++pass) {
             const int i = i0 + pass * kRowsPerPass;
+            if (acc_head) {  // i < Lqpad always: the grid covers the padded tiles
+                float4* z = reinterpret_cast<float4*>(acc_head + (size_t)i * D);
+                z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+                z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
             float acc = 0.0f;
             if (i < p.Lq) {
                 const uint4 a = *reinterpret_cast<const uint4*>(o_head + (size_t)i * o_step);

@@ -79,6 +79,7 @@ struct BwdPreParams {
     const float* lse;    // [BH, Lq]
     float* nlse2_pad;    // [BH, Lqpad]: -LSE * log2(e), zero past Lq
     float* delta_pad;    // [BH, Lqpad]: rowsum(dO * O), zero past Lq
+    float* dq_acc;       // [BH, Lqpad, D] fp32, zeroed here (dQ by reduction), or null
     int Lq, Lqpad, H, BH, D;
     int first_seen_row;  // rows below this see no key (causal with Lq > Lk), else 0
     int bf16;
@@ -118,6 +119,7 @@ struct BwdParams {
     float scale;        // softmax scale (applied to dQ and dK)
     float scale_log2;   // scale * log2(e)
     Dropout drop;
+    float* dq_acc;      // [BH, Lqpad, D] fp32: dQ by reduction in the dK/dV pass, or null
     int* status;
     uint64_t timeout_ns;
 };
@@ -154,6 +156,10 @@ cudaError_t launch_fwd_empty_rows(const FwdParams& p, int D, int rows, cudaStrea
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdParams& p, int D, bool bf16, bool causal, bool drop,
                             cudaStream_t s);
+// The dK/dV pass that also reduces dQ = dS K into p.dq_acc (D = 64, no dropout), then the
+// conversion of p.dq_acc (times the scale) into p.dq.
+cudaError_t launch_bwd_dkdv_dq_reduce(const BwdParams& p, bool bf16, bool causal, cudaStream_t s);
+cudaError_t launch_bwd_dq_convert(const BwdParams& p, int D, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dq(const BwdParams& p, int D, bool bf16, bool causal, bool drop,
                           cudaStream_t s);
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s);
