@@ -244,6 +244,17 @@ fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cach
  */
 fa_status fa_get_device_status(void* stream);
 
+/*
+ * Selects the forward kernel at D = 128 without dropout: mode 1 runs it on CTA pairs (one
+ * tensor-core contraction of 256 query rows over two SMs, tcgen05 cta_group::2, each CTA
+ * loading half of every K and V tile), mode 0 (the default) on single CTAs.  The two give the
+ * same results up to the order of nothing: every row's arithmetic is the same, so O and LSE are
+ * bit for bit equal.  Process-wide; other head sizes and dropout always use single CTAs.
+ * FA_ERR_INVALID_ARG for other modes.  The pages have no counterpart (TFLOPS page, sections
+ * 3.2-3.3 size tiles for one SM).
+ */
+fa_status fa_set_forward_pair(int mode);
+
 /* Time limit of every device-side wait, in nanoseconds (default 4e9).  0 restores the
  * default.  Applies to launches made after the call; returns FA_OK. */
 fa_status fa_set_wait_timeout_ns(uint64_t timeout_ns);

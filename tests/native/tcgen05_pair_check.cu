@@ -8,7 +8,9 @@
 //     each CTA's tensor memory receives its own 128 rows x all N columns;
 //   * the TS form (A from tensor memory, each CTA holding its 128 rows);
 //   * completion signalled to both CTAs' mbarriers with two plain commits (no multicast).
-// Inputs are small integers, so every fp32 sum is exact and the check is bit for bit.
+// Inputs are small integers, so every fp32 sum is exact and the check is bit for bit.  It also
+// times 2048 back-to-back pair steps (M = 256, N = 128, K = 16) of each form: clock64 cycles
+// per step, against 64 for a single-CTA M = 128 step.
 // Every wait is bounded (2 s); the program prints one JSON object and exits non-zero on a
 // mismatch or a timeout.
 //
@@ -99,8 +101,10 @@ __device__ void put(uint8_t* tile, int row, int k, float v) {
 }
 
 // ts = 0: D = A B^T with A from shared memory; ts = 1: A copied into tensor memory first.
+// reps > 0: instead of one product, `reps` groups of 8 steps back to back, timed (cycles of the
+// even CTA into *cycles).
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
-    pair_kernel(int ts, float* out, int* status) {
+    pair_kernel(int ts, int reps, float* out, int* status, long long* cycles) {
     extern __shared__ uint8_t raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -145,17 +149,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
         cluster_sync_all();  // both CTAs' A in TMEM before the even CTA issues
         tc_fence_after_sync();
     }
+    long long t0 = 0;
     if (same && rank == 0 && warp == 0) {
         const uint32_t idesc = idesc_f16(true, 256, N, false, false);
         const uint64_t ad = sdesc_kmajor_sw128(smem_u32(a_tile));
         const uint64_t bd = sdesc_kmajor_sw128(smem_u32(b_tile));
+        __syncwarp();
+        t0 = clock64();
+        const int groups = reps > 0 ? reps : 1;
+        for (int g = 0; g < groups; ++g) {
 #pragma unroll
-        for (int kk = 0; kk < K / 16; ++kk) {
-            if (ts)
-                mma_pair_ts(tm, tm + 128 + kk * 8, sdesc_advance(bd, kk * 32), idesc, kk > 0);
-            else
-                mma_pair_ss(tm, sdesc_advance(ad, kk * 32), sdesc_advance(bd, kk * 32), idesc,
-                            kk > 0);
+            for (int kk = 0; kk < 8; ++kk) {
+                const int k4 = kk & (K / 16 - 1);  // K / 16 = 4 distinct slices, repeated
+                if (ts)
+                    mma_pair_ts(tm, tm + 128 + k4 * 8, sdesc_advance(bd, k4 * 32), idesc,
+                                (g | kk) ? 1u : 0u);
+                else
+                    mma_pair_ss(tm, sdesc_advance(ad, k4 * 32), sdesc_advance(bd, k4 * 32),
+                                idesc, (g | kk) ? 1u : 0u);
+                if (reps == 0 && kk == K / 16 - 1) break;  // the checked product: K = 64
+            }
         }
         commit_pair(smem_u32(&bar));                  // this CTA
         commit_pair(peer_addr(smem_u32(&bar), 1u));   // the odd CTA
@@ -164,7 +177,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
     if (same) {
         ok = wait_warp(&bar, 0, nullptr, kWaitNs);
         tc_fence_after_sync();
-        if (ok) {
+        if (rank == 0 && warp == 0 && lane == 0 && reps > 0) *cycles = clock64() - t0;
+        if (ok && reps == 0) {
             const int row = warp * 32 + lane;
             for (int c = 0; c < N; c += 32) {
                 uint32_t r[32];
@@ -189,8 +203,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
 int main() {
     float* d_out = nullptr;
     int* d_status = nullptr;
+    long long* d_cycles = nullptr;
     if (cudaMalloc(&d_out, 256 * N * sizeof(float)) != cudaSuccess ||
-        cudaMalloc(&d_status, sizeof(int)) != cudaSuccess)
+        cudaMalloc(&d_status, sizeof(int)) != cudaSuccess ||
+        cudaMalloc(&d_cycles, sizeof(long long)) != cudaSuccess)
         return 1;
     if (cudaFuncSetAttribute(pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
         cudaSuccess)
@@ -207,7 +223,7 @@ int main() {
     for (int ts = 0; ts < 2; ++ts) {
         cudaMemset(d_out, 0xff, 256 * N * sizeof(float));
         cudaMemset(d_status, 0, sizeof(int));
-        pair_kernel<<<2, 128, kSmem>>>(ts, d_out, d_status);
+        pair_kernel<<<2, 128, kSmem>>>(ts, 0, d_out, d_status, d_cycles);
         const cudaError_t e = cudaDeviceSynchronize();
         std::vector<float> h(256 * N);
         int status = -1;
@@ -221,8 +237,22 @@ int main() {
                     ts ? "ts" : "ss", cudaGetErrorString(e), status, bad);
         if (e != cudaSuccess) break;
     }
+    const int reps = 256;
+    for (int ts = 0; ts < 2 && all_ok; ++ts) {
+        cudaMemset(d_status, 0, sizeof(int));
+        pair_kernel<<<2, 128, kSmem>>>(ts, reps, d_out, d_status, d_cycles);
+        long long cyc = -1;
+        int status = -1;
+        const cudaError_t e = cudaDeviceSynchronize();
+        cudaMemcpy(&cyc, d_cycles, sizeof(cyc), cudaMemcpyDeviceToHost);
+        cudaMemcpy(&status, d_status, sizeof(int), cudaMemcpyDeviceToHost);
+        all_ok &= e == cudaSuccess && status == 0;
+        std::printf(", \"%s_pair_M256_N128_cycles_per_step\": %.1f", ts ? "ts" : "ss",
+                    (double)cyc / (reps * 8.0));
+    }
     std::printf(", \"ok\": %s}\n", all_ok ? "true" : "false");
     cudaFree(d_out);
     cudaFree(d_status);
+    cudaFree(d_cycles);
     return all_ok ? 0 : 2;
 }

@@ -23,7 +23,8 @@ import os
 import threading
 
 __all__ = ["FaError", "load_library", "library_path", "fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_ex",
-           "fa_bwd_workspace_bytes", "fa_bwd_workspace_bytes_ex", "fa_get_device_status",
+           "fa_bwd_workspace_bytes", "fa_bwd_workspace_bytes_ex", "fa_set_forward_pair",
+           "fa_get_device_status",
            "fa_set_wait_timeout_ns",
            "fa_selftest_wait_timeout", "fa_trace_next_call", "fa_launch_count", "fa_status_string",
            "fa_bwd_noalloc", "forward", "backward", "attention", "attention_blhd",
@@ -42,7 +43,7 @@ _lib = None
 _lock = threading.Lock()
 
 EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_ex", "fa_bwd_workspace_bytes",
-            "fa_bwd_workspace_bytes_ex", "fa_get_device_status",
+            "fa_bwd_workspace_bytes_ex", "fa_set_forward_pair", "fa_get_device_status",
             "fa_set_wait_timeout_ns", "fa_selftest_wait_timeout", "fa_trace_next_call",
             "fa_launch_count", "fa_status_string", "fa_bwd_noalloc", "fa_decode_paged",
             "fa_decode_workspace_bytes")
@@ -98,6 +99,8 @@ def load_library():
         lib.fa_bwd_noalloc.restype = i
         lib.fa_get_device_status.argtypes = [vp]
         lib.fa_get_device_status.restype = i
+        lib.fa_set_forward_pair.argtypes = [i]
+        lib.fa_set_forward_pair.restype = i
         lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
         lib.fa_set_wait_timeout_ns.restype = i
         lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
@@ -191,6 +194,10 @@ def fa_trace_next_call(events, n_pairs: int) -> int:
     """``events``: sequence of 2*n_pairs raw cudaEvent_t handles (ints)."""
     arr = (ctypes.c_void_p * max(1, len(events)))(*[ctypes.c_void_p(int(e)) for e in events])
     return load_library().fa_trace_next_call(arr, n_pairs)
+
+
+def fa_set_forward_pair(mode: int) -> int:
+    return int(load_library().fa_set_forward_pair(int(mode)))
 
 
 def fa_launch_count() -> int:

@@ -19,6 +19,7 @@ namespace {
 __device__ int g_status_word;  // first device-side error since the last fa_get_device_status
 
 std::atomic<uint64_t> g_timeout_ns{4000000000ull};
+std::atomic<int> g_fwd_pair{0};  // fa_set_forward_pair
 constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;
 
 std::mutex g_mu;
@@ -67,12 +68,12 @@ bool bind_context() {
 // descriptors expect.  Rows past L read as zeros.  The strides are positive multiples of 8
 // elements (16 bytes), checked by the caller.
 bool make_map(CUtensorMap* m, const void* ptr, int B, int H, int L, int D, const Strides& st,
-              bool bf16) {
+              bool bf16, int box_rows = kTileRows) {
     auto enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)H, (cuuint64_t)B};
     cuuint64_t strides[3] = {(cuuint64_t)st.l * 2, (cuuint64_t)st.h * 2, (cuuint64_t)st.b * 2};
-    cuuint32_t box[4] = {(cuuint32_t)kChunkElems, (cuuint32_t)kTileRows, 1, 1};
+    cuuint32_t box[4] = {(cuuint32_t)kChunkElems, (cuuint32_t)box_rows, 1, 1};
     cuuint32_t elem[4] = {1, 1, 1, 1};
     CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                      4, const_cast<void*>(ptr), dims, strides, box, elem,
@@ -290,6 +291,12 @@ const char* fa_status_string(int status) {
     }
 }
 
+fa_status fa_set_forward_pair(int mode) {
+    if (mode != 0 && mode != 1) return FA_ERR_INVALID_ARG;
+    g_fwd_pair.store(mode);
+    return FA_OK;
+}
+
 fa_status fa_set_wait_timeout_ns(uint64_t timeout_ns) {
     g_timeout_ns.store(timeout_ns ? timeout_ns : kDefaultTimeoutNs);
     return FA_OK;
@@ -364,7 +371,13 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
     if (!p.status) return FA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool dr = dropout_p > 0.0;
-    cudaError_t e = traced_launch(0, s, [&] { return launch_fwd(p, D, bf16, causal != 0, dr, s); });
+    // The CTA-pair forward: D = 128 without dropout, when selected (fa_set_forward_pair).
+    const bool pair = D == 128 && !dr && g_fwd_pair.load() == 1;
+    if (pair && !make_map(&p.tm_k_half, k, B, H, Lk, D, sk, bf16, 64)) return FA_ERR_CUDA;
+    cudaError_t e = traced_launch(0, s, [&] {
+        return pair ? launch_fwd_pair(p, bf16, causal != 0, s)
+                    : launch_fwd(p, D, bf16, causal != 0, dr, s);
+    });
     if (e != cudaSuccess) return FA_ERR_CUDA;
     // Under the causal mask the first Lq - Lk query rows see no key when Lq > Lk.
     const int empty_rows = (causal && Lq > Lk) ? Lq - Lk : 0;

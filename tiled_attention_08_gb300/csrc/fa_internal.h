@@ -58,6 +58,7 @@ struct Dropout {
 
 struct FwdParams {
     CUtensorMap tm_q, tm_k, tm_v;  // 16-bit {D, L, H, B} (strided), box {64, 128, 1, 1}
+    CUtensorMap tm_k_half;         // K with box {64, 64, 1, 1} (CTA-pair forward only)
     void* o;                       // [B, H, Lq, D] 16-bit, strides so
     Strides so;
     float* lse;                    // [B*H, Lq] natural-log LSE (contiguous)
@@ -152,6 +153,8 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 // Launchers (one per kernel unit).  Return the launch error, if any.
 cudaError_t launch_fwd(const FwdParams& p, int D, bool bf16, bool causal, bool drop,
                        cudaStream_t s);
+// The forward at D = 128 on CTA pairs (fa_fwd_pair.cu); needs p.tm_k_half.
+cudaError_t launch_fwd_pair(const FwdParams& p, bool bf16, bool causal, cudaStream_t s);
 cudaError_t launch_fwd_empty_rows(const FwdParams& p, int D, int rows, cudaStream_t s);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdParams& p, int D, bool bf16, bool causal, bool drop,
