@@ -315,6 +315,8 @@ def run_ours(args, w):
         fa_build.build()
     barrier(dev)
     fa.load_library()
+    if args.forward_pair and fa.fa_set_forward_pair(1) != fa.FA_OK:
+        raise SystemExit("fa_set_forward_pair(1) failed")
 
     inp = workloads.make_inputs(w, seed=rank)
     q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
@@ -432,6 +434,8 @@ def run_ours(args, w):
                        parallelism=("replicas: one independent copy per GPU"
                                     if world > 1 else "single GPU"),
                        step="fa_fwd + fa_bwd (4 kernels)",
+                       forward=("CTA pairs (fa_set_forward_pair(1))" if args.forward_pair
+                                else "single CTAs"),
                        l2=f"inputs larger than L2 ({q.numel() * 2 / 2**20:.0f} MiB per tensor); "
                           "no flush"),
         "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2),
@@ -815,6 +819,8 @@ def main(argv=None):
                     help="skip the host-buffer end-to-end pass (profiling runs)")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-config measurements of the other workloads")
+    ap.add_argument("--forward-pair", action="store_true",
+                    help="run the forward on CTA pairs (D = 128; fa_set_forward_pair(1))")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
