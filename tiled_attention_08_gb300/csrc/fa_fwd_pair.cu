@@ -30,7 +30,10 @@
 // with remote arrives (one per warp).  MMA order and the reasoning that makes the in-place O rescale safe are
 // those of fa_fwd.cu (S_t(j+1) is issued after PV_t(j)).
 //
-// No persistent form and no dropout variant: fa_fwd_ex picks this kernel only where it pays.
+// No persistent form and no dropout variant.  fa_fwd_ex runs it only after
+// fa_set_forward_pair(1): on this GPU a pair TS step (the PV contraction) runs at 78% of the
+// single-CTA rate and the pair couples the two CTAs' softmax every step, so the single-CTA
+// forward is faster and stays the default.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 #include "fa_sched.h"
