@@ -106,9 +106,9 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
 
 /*
  * Bytes of device workspace fa_bwd needs for this shape: two fp32 vectors per head padded to
- * a whole number of 128-row tiles (-LSE * log2(e) and Delta = rowsum(dO * O)).
- * Returns 0 for an empty problem or invalid sizes.
- * The pages have no such call: they keep "the max and the sum of exponentials" for the
+ * a whole number of 128-row tiles (-LSE * log2(e) and Delta = rowsum(dO * O)), then 16 bytes
+ * of work counters for the persistent passes.  Returns 0 for an empty problem or invalid sizes.
+ * The pages have no such call: they keep the row maximum and the sum of exponentials for the
  * backward (data-flow page, section 2.2, third layer) without saying where the per-row
  * vectors the backward derives from them live.  Here the caller owns that memory, so the
  * library reports how much it needs.
@@ -119,7 +119,8 @@ size_t fa_bwd_workspace_bytes(int B, int H, int L, int D);
  * Bytes of device workspace fa_bwd_ex needs for q of [B, H, Lq, D] and the given
  * `deterministic` flag (0 or 1; else 0 is returned): with deterministic = 0 at D = 64 the
  * backward reduces dQ into an fp32 accumulator [B*H, Lqpad, D] kept in the workspace after the
- * two per-row vectors (Lqpad = Lq rounded up to a multiple of 128).  A workspace of this size
+ * two per-row vectors (Lqpad = Lq rounded up to a multiple of 128; the work counters follow
+ * it).  A workspace of this size
  * also serves the same shape with dropout (which always takes the deterministic path).
  * fa_bwd_workspace_bytes(B, H, L, D) = fa_bwd_workspace_bytes_ex(B, H, L, D, 1).
  * Pages: silent (as for fa_bwd_workspace_bytes).
@@ -131,9 +132,10 @@ size_t fa_bwd_workspace_bytes_ex(int B, int H, int Lq, int D, int deterministic)
  * dq, dk, dv [B,H,L,D] (dtype).  `workspace` is a device buffer of at least
  * fa_bwd_workspace_bytes(B,H,L,D) bytes, 16-byte aligned, owned by the caller; its contents
  * on entry do not matter.  Three kernels are enqueued on `stream`: the Delta/LSE preprocess,
- * the dK/dV pass (one CTA per key tile, or, when key tiles are seen by at most 12 query tiles
- * on average, one persistent CTA per SM taking key tiles in turn) and the dQ pass (likewise
- * per query tile, persistent when query tiles see at most 32 key tiles on average); the
+ * the dK/dV pass (one CTA per key tile, or, when key tiles are seen by at most 32 query tiles
+ * on average, one persistent CTA per SM) and the dQ pass (likewise per query tile, persistent
+ * when query tiles see at most 32 key tiles on average); persistent CTAs take the next tile of
+ * a heaviest-first order from a counter in the workspace whenever they are ready for one.  The
  * results are the same either way.
  * Data-flow page, section 2.2, third layer (recompute P from the saved statistics).
  */
@@ -170,8 +172,9 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
                     int Lk, int D, float scale, int causal, double dropout_p, uint64_t seed,
                     int deterministic, int dtype, void* stream);
 
-/* Size of the fixed device scratch array behind fa_bwd_noalloc: 16 MiB. */
-#define FA_BWD_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+/* Size of the fixed device scratch array behind fa_bwd_noalloc: 16 MiB for the per-row
+ * vectors and 256 bytes for the work counters. */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (((size_t)16 << 20) + 256)
 
 /*
  * Backward for callers that cannot allocate device memory.  The pages describe no such entry
@@ -183,8 +186,8 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
  * Same arguments, results and checks as fa_bwd, minus the workspace: the scratch fa_bwd would
  * take from `workspace` comes from a file-scope device array of FA_BWD_NOALLOC_SCRATCH_BYTES
  * compiled into the library, which every GPU that loads the library's code holds until the
- * process exits.  The limit: fa_bwd_workspace_bytes(B,H,L,D) = 8*B*H*ceil(L/128)*128 bytes
- * must not exceed FA_BWD_NOALLOC_SCRATCH_BYTES (B*H*ceil(L/128)*128 <= 2^21 rows, e.g.
+ * process exits.  The limit: fa_bwd_workspace_bytes(B,H,L,D) = 8*B*H*ceil(L/128)*128 + 16
+ * bytes must not exceed FA_BWD_NOALLOC_SCRATCH_BYTES (B*H*ceil(L/128)*128 <= 2^21 rows, e.g.
  * B*H = 256 heads at L = 8192); larger problems return FA_ERR_UNSUPPORTED before anything is
  * enqueued.  The call allocates nothing (no cudaMalloc, cudaFree or allocating library call).
  *

@@ -149,16 +149,16 @@ int main() {
             ++failures;
         }
     }
-    // The dK/dV pass: persistent only up to a mean of 12 query tiles per key tile.
-    const int kcases[][6] = {{4096, 4096, 256, 1, 152, 8192},   // B8 H32 L4096 causal: mean 16.5
+    // The dK/dV pass: persistent only up to a mean of 32 query tiles per key tile.
+    const int kcases[][6] = {{4096, 4096, 256, 1, 152, 152},    // B8 H32 L4096 causal: mean 16.5
                              {2048, 2048, 32, 1, 152, 152},     // B1 H32 L2048 causal: mean 8.5
                              {16384, 16384, 16, 1, 152, 2048},  // B1 H16 L16384 causal: mean 64.5
                              {512, 512, 512, 0, 152, 152},      // B16 H32 L512: mean 4
                              {1024, 1024, 512, 0, 152, 152},    // B16 H32 L1024: mean 8
-                             {1536, 1536, 64, 0, 152, 152},     // non-causal, mean 12 (limit)
-                             {1664, 1664, 64, 0, 152, 832},     // non-causal, mean 13
-                             {2944, 2944, 64, 1, 152, 152},     // causal, mean 12
-                             {3072, 3072, 64, 1, 152, 1536},    // causal, mean 12.5
+                             {4096, 4096, 64, 0, 152, 152},     // non-causal, mean 32 (limit)
+                             {4224, 4224, 64, 0, 152, 2112},    // non-causal, mean 33
+                             {8064, 8064, 64, 1, 152, 152},     // causal, mean 32
+                             {8192, 8192, 64, 1, 152, 4096},    // causal, mean 32.5
                              {128, 128, 1, 0, 152, 1},          // fewer tiles than SMs
                              {512, 512, 512, 0, 0, 2048}};      // SM count unknown
     for (const auto& c : kcases) {

@@ -82,9 +82,9 @@ def test_forward_argument_checks(lib, kw, status):
 
 
 def test_workspace_size(lib):
-    # two fp32 vectors per head, padded to whole 128-row tiles
-    assert fa.fa_bwd_workspace_bytes(2, 3, 200, 64) == 2 * 6 * 256 * 4
-    assert fa.fa_bwd_workspace_bytes(1, 1, 128, 128) == 2 * 128 * 4
+    # two fp32 vectors per head, padded to whole 128-row tiles, and 16 bytes of work counters
+    assert fa.fa_bwd_workspace_bytes(2, 3, 200, 64) == 2 * 6 * 256 * 4 + 16
+    assert fa.fa_bwd_workspace_bytes(1, 1, 128, 128) == 2 * 128 * 4 + 16
     assert fa.fa_bwd_workspace_bytes(1, 1, 0, 128) == 0
     assert fa.fa_bwd_workspace_bytes(1, 1, 128, 96) == 0
     assert fa.fa_bwd_workspace_bytes(-1, 1, 128, 64) == 0
@@ -221,11 +221,13 @@ def test_product_package_does_not_touch_the_oracle():
 def test_backward_workspace_sizes(lib):
     B, H, L = 2, 3, 300
     Lp = 384
+    counters = 16  # work counters of the persistent passes, at the end
     for D in (64, 128):
-        assert fa.fa_bwd_workspace_bytes(B, H, L, D) == 2 * B * H * Lp * 4
-        assert fa.fa_bwd_workspace_bytes_ex(B, H, L, D, 1) == 2 * B * H * Lp * 4
-    # dQ by reduction (D = 64 only): the fp32 accumulator [B*H, Lqpad, D] follows
-    assert fa.fa_bwd_workspace_bytes_ex(B, H, L, 64, 0) == 2 * B * H * Lp * 4 + B * H * Lp * 64 * 4
-    assert fa.fa_bwd_workspace_bytes_ex(B, H, L, 128, 0) == 2 * B * H * Lp * 4
+        assert fa.fa_bwd_workspace_bytes(B, H, L, D) == 2 * B * H * Lp * 4 + counters
+        assert fa.fa_bwd_workspace_bytes_ex(B, H, L, D, 1) == 2 * B * H * Lp * 4 + counters
+    # dQ by reduction (D = 64 only): the fp32 accumulator [B*H, Lqpad, D] follows the vectors
+    assert (fa.fa_bwd_workspace_bytes_ex(B, H, L, 64, 0) ==
+            2 * B * H * Lp * 4 + B * H * Lp * 64 * 4 + counters)
+    assert fa.fa_bwd_workspace_bytes_ex(B, H, L, 128, 0) == 2 * B * H * Lp * 4 + counters
     assert fa.fa_bwd_workspace_bytes_ex(B, H, L, 64, 2) == 0
     assert fa.fa_bwd_workspace_bytes_ex(B, H, 0, 64, 0) == 0

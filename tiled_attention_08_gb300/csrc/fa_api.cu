@@ -217,10 +217,13 @@ bool dq_reduce_path(int D, int deterministic, double dropout_p) {
 }
 
 // Backward workspace: -LSE*log2(e) and Delta ([BH, Lqpad] fp32 each), then for dQ by reduction
-// the fp32 accumulator [BH, Lqpad, D].
-size_t bwd_workspace_need(const Shape& sh, int D, bool dq_reduce) {
+// the fp32 accumulator [BH, Lqpad, D], then the persistent passes' work counters.
+size_t bwd_sched_offset(const Shape& sh, int D, bool dq_reduce) {
     const size_t rows = (size_t)sh.BH * (size_t)sh.Lqpad;
     return 2u * rows * 4u + (dq_reduce ? rows * (size_t)D * 4u : 0u);
+}
+size_t bwd_workspace_need(const Shape& sh, int D, bool dq_reduce) {
+    return bwd_sched_offset(sh, D, dq_reduce) + kSchedBytes;
 }
 
 }  // namespace
@@ -249,7 +252,7 @@ int bwd_check_args(const void* q, const void* k, const void* v, const void* o, c
     if (st != FA_OK) return st;
     if (sh.empty) return FA_OK;
     if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-    *ws_need = 2u * (size_t)sh.BH * (size_t)sh.Lqpad * 4u;
+    *ws_need = bwd_workspace_need(sh, D, false);
     return FA_OK;
 }
 
@@ -486,6 +489,8 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     p.scale_log2 = scale * 1.4426950408889634f;
     p.drop = drop;
     p.dq_acc = dqr ? delta_pad + (size_t)sh.BH * sh.Lqpad : nullptr;
+    p.sched = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) +
+                                     bwd_sched_offset(sh, D, dqr));
     p.status = status_ptr();
     p.timeout_ns = g_timeout_ns.load();
     if (!p.status) return FA_ERR_CUDA;
@@ -502,6 +507,7 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     pp.nlse2_pad = nlse2_pad;
     pp.delta_pad = delta_pad;
     pp.dq_acc = p.dq_acc;
+    pp.sched = p.sched;
     pp.Lq = Lq;
     pp.Lqpad = sh.Lqpad;
     pp.H = H;

@@ -28,8 +28,9 @@
 //
 // Scheduling (dkdv_grid).  A work item is one key tile of one head, ordered heaviest first
 // (key tile 0 sees every query tile under the causal mask) inside L2-sized head groups
-// (tile_coords).  For rows of few query tiles the grid is one CTA per SM, each taking items in
-// the snake rounds of persistent_tile, so a CTA's fixed cost is paid once per SM: the Q / dO
+// (tile_coords).  For rows of few query tiles the grid is one CTA per SM, each taking the next
+// item from the pass's work counter whenever it is ready for one (fa_queue.cuh), so a CTA's
+// fixed cost is paid once per SM and the items stay balanced: the Q / dO
 // rings run on from one item to the next, the next item's K_j / V_j are loaded as soon as the
 // current item's last S^T and dP^T have completed (at D = 64 into a second K/V slot, at once),
 // and the next item's first S^T and dP^T run while the elementwise warps read out dK and dV.
@@ -40,6 +41,7 @@
 // CTA's lifetime.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
+#include "fa_queue.cuh"
 #include "fa_sched.h"
 
 namespace fa {
@@ -103,6 +105,7 @@ template <int KVS, int QS, int OS>
 struct DkdvBars {
     uint64_t kvf[KVS], kve[KVS], qf[QS], qe[QS], of[OS], oe[OS], sf, df, sr, ppd, done, fin;
     uint64_t dqf[2], dqe[2];
+    WorkQueue queue;  // persistent kernel: the items, fetched from the pass's counter
     uint32_t tmem_base;
     int abort;
 };
@@ -123,16 +126,15 @@ struct DkdvItem {
     int bh, b, h, kt, it0, n_it;
 };
 
+// Work id -> item: ids follow tile_coords (heads in L2-sized groups, key tile 0, the heaviest,
+// first).  The persistent kernel takes its ids from the pass's counter (fa_queue.cuh).
 template <bool CAUSAL>
-__device__ __forceinline__ bool dkdv_item(const BwdParams& p, int round, DkdvItem& it) {
-    const int id = persistent_tile(round, (int)blockIdx.x, (int)gridDim.x, p.n_ktiles * p.BH);
-    if (id < 0) return false;
+__device__ __forceinline__ void dkdv_item(const BwdParams& p, int id, DkdvItem& it) {
     tile_coords(id, p.BH, p.n_ktiles, p.group, it.bh, it.kt);  // key tile 0 (heaviest) first
     it.b = it.bh / p.H;
     it.h = it.bh - it.b * p.H;
     it.it0 = k_tile_q0(it.kt, p.Lq, p.Lk, CAUSAL);
     it.n_it = p.n_qtiles - it.it0;
-    return true;
 }
 
 // One CTA per (b*h, key tile), in tile_coords order (the hardware's block scheduler balances
@@ -689,6 +691,7 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
         mbar_init(&bar_ppd, C::kEwThreads);  // P^T and dS^T written into the dP^T columns
         mbar_init(&bar_done, 1);             // every MMA of an item complete: dK, dV final
         mbar_init(&bar_fin, 1);
+        queue_init(bars.queue, 1 + C::kEwWarps);  // read by the MMA and elementwise warps
         mbar_fence_init();
     }
     if (warp == C::kMmaWarp) tmem_alloc(&tmem_base_sh, C::kTmemCols);
@@ -746,7 +749,16 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
             };
             int u = 0;
             DkdvItem it;
-            for (int round = 0; ok && dkdv_item<CAUSAL>(p, round, it); ++round) {
+            // Item ids are fetched one round ahead of the loads (fa_queue.cuh).
+            int next_id = queue_push(bars.queue, 0, p.sched, p.n_ktiles * p.BH, false, abort_v,
+                                     p.timeout_ns);
+            for (int round = 0; ok; ++round) {
+                const int id = next_id;
+                if (id == -2) ok = false;
+                if (id < 0) break;
+                next_id = queue_push(bars.queue, round + 1, p.sched, p.n_ktiles * p.BH, false,
+                                     abort_v, p.timeout_ns);
+                dkdv_item<CAUSAL>(p, id, it);
                 // K_j and V_j into K/V slot round % kKVSlots, once the item that used it last has
                 // completed its S^T and dP^T contractions.
                 const int kvs = round % C::kKVSlots;
@@ -809,7 +821,11 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
         bool ok = true;
         int u = 0;
         DkdvItem it;
-        for (int round = 0; ok && dkdv_item<CAUSAL>(p, round, it); ++round) {
+        for (int round = 0; ok; ++round) {
+            const int id = queue_pop_warp(bars.queue, round, abort_v, p.timeout_ns);
+            if (id == -2) ok = false;
+            if (id < 0) break;
+            dkdv_item<CAUSAL>(p, id, it);
             const int kvs = round % C::kKVSlots;
             const int n = it.n_it;
             const uint64_t kdesc = sdesc_kmajor_sw128(smem_u32(k_tile(kvs)));
@@ -914,7 +930,13 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
         int u = 0;                 // query tiles of earlier items
         uint32_t done_par = 0u;    // phase of the item's done barrier
         DkdvItem it;
-        for (int round = 0; ok && dkdv_item<CAUSAL>(p, round, it); ++round) {
+        for (int round = 0; ok; ++round) {
+            // The quadrant's warps agree on the outcome before any of them goes on: they meet
+            // at named barriers below.
+            const int id = queue_pop_warp(bars.queue, round, abort_v, p.timeout_ns);
+            ok = bar_and(grp_bar, kGrpThreads, id != -2);
+            if (!ok || id < 0) break;
+            dkdv_item<CAUSAL>(p, id, it);
             const int key = it.kt * kTileRows + row;
             const int u_end = u + it.n_it;
             const int qi_off = it.it0 - u;  // query tile of ring index uu: uu + qi_off

@@ -29,21 +29,22 @@
 //
 // Two schedules (dq_grid).  For rows of few key tiles (a mean of at most kPersistMaxKv per
 // query tile) fa_bwd_dq_kernel_persistent runs one CTA per SM (a CTA fills an SM: all 512 TMEM
-// columns and over 200 KB of shared memory), each taking its query tiles in the rounds of
-// persistent_tile.  The fixed cost of a CTA (launch, barrier and TMEM set-up, the first copies'
+// columns and over 200 KB of shared memory), each taking the next query tile of a
+// heaviest-first order from the pass's work counter whenever it is ready for one
+// (fa_queue.cuh).  The fixed cost of a CTA (launch, barrier and TMEM set-up, the first copies'
 // latency, the pipeline fill and the dQ read-out) is then paid once per SM instead of once per
 // tile, and most of it overlaps the neighbouring tiles: the K_j / V_j ring runs on across
 // tiles, Q of the next tile is loaded as soon as the S contractions of this one have
 // completed, the elementwise warps stage the next dO right after reading this tile's last dP,
 // and the next tile's first S and dP run while they read out dQ.  Its barrier phases count
 // key-tile iterations (or tiles) over the CTA's lifetime.  For longer rows the fixed cost
-// matters less than the balance of the hardware's own block scheduling over heaviest-first
-// tiles, and fa_bwd_dq_kernel runs one CTA per query tile.  Measured: B8 H32 L4096 D128
-// causal (16.5 key tiles per query tile on average) 1.205 ms one CTA per tile, 1.109
-// persistent; B1 H16 L16384 D64 causal (64.5) 0.688 one CTA per tile, 0.715 persistent (0.722
-// with the persistent kernel launched one CTA per tile).
+// matters less than the per-tile speed of fa_bwd_dq_kernel, which runs one CTA per query tile.
+// Measured: B8 H32 L4096 D128 causal (16.5 key tiles per query tile on average) 1.205 ms one
+// CTA per tile, 1.109 persistent in fixed rounds, 1.047 persistent with the work counter;
+// B1 H16 L16384 D64 causal (64.5) 0.688 one CTA per tile, 0.729 persistent with the counter.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
+#include "fa_queue.cuh"
 #include "fa_sched.h"
 
 namespace fa {
@@ -413,29 +414,27 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
     __shared__ uint64_t bar_done; // every MMA of the tile complete: dQ_i final
     __shared__ uint64_t bar_dqr;  // dQ_i read out: the accumulator may be overwritten
     __shared__ uint64_t bar_fin;
+    __shared__ WorkQueue queue;  // this CTA's query tiles, fetched from the pass's counter
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     volatile int* abort_v = &abort_flag;
-    // Persistent CTAs: this CTA's query tiles in round order (persistent_tile); inside each
-    // round the ids follow tile_coords (heads in L2-sized groups, heaviest tiles first).
-    // (The launcher uses this kernel only when every query tile sees at least one key.)
+    // Work ids 0 .. total-1 follow tile_coords (heads in L2-sized groups, heaviest query tiles
+    // first); every CTA takes the next id when it is ready for one (fa_queue.cuh).  (The
+    // launcher uses this kernel only when every query tile sees at least one key.)
     const int total = p.n_qtiles * p.BH;
     struct Tile {
         int bh, b, h, qt, n_kv;
     };
-    auto tile_of = [&](int round, Tile& t) -> bool {
-        const int id = persistent_tile(round, (int)blockIdx.x, (int)gridDim.x, total);
-        if (id < 0) return false;
+    auto tile_from = [&](int id, Tile& t) {
         int rank;
         tile_coords(id, p.BH, p.n_qtiles, p.group, t.bh, rank);
         t.b = t.bh / p.H;
         t.h = t.bh - t.b * p.H;
         t.qt = p.n_qtiles - 1 - rank;
         t.n_kv = q_tile_kv(t.qt, p.Lq, p.Lk, CAUSAL);
-        return true;
     };
 
     if (threadIdx.x == 0) {
@@ -456,6 +455,7 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
         mbar_init(&bar_done, 1);
         mbar_init(&bar_dqr, C::kEwThreads);
         mbar_init(&bar_fin, 1);
+        queue_init(queue, 1 + C::kEwWarps);  // read by the MMA warp and the elementwise warps
         mbar_fence_init();
     }
     if (warp == C::kMmaWarp) tmem_alloc(&tmem_base_sh, C::kTmemCols);
@@ -466,9 +466,10 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
 
     if (warp == C::kProducerWarp) {
         // ------------------------------ TMA producer ------------------------------
-        // Per tile: Q_i (once the previous tile's S contractions have completed), then its
-        // K_j / V_j into the ring, which runs on across tiles, so the next tile's first key
-        // tiles are already in flight while this one finishes.
+        // Fetches the tile ids (one round ahead).  Per tile: Q_i (once the previous tile's S
+        // contractions have completed), then its K_j / V_j into the ring, which runs on across
+        // tiles, so the next tile's first key tiles are already in flight while this one
+        // finishes.
         if (lane == 0) {
             tma_prefetch_desc(&p.tm_k);
             tma_prefetch_desc(&p.tm_v);
@@ -477,7 +478,14 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
             int gk = 0;       // K/V fills handed to the TMA unit
             int q_loads = 0;  // Q fills handed to the TMA unit
             Tile t;
-            for (int round = 0; ok && tile_of(round, t); ++round) {
+            int next_id = queue_push(queue, 0, p.sched + 1, total, false, abort_v, p.timeout_ns);
+            for (int round = 0; ok; ++round) {
+                const int id = next_id;
+                if (id == -2) ok = false;
+                if (id < 0) break;
+                next_id = queue_push(queue, round + 1, p.sched + 1, total, false, abort_v,
+                                     p.timeout_ns);
+                tile_from(id, t);
                 if (q_loads > 0 &&
                     !wait_bounded(&bar_qe, (uint32_t)(q_loads - 1) & 1u, abort_v, p.timeout_ns)) {
                     ok = false;
@@ -557,7 +565,11 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
         int g = 0;
         int tc = 0;
         Tile t;
-        for (int round = 0; ok && tile_of(round, t); ++round, ++tc) {
+        for (int round = 0; ok; ++round, ++tc) {
+            const int id = queue_pop_warp(queue, round, abort_v, p.timeout_ns);
+            if (id == -2) ok = false;
+            if (id < 0) break;
+            tile_from(id, t);
             const int n = t.n_kv;
             // Q_i landed and dO_i staged; the previous tile's last S and dP have been read (their
             // columns are reused); K_0 / V_0 of this tile landed.
@@ -649,11 +661,22 @@ __global__ void __launch_bounds__(DqCfg<D, BF16, CAUSAL>::kThreads, 1)
         };
         Tile cur, nxt;
         float nlse2 = 0.0f, dlt = 0.0f;  // -LSE * log2(e) and Delta of this thread's row
-        bool ok = tile_of(0, cur);       // every CTA has at least one tile
-        if (ok) stage_do(cur, nlse2, dlt);
+        const int id0 = queue_pop_warp(queue, 0, abort_v, p.timeout_ns);
+        bool ok = id0 != -2;
+        const bool any = id0 >= 0;  // a CTA that starts late may find no tile left
+        if (any) {
+            tile_from(id0, cur);
+            stage_do(cur, nlse2, dlt);
+        }
         int g = 0;
-        for (int round = 0, tc = 0; ok; ++round, ++tc) {
-            const bool has_next = tile_of(round + 1, nxt);
+        for (int round = 0, tc = 0; ok && any; ++round, ++tc) {
+            const int idn = queue_pop_warp(queue, round + 1, abort_v, p.timeout_ns);
+            if (idn == -2) {
+                ok = false;
+                break;
+            }
+            const bool has_next = idn >= 0;
+            if (has_next) tile_from(idn, nxt);
             const int n = cur.n_kv;
             const int q_row = cur.qt * kTileRows + row;
             const int klim = CAUSAL ? min(p.Lk - 1, q_row + (p.Lk - p.Lq)) : (p.Lk - 1);

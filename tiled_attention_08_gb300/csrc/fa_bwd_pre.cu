@@ -9,7 +9,7 @@
 // see no key (the first Lq - Lk queries under the causal mask when Lq > Lk) get dQ = 0 here;
 // the dQ pass skips query tiles in which no row sees a key.  When dQ is reduced into an fp32
 // accumulator by the dK/dV pass instead, this kernel zeroes the accumulator's rows (all Lqpad
-// of them) as it goes.
+// of them) as it goes, and it zeroes the work counters of the persistent passes that follow.
 //
 // HBM-bound: every (row, D) element of O and dO is read once, with 16-byte loads; D/8 threads
 // share a row and reduce with shuffles.
@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdPreParams p) {
     constexpr int kRowsPerPass = 256 / G;
     const int g = threadIdx.x % G;
     const int i0 = blockIdx.x * kTileRows + threadIdx.x / G;
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < kSchedCounters) p.sched[threadIdx.x] = 0;
     for (int bh = blockIdx.y; bh < p.BH; bh += gridDim.y) {
         const uint8_t* o_head =
             reinterpret_cast<const uint8_t*>(p.o) + row_offset(p.so, bh, p.H, 0) + g * 16;

@@ -81,10 +81,15 @@ struct BwdPreParams {
     float* nlse2_pad;    // [BH, Lqpad]: -LSE * log2(e), zero past Lq
     float* delta_pad;    // [BH, Lqpad]: rowsum(dO * O), zero past Lq
     float* dq_acc;       // [BH, Lqpad, D] fp32, zeroed here (dQ by reduction), or null
+    int* sched;          // work counters of the persistent passes, zeroed here
     int Lq, Lqpad, H, BH, D;
     int first_seen_row;  // rows below this see no key (causal with Lq > Lk), else 0
     int bf16;
 };
+
+// Work counters of the persistent backward passes at the end of the backward workspace.
+constexpr int kSchedCounters = 4;
+constexpr size_t kSchedBytes = kSchedCounters * sizeof(int);
 
 // Decode over a paged key/value cache: tokens per page.
 constexpr int kPageTokens = 16;
@@ -121,6 +126,7 @@ struct BwdParams {
     float scale_log2;   // scale * log2(e)
     Dropout drop;
     float* dq_acc;      // [BH, Lqpad, D] fp32: dQ by reduction in the dK/dV pass, or null
+    int* sched;         // [kSchedCounters] work counters: [0] dK/dV pass, [1] dQ pass
     int* status;
     uint64_t timeout_ns;
 };

@@ -47,7 +47,9 @@ __host__ __device__ __forceinline__ int persistent_tile(int round, int cta, int 
 // all (summed over the items of one head).  Persistent (one CTA per SM) when the items see at
 // most `max_mean` tiles on average and there are more items than SMs; otherwise one CTA per
 // item.  The fixed cost of a CTA is worth hiding only for short rows; for long rows the
-// hardware's own block scheduling balances the causal items better than fixed rounds.
+// one-CTA-per-item kernels run each tile a little faster than the persistent ones, and that
+// outweighs it.  (The forward's persistent CTAs take fixed rounds, persistent_tile; the
+// backward's take the next item from a counter, fa_queue.cuh.)
 constexpr int kPersistMaxKv = 32;
 __host__ __device__ __forceinline__ int persistent_grid(int items_per_head, long long row_tiles,
                                                         int BH, int max_mean, int n_sm) {
@@ -65,12 +67,13 @@ __host__ __device__ __forceinline__ int dq_grid(int Lq, int Lk, int BH, bool cau
 }
 
 // Grid of the dK/dV pass: one item per key tile.  Its persistent kernel carries per-item state
-// across the query-tile loop in elementwise warps already at the 96-register limit of an
-// 18-warp CTA, so it costs a few percent per query tile against the one-CTA-per-item kernel;
-// it is used only for rows of at most kDkdvPersistMaxKv query tiles on average, where the saved
-// fixed cost is larger (measured: B1 H32 L2048 causal, mean 8.5, +2.3%; B16 H32 L512 and
-// L1024, +3 to +13%; B8 H32 L4096 causal, mean 16.5, -2.8%).
-constexpr int kDkdvPersistMaxKv = 12;
+// across the query-tile loop in elementwise warps at the 96-register limit of an 18-warp CTA
+// (a few spilled bytes at D = 128), so per query tile it is a little slower than the
+// one-CTA-per-item kernel; with items taken from the work counter it wins up to a mean of
+// kDkdvPersistMaxKv query tiles per key tile (measured: B8 H32 L4096 causal, mean 16.5, 1.534
+// against 1.597 ms at D = 128 and 1.092 against 1.190 ms at D = 64; B1 H16 L16384 D64 causal,
+// mean 64.5, 0.991 against 0.987 ms).
+constexpr int kDkdvPersistMaxKv = 32;
 __host__ __device__ __forceinline__ int dkdv_grid(int Lq, int Lk, int BH, bool causal,
                                                   int n_sm) {
     const int n_q = (Lq + 127) / 128, n_k = (Lk + 127) / 128;
