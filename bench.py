@@ -514,7 +514,7 @@ def _time_config(w, dev, peaks, dropout_p=0.0):
             st = fa.fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                               do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
                               dv.data_ptr(), ws.data_ptr(), ws_bytes, [contig] * 8, B, H, L, L,
-                              D, w.scale, int(w.causal), dropout_p, 1234, dt, sh)
+                              D, w.scale, int(w.causal), dropout_p, 1234, 1, dt, sh)
         else:
             st = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                            do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
