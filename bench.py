@@ -443,6 +443,7 @@ def run_ours(args, w):
         "bwd_frac_of_peak": round(bwd_tf / peak_tf, 4),
         "peak_tflops": peak_tf, "peak_hbm_gbs": peak_bw,
         "kernels": kernels,
+        "step_stats": _step_stats(kev, K),
         "roofline": roofline,
         "gpu_launches": int(reduce_sum(launches, dev)),
         "clocks": clocks,
@@ -461,6 +462,18 @@ def run_ours(args, w):
 
 
 L2_BYTES = 129 * 2**20  # GB300 L2
+
+
+def _step_stats(kev, steps):
+    """Mean and median over the timed steps of the forward (its call's events) and of the
+    backward (the sum of its three kernels' events in the same step), in ms."""
+    fwd = [kev[i][0].elapsed_time(kev[i][1]) for i in range(steps)]
+    bwd = [sum(kev[i][2 * j].elapsed_time(kev[i][2 * j + 1]) for j in range(1, 4))
+           for i in range(steps)]
+    return {"fwd_ms_mean": round(statistics.mean(fwd), 4),
+            "fwd_ms_median": round(statistics.median(fwd), 4),
+            "bwd_ms_mean": round(statistics.mean(bwd), 4),
+            "bwd_ms_median": round(statistics.median(bwd), 4)}
 
 
 def _time_config(w, dev, peaks, dropout_p=0.0):
@@ -571,6 +584,7 @@ def _time_config(w, dev, peaks, dropout_p=0.0):
         "fwd_hbm_gbs": round(pm.bytes_fwd(B, H, L, D) / (fwd_ms * 1e-3) / 1e9, 1),
         "bwd_hbm_gbs": round(pm.bytes_bwd(B, H, L, D) / (bwd_ms * 1e-3) / 1e9, 1),
         "kernels_ms": {n: round(kern_ms[n], 4) for n in KERNELS},
+        "step_stats": _step_stats(kev, steps),
         "dominant": {"kernel": dom, "tflops": round(dom_tf, 2),
                      "frac": round(dom_tf / peak_tf, 4)},
         "clocks": clocks,
