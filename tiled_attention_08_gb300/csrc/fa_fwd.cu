@@ -78,7 +78,10 @@ struct FwdCfg {
     static constexpr int kOffQ = 0;                            // slot s: Q_A, then Q_B
     static constexpr int kOffK = kOffQ + kQSlots * 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kKStages * kTileBytes;
-    static constexpr int kSmemBytes = kOffV + kVStages * kTileBytes + 1024;  // + alignment slack
+    // One 4 KB buffer per softmax warp for the O read-out (32 rows x 64 columns, 16-bit).
+    static constexpr int kStageBytes = 32 * 64 * 2;
+    static constexpr int kOffStage = kOffV + kVStages * kTileBytes;
+    static constexpr int kSmemBytes = kOffStage + 8 * kStageBytes + 1024;  // + alignment slack
     static constexpr int kGroupWarps = 4;                      // softmax warps per query tile
     static constexpr int kGroupThreads = kGroupWarps * 32;
     static constexpr int kSoftmaxWarps = 2 * kGroupWarps;
@@ -117,6 +120,47 @@ __device__ __forceinline__ bool fwd_item(const FwdParams& p, int round, FwdItem&
     it.n_kv_b = has_b ? q_tile_kv(it.q_b, p.Lq, p.Lk, CAUSAL) : 0;
     it.n_kv = it.n_kv_b > it.n_kv_a ? it.n_kv_b : it.n_kv_a;  // n_kv_a <= n_kv_b
     return true;
+}
+
+// The O rows of a warp (lane = query row, NCOLS fp32 TMEM columns from taddr) times `mul`, as
+// 16-bit values into rows row0 .. row0 + 31 of one head (row r at dst0 + r * row_bytes; rows
+// at or past n_rows are not written).  A row per lane would make every 16-byte store of the
+// warp touch 32 cache lines; instead each 64-column chunk goes through the warp's 4 KB buffer
+// at shared address `stage` (row r at 128 r, its 16-byte units XORed by r % 8, so that the
+// row-wise writes and the column-wise reads are free of bank conflicts) and leaves as 4 rows
+// of 128 contiguous bytes per store instruction.
+template <bool BF16, int NCOLS>
+__device__ __forceinline__ void tmem_rows_to_global_staged(uint32_t taddr, uint32_t stage,
+                                                           uint8_t* dst0, size_t row_bytes,
+                                                           int n_rows, float mul, int lane) {
+    static_assert(NCOLS % 64 == 0, "64-column chunks");
+#pragma unroll
+    for (int c = 0; c < NCOLS / 64; ++c) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {  // 32 columns at a time
+            uint32_t r[32];
+            tmem_ld32(taddr + 64 * c + 32 * hf, r);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int u = 4 * hf + v;
+                uint4 w;
+                w.x = pack2<BF16>(__uint_as_float(r[8 * v + 0]) * mul, __uint_as_float(r[8 * v + 1]) * mul);
+                w.y = pack2<BF16>(__uint_as_float(r[8 * v + 2]) * mul, __uint_as_float(r[8 * v + 3]) * mul);
+                w.z = pack2<BF16>(__uint_as_float(r[8 * v + 4]) * mul, __uint_as_float(r[8 * v + 5]) * mul);
+                w.w = pack2<BF16>(__uint_as_float(r[8 * v + 6]) * mul, __uint_as_float(r[8 * v + 7]) * mul);
+                sts_u32x4(stage + lane * 128 + ((u ^ (lane & 7)) << 4), w);
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int rr = 4 * k + (lane >> 3), uu = lane & 7;
+            const uint4 w = lds_u32x4(stage + rr * 128 + ((uu ^ (rr & 7)) << 4));
+            if (rr < n_rows)
+                *reinterpret_cast<uint4*>(dst0 + (size_t)rr * row_bytes + c * 128 + uu * 16) = w;
+        }
+        __syncwarp();
+    }
 }
 
 // DROP: dropout on P (p.drop): the PV operand carries the kept entries only, the running sum
@@ -455,11 +499,16 @@ __global__ void __launch_bounds__(FwdCfg<D, BF16, CAUSAL>::kThreads, 1)
             if (valid)
                 p.lse[(size_t)it.bh * p.Lq + q_row] =
                     l_sum > 0.0f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
-            uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) + row_offset(p.so, it.bh, p.H, q_row);
+            // This warp's 32 rows start at q_row - lane; those at or past Lq are not written.
+            const int row0 = q_row - lane;
+            uint8_t* orow0 = reinterpret_cast<uint8_t*>(p.o) + row_offset(p.so, it.bh, p.H, row0);
+            const size_t row_bytes = (size_t)p.so.l * 2u;
             // The read-out finishes (tcgen05.ld waits) before this group publishes P_t0 of the
             // next item, which is what lets PV_t0 overwrite O_t.
             const float inv_l = l_sum > 0.0f ? (DROP ? p.drop.keep_scale : 1.0f) / l_sum : 0.0f;
-            tmem_row_to_global<BF16, D>(o_addr, orow, inv_l, valid);
+            tmem_rows_to_global_staged<BF16, D>(
+                o_addr, smem_u32(smem + C::kOffStage + warp * C::kStageBytes), orow0, row_bytes,
+                p.Lq - row0, inv_l, lane);
             ps += n_mine;
             ++n_done;
         }

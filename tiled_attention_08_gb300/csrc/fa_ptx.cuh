@@ -380,6 +380,21 @@ __device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
     return v;
 }
 
+// 16 bytes to / from shared memory at a 16-byte aligned shared address.
+__device__ __forceinline__ void sts_u32x4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ uint4 lds_u32x4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------------------------------
 // Counter-based random numbers for dropout: Philox-4x32 with 10 rounds (Salmon, Moraes, Dror,
 // Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011), from that definition: each
