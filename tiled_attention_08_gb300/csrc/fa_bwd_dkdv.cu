@@ -614,16 +614,17 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL, DQA>::kThreads, 1)
             if (lane == 0) record_timeout(p.status, abort_v);
         } else {
             tc_fence_after_sync();
-            const bool valid = key < p.Lk;
+            // The warp's 32 key rows from key - lane, stored coalesced across the warp.
+            const int key0 = key - lane;
             const size_t coff = (size_t)part * C::kOutCols * 2;
-            tmem_row_to_global<BF16, C::kOutCols>(
+            tmem_rows_to_global_xpose<BF16, C::kOutCols>(
                 tmem + lane_off + C::kTmDV + part * C::kOutCols,
-                reinterpret_cast<uint8_t*>(p.dv) + row_offset(p.sdv, bh, p.H, key) + coff,
-                DROP ? p.drop.keep_scale : 1.0f, valid);
-            tmem_row_to_global<BF16, C::kOutCols>(
+                reinterpret_cast<uint8_t*>(p.dv) + row_offset(p.sdv, bh, p.H, key0) + coff,
+                (size_t)p.sdv.l * 2u, p.Lk - key0, DROP ? p.drop.keep_scale : 1.0f, lane);
+            tmem_rows_to_global_xpose<BF16, C::kOutCols>(
                 tmem + lane_off + C::kTmDK + part * C::kOutCols,
-                reinterpret_cast<uint8_t*>(p.dk) + row_offset(p.sdk, bh, p.H, key) + coff, p.scale,
-                valid);
+                reinterpret_cast<uint8_t*>(p.dk) + row_offset(p.sdk, bh, p.H, key0) + coff,
+                (size_t)p.sdk.l * 2u, p.Lk - key0, p.scale, lane);
         }
     }
 
@@ -1041,16 +1042,17 @@ __global__ void __launch_bounds__(DkdvCfg<D, BF16, CAUSAL>::kThreads, 1)
             tc_fence_after_sync();
             // tcgen05.ld waits for its data: the read-out is complete before this warp publishes
             // P^T / dS^T of the next item, which is what lets dK / dV of that item start.
-            const bool valid = key < p.Lk;
+            // The warp's 32 key rows from key - lane, stored coalesced across the warp.
+            const int key0 = key - lane;
             const size_t coff = (size_t)part * C::kOutCols * 2;
-            tmem_row_to_global<BF16, C::kOutCols>(
+            tmem_rows_to_global_xpose<BF16, C::kOutCols>(
                 tmem + lane_off + C::kTmDV + part * C::kOutCols,
-                reinterpret_cast<uint8_t*>(p.dv) + row_offset(p.sdv, it.bh, p.H, key) + coff, 1.0f,
-                valid);
-            tmem_row_to_global<BF16, C::kOutCols>(
+                reinterpret_cast<uint8_t*>(p.dv) + row_offset(p.sdv, it.bh, p.H, key0) + coff,
+                (size_t)p.sdv.l * 2u, p.Lk - key0, 1.0f, lane);
+            tmem_rows_to_global_xpose<BF16, C::kOutCols>(
                 tmem + lane_off + C::kTmDK + part * C::kOutCols,
-                reinterpret_cast<uint8_t*>(p.dk) + row_offset(p.sdk, it.bh, p.H, key) + coff,
-                p.scale, valid);
+                reinterpret_cast<uint8_t*>(p.dk) + row_offset(p.sdk, it.bh, p.H, key0) + coff,
+                (size_t)p.sdk.l * 2u, p.Lk - key0, p.scale, lane);
             u = u_end;
         }
         if (!ok && lane == 0) record_timeout(p.status, abort_v);

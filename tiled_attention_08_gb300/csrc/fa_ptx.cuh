@@ -550,6 +550,58 @@ __device__ __forceinline__ void tmem_row_to_global(uint32_t taddr, uint8_t* dst,
     }
 }
 
+// The same read-out for a whole warp with coalesced stores.  Lane l holds row l of the warp's
+// 32 (its TMEM lane); its NCOLS columns (16, 32 or 64), scaled and rounded to 16 bits, are
+// U = NCOLS/8 16-byte units bound for dst0 + l * row_bytes.  A store per lane would touch 32
+// rows (32 cache lines) per instruction.  Instead the warp transposes the units in groups of U
+// lanes (a butterfly of xor shuffles), after which lane g*U + i holds unit i of rows
+// g*U .. g*U+U-1, and each of U store instructions writes U contiguous units of one row per
+// group: 32/U rows per instruction.  Rows at or past n_rows are not written.
+template <bool BF16, int NCOLS>
+__device__ __forceinline__ void tmem_rows_to_global_xpose(uint32_t taddr, uint8_t* dst0,
+                                                          size_t row_bytes, int n_rows,
+                                                          float mul, int lane) {
+    static_assert(NCOLS == 16 || NCOLS == 32 || NCOLS == 64, "16, 32 or 64 columns");
+    constexpr int U = NCOLS / 8;  // 16-byte units per row slice
+    uint32_t m[U][4];             // m[e]: unit e of this row (before), unit i of row g*U+e (after)
+#pragma unroll
+    for (int c = 0; c < NCOLS; c += 16) {
+        uint32_t r[16];
+        tmem_ld16(taddr + c, r);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            m[c / 8 + k / 4][k % 4] =
+                pack2<BF16>(__uint_as_float(r[2 * k]) * mul, __uint_as_float(r[2 * k + 1]) * mul);
+    }
+    // Stage s swaps, between lanes l and l^s, the units whose index differs from the lane's in
+    // bit s: afterwards unit e of lane l came from lane (l & ~(U-1)) + e, unit index l % U.
+#pragma unroll
+    for (int s = U / 2; s >= 1; s /= 2) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int e = 0; e < U; ++e) {
+            if (e & s) continue;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t send = upper ? m[e][k] : m[e | s][k];
+                const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, s);
+                if (upper)
+                    m[e][k] = recv;
+                else
+                    m[e | s][k] = recv;
+            }
+        }
+    }
+    const int g = lane / U, i = lane % U;
+#pragma unroll
+    for (int e = 0; e < U; ++e) {
+        const int r = g * U + e;
+        if (r < n_rows)
+            *reinterpret_cast<uint4*>(dst0 + (size_t)r * row_bytes + i * 16) =
+                make_uint4(m[e][0], m[e][1], m[e][2], m[e][3]);
+    }
+}
+
 // Multiplies NCOLS fp32 TMEM columns of this thread's lane by `mul` in place.
 template <int NCOLS>
 __device__ __forceinline__ void tmem_row_scale(uint32_t taddr, float mul) {
