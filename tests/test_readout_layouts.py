@@ -5,7 +5,7 @@
   each unit pair (e, e|s) with bit s clear in e, the lane with bit s set sends unit e and keeps
   the received one there, the other lane sends unit e|s) must leave lane g*U + i holding unit i
   of rows g*U + e in slot e, so that store e writes U contiguous units of one row per group.
-* tmem_rows_to_global_staged (csrc/fa_fwd.cu, used by the forward): row r of a warp's 4 KB
+* tmem_rows_to_global_staged (csrc/fa_ptx.cuh, used by both forwards): row r of a warp's 4 KB
   buffer at 128 r, 16-byte unit u at ((u ^ (r % 8)) * 16).  Lane = row writes unit u (for each
   u); in the read-back store k lane l reads unit l % 8 of row 4k + l / 8.  Both access patterns
   must be free of shared-memory bank conflicts (a 16-byte-per-lane access is served in four

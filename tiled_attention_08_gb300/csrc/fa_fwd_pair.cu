@@ -55,7 +55,10 @@ struct PairCfg {
     static constexpr int kOffQ = 0;                       // Q_A, then Q_B (this CTA's rows)
     static constexpr int kOffK = 2 * kQBytes;
     static constexpr int kOffV = kOffK + kKStages * kKHalf;
-    static constexpr int kSmemBytes = kOffV + kVStages * kVHalf + 1024;  // + alignment slack
+    // One 4 KB buffer per softmax warp for the O read-out (32 rows x 64 columns, 16-bit).
+    static constexpr int kStageBytes = 32 * 64 * 2;
+    static constexpr int kOffStage = kOffV + kVStages * kVHalf;
+    static constexpr int kSmemBytes = kOffStage + 8 * kStageBytes + 1024;  // + alignment slack
     static constexpr int kGroupWarps = 4;
     static constexpr int kGroupThreads = kGroupWarps * 32;
     static constexpr int kSoftmaxWarps = 2 * kGroupWarps;
@@ -470,10 +473,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BF16, CAUSAL
                 if (valid)
                     p.lse[(size_t)it.bh * p.Lq + q_row] =
                         l_sum > 0.0f ? (m_ref + log2f(l_sum)) * kLn2Pair : -INFINITY;
-                uint8_t* orow =
-                    reinterpret_cast<uint8_t*>(p.o) + row_offset(p.so, it.bh, p.H, q_row);
-                tmem_row_to_global<BF16, D>(o_addr, orow, l_sum > 0.0f ? 1.0f / l_sum : 0.0f,
-                                            valid);
+                // This warp's 32 rows start at q_row - lane; those at or past Lq are not
+                // written.  Coalesced through the warp's staging buffer.
+                const int row0 = q_row - lane;
+                uint8_t* orow0 =
+                    reinterpret_cast<uint8_t*>(p.o) + row_offset(p.so, it.bh, p.H, row0);
+                tmem_rows_to_global_staged<BF16, D>(
+                    o_addr, smem_u32(smem + C::kOffStage + warp * C::kStageBytes), orow0,
+                    (size_t)p.so.l * 2u, p.Lq - row0, l_sum > 0.0f ? 1.0f / l_sum : 0.0f, lane);
             }
         }
         if (!ok && lane == 0) record_timeout(p.status, abort_v);

@@ -550,6 +550,47 @@ __device__ __forceinline__ void tmem_row_to_global(uint32_t taddr, uint8_t* dst,
     }
 }
 
+// The rows of a warp (lane = row, NCOLS fp32 TMEM columns from taddr, NCOLS a multiple of 64)
+// times `mul`, as 16-bit values into rows 0 .. 31 at dst0 + r * row_bytes (rows at or past
+// n_rows are not written).  A row per lane would make every 16-byte store of the
+// warp touch 32 cache lines; instead each 64-column chunk goes through the warp's 4 KB buffer
+// at shared address `stage` (row r at 128 r, its 16-byte units XORed by r % 8, so that the
+// row-wise writes and the column-wise reads are free of bank conflicts) and leaves as 4 rows
+// of 128 contiguous bytes per store instruction.
+template <bool BF16, int NCOLS>
+__device__ __forceinline__ void tmem_rows_to_global_staged(uint32_t taddr, uint32_t stage,
+                                                           uint8_t* dst0, size_t row_bytes,
+                                                           int n_rows, float mul, int lane) {
+    static_assert(NCOLS % 64 == 0, "64-column chunks");
+#pragma unroll
+    for (int c = 0; c < NCOLS / 64; ++c) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {  // 32 columns at a time
+            uint32_t r[32];
+            tmem_ld32(taddr + 64 * c + 32 * hf, r);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int u = 4 * hf + v;
+                uint4 w;
+                w.x = pack2<BF16>(__uint_as_float(r[8 * v + 0]) * mul, __uint_as_float(r[8 * v + 1]) * mul);
+                w.y = pack2<BF16>(__uint_as_float(r[8 * v + 2]) * mul, __uint_as_float(r[8 * v + 3]) * mul);
+                w.z = pack2<BF16>(__uint_as_float(r[8 * v + 4]) * mul, __uint_as_float(r[8 * v + 5]) * mul);
+                w.w = pack2<BF16>(__uint_as_float(r[8 * v + 6]) * mul, __uint_as_float(r[8 * v + 7]) * mul);
+                sts_u32x4(stage + lane * 128 + ((u ^ (lane & 7)) << 4), w);
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int rr = 4 * k + (lane >> 3), uu = lane & 7;
+            const uint4 w = lds_u32x4(stage + rr * 128 + ((uu ^ (rr & 7)) << 4));
+            if (rr < n_rows)
+                *reinterpret_cast<uint4*>(dst0 + (size_t)rr * row_bytes + c * 128 + uu * 16) = w;
+        }
+        __syncwarp();
+    }
+}
+
 // The same read-out for a whole warp with coalesced stores.  Lane l holds row l of the warp's
 // 32 (its TMEM lane); its NCOLS columns (16, 32 or 64), scaled and rounded to 16 bits, are
 // U = NCOLS/8 16-byte units bound for dst0 + l * row_bytes.  A store per lane would touch 32
